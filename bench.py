@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective KV-cache refresh (packed, layer-major) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama8b]
+
+One step = one whole refresh: kvr_select (upload and pack the 282 selected
+positions, gather their embedding rows) + all 32 layers through kvr_refresh
++ the metadata commit, on the Llama-3-8B-shaped workload (N = 7680 after a
+512-token deletion, 5 % of the 5632-token retained suffix in units of 32-64
+tokens).  Weights (14 GB) and cache stay resident; every step streams all
+weights, far more than the 129 MB L2, so no explicit flush is needed.
+
+Prints ONE JSON line (rank 0).  With --gpus N > 1 (torchrun) every rank runs
+an independent replica of the same refresh (one sequence does not shard
+without tensor parallelism); `value` is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "refreshed tokens/sec & refresh latency/edit; HBM and tensor-pipe % of peak"
+UNIT = "tokens/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "selective_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_class, sha):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    if it was taken on the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        m = re.match(r"\s*(\S+)\s+sha=(\S+)\s+dram_bytes_per_launch=(\d+)", line)
+        if m and m.group(1) == kernel_class and m.group(2) == sha:
+            return int(m.group(3))
+    return None
+
+
+# per-kernel algorithmic work at the workload (measurement)
+def algorithmic(shape, R, M_pairs_per_head, u_max):
+    """Algorithmic FLOPs and bytes per launch of each kernel class for R packed
+    rows: a projection reads its weights once and the rows once and writes
+    fp32 partials; attention reads each K/V row up to the last selected
+    position once per K/V head, reads Q and writes O, and spends
+    4 d_h FLOPs per causal query-key pair per query head."""
+    d, Hq, Hkv, dh, F = shape.d_model, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim
+    qkv = (Hq + 2 * Hkv) * dh
+
+    def gemm(n_out, K):
+        return dict(flops=2.0 * R * n_out * K, bytes=2.0 * n_out * K + 2.0 * R * K + 4.0 * R * n_out)
+
+    return {
+        "gemm_qkv": gemm(qkv, d),
+        "gemm_o": gemm(d, Hq * dh),
+        "gemm_gate_up": gemm(2 * F, d),
+        "gemm_down": gemm(d, F),
+        "attention": dict(flops=4.0 * dh * Hq * M_pairs_per_head,
+                          bytes=2.0 * 2 * Hkv * dh * (u_max + 1) + 2.0 * 2 * R * Hq * dh),
+    }
+
+
+def source_files(kernel_class):
+    if kernel_class.startswith("gemm"):
+        return ["gemm.cu", "ptx.cuh"]
+    if kernel_class == "attention":
+        return sorted(f for f in os.listdir(os.path.join(ROOT, "selective_kv_cache_gb300", "csrc"))
+                      if f.startswith("attn") or f == "ptx.cuh")
+    return ["elementwise.cu"]
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from selective_kv_cache_gb300 import kvr, workloads as wl
+    from selective_kv_cache_gb300.harness import Setup
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    w = wl.WORKLOADS[args.workload]
+    s = Setup(w)
+    m = w.model
+    stream = torch.cuda.current_stream()
+
+    def step():
+        s.select(stream=stream)
+        s.refresh(stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    s.sync()
+
+    # ---- timed region: device-resident inputs
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local_rank) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    s.sync()
+    t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    rows = s.n_rows
+    value = rows * args.steps * world / (ms_total / 1e3)
+
+    # ---- per-kernel breakdown: the same K steps again with CUDA events around every launch
+    kvr.kvr_profile_read(s.handle)
+    kvr.kvr_profile_enable(s.handle, True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    prof = kvr.kvr_profile_read(s.handle)
+    kvr.kvr_profile_enable(s.handle, False)
+    launches_per_step = sum(n for n, _ in prof.values()) / args.steps
+
+    # ---- end to end through the C ABI with host buffers: token ids in, refreshed rows out
+    ids_host = s.ids.cpu().pin_memory()
+    out_host = torch.empty(s.hidden.shape, dtype=s.hidden.dtype).pin_memory()
+    h2d = ids_host.numel() * ids_host.element_size() + s.pos_host.nbytes + s.counts.nbytes
+    d2h = out_host.numel() * out_host.element_size()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.ids.copy_(ids_host, non_blocking=True)
+        step()
+        out_host.copy_(s.hidden, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    t = torch.tensor([e2e_s], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = rows * args.steps * world / float(t.item())
+
+    # ---- roofline of the dominant kernel
+    hbm, tf_burst, tf_sust, src = peaks()
+    per_kernel = {k: (n, v) for k, (n, v) in prof.items() if n}
+    dom = max(per_kernel, key=lambda k: per_kernel[k][1])
+    n_l, ms_l = per_kernel[dom]
+    avg_s = ms_l / n_l / 1e3
+    U = np.sort(np.concatenate(s.positions))
+    M = float(np.sum(U + 1))
+    work = algorithmic(m, rows, M, int(U.max()))
+    roof = None
+    if dom in work and work[dom].get("bytes"):
+        wk = work[dom]
+        t_hbm = wk["bytes"] / (hbm * 1e9)
+        t_tc = wk["flops"] / (tf_sust * 1e12)
+        if t_hbm >= t_tc:
+            ach = wk["bytes"] / avg_s / 1e9
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(ach / hbm, 4)}
+        else:
+            ach = wk["flops"] / avg_s / 1e12
+            roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tf_sust, "unit": "TFLOP/s",
+                    "frac": round(ach / tf_sust, 4)}
+        roof["kernel"] = dom
+        roof["peak_source"] = f"{src} ({'sustained bf16' if roof['bound'] == 'tensor' else 'copy'})"
+        roof["avg_launch_us"] = round(avg_s * 1e6, 2)
+        roof["traffic"] = ncu_traffic(dom, kernel_source_sha(source_files(dom)))
+    breakdown = {k: {"launches_per_step": n / args.steps, "us_per_step": round(v * 1e3 / args.steps, 1)}
+                 for k, (n, v) in per_kernel.items()}
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0 only)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(s, w)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random weights, "
+        "token ids, embeddings and stale cache)",
+        "config": {"workload": f"{w.name}: Llama-3-8B-shaped stack (32 L, d 4096, 32/8 heads x 128, FFN 14336, "
+                   f"RoPE theta 5e5), N={w.n_tokens}, suffix [{w.suffix_start},{w.n_tokens}), "
+                   f"{rows} refreshed positions in units of 32-64 (5 % budget)",
+                   "rows": rows, "n_tokens": w.n_tokens, "layers": m.n_layers,
+                   "refresh_latency_ms": round(ms_total / args.steps, 4),
+                   "per_layer_latency_us": round(ms_total / args.steps / m.n_layers * 1e3, 2),
+                   "l2": "no flush: each step streams 14 GB of weights (> 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline": roof,
+        "kernels": breakdown,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    s.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(s, w, reference_line=False):
+    """The float64 oracle as it stands, on one layer of the same refresh
+    (all rows), scaled to tokens/s of the whole L-layer refresh."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    def f64(t):
+        return t.detach().to("cpu", torch.float64).numpy()
+
+    spec = oracle.Spec.of(w.model)
+    U = oracle.sorted_positions(s.positions[0])
+    Wl = {k: f64(v) if v is not None else None for k, v in s.layers[0].items()}
+    K0 = f64(s.K[0, 0])
+    V0 = f64(s.V[0, 0])
+    ids = s.ids[0].cpu().numpy()
+    X = f64(s.embed[torch.from_numpy(ids[U].astype(np.int64)).to(s.embed.device)])
+    sel = np.zeros(w.capacity, bool)
+    sel[U] = True
+    loc, snk = oracle.effective_masks(s.local_mask[0], s.sink_mask[0], sel)
+    bias = w.alpha * loc + w.beta * snk
+    t0 = time.perf_counter()
+    oracle.layer_rows(spec, Wl, oracle.round_store(X, spec.dtype), K0, V0, U, bias)
+    dt = time.perf_counter() - t0
+    per_refresh = dt * w.model.n_layers
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": round(len(U) / per_refresh, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"layer 0 of {w.model.n_layers} for all {len(U)} rows in float64 numpy "
+                      f"({dt:.2f} s), scaled by {w.model.n_layers} layers"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    from selective_kv_cache_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    # the oracle needs only layer 0's weights and cache; generate them on the GPU if present
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    import dataclasses
+    w1 = dataclasses.replace(w, model=dataclasses.replace(w.model, n_layers=1))
+
+    class S:
+        pass
+
+    s = S()
+    s.layers = wl.make_layer_weights(w1, dev)
+    s.K, s.V = wl.make_random_cache(w1, dev)
+    s.embed = wl.make_embeddings(w1, dev)
+    s.ids = wl.make_token_ids(w1, dev)
+    s.positions = wl.make_positions(w1)
+    s.local_mask, s.sink_mask = wl.make_metadata(w1)
+    times = []
+    for i in range(args.warmup + args.steps):
+        c = cpu_baseline(s, w)
+        if i >= args.warmup:
+            times.append(c)
+    vals = [c["value"] for c in times]
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(282 / v * 1e3, 1) if v else None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} (same as the GPU arm)"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": times[0]["cores"], "kind": "oracle",
+                         "sample": times[0]["sample"] + "; median over steps"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * kvr.h -- C ABI of libkvr: selective KV-cache refresh on one GB300 GPU.
+ *
+ * After a context edit (a deleted span, a changed block seam, or an updated
+ * adapter), a chosen set of retained-suffix positions is recomputed layer by
+ * layer against a mixed cache of fresh and stale K/V.  Per layer, the rows of
+ * all selected positions are packed together, normalised, projected, rotated
+ * at their global positions, and their K/V rows are written back into the
+ * cache before any of them attends ("Budgeted KV-Cache Repair for Evolving
+ * Contexts", Sec. 13.2, Eq. 21).  Each packed query then attends causally
+ * over the whole cache, every key j <= g_i, fresh or stale (ibid. Eq. 22),
+ * with the per-key logit bias of operator F,
+ *     s_ij = <q_i, k_j>/sqrt(d_h) + alpha*1[type_j = local] + beta*1[j in S']
+ * ("kv-cross-attention-reuse", Sec. 6.4, Logit form), and finishes with the
+ * output projection, residual, RMSNorm and SwiGLU MLP.  After the last layer
+ * the refreshed positions become type global (ibid., physical repair mode).
+ *
+ * Conventions for every entry point:
+ *   - Plain C; every call returns a kvr_status; a thread-local message for
+ *     the last failure is available from kvr_last_error().
+ *   - "device" pointers are CUDA global-memory addresses on the current
+ *     device; "host" pointers are CPU memory.  The caller owns every buffer
+ *     passed in; the library owns only the kvr_cache object and the small
+ *     device buffers it allocates in kvr_create_cache (selection lists,
+ *     metadata bit masks, the execution plan, the rotary table, counters)
+ *     and frees them in kvr_destroy_cache.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work unless documented as synchronous;
+ *     kvr_sync_status() synchronises and reports device-side failures.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     failed validation enqueues nothing and leaves the cache unchanged.
+ *   - After any error the cache can still be destroyed.
+ */
+#ifndef KVR_H
+#define KVR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVR_OK = 0,
+    KVR_EINVAL = 1,       /* malformed argument: NULL, duplicate position, budget mismatch, bad shape */
+    KVR_ERANGE = 2,       /* index out of range: position outside the suffix, layer >= n_layers */
+    KVR_ENOMEM = 3,       /* a library-owned allocation failed */
+    KVR_ECUDA = 4,        /* a CUDA runtime call or launch failed */
+    KVR_ETIMEOUT = 5,     /* a device-side wait gave up (reported by kvr_sync_status) */
+    KVR_EDEVICE = 6,      /* a device-side check failed (reported by kvr_sync_status) */
+    KVR_ESTATE = 7,       /* call out of order, e.g. a refresh before any kvr_select */
+    KVR_EUNSUPPORTED = 8  /* shape or dtype this build does not implement */
+} kvr_status;
+
+typedef enum { KVR_F32 = 0, KVR_BF16 = 1 } kvr_dtype;
+
+/* kvr_create_cache flags */
+#define KVR_SINK_STATIC 0x1u   /* S' keeps its beta penalty after refresh */
+
+/* kvr_refresh_layer / kvr_refresh flags */
+#define KVR_COMMIT_META 0x1u   /* after this layer: type_t <- global (and t leaves S') for the selection */
+
+/* Model shape, copied by kvr_create_cache.  Dense pre-norm decoder with
+ * rotate-half RoPE (no scaling) and grouped-query attention; the shapes of
+ * Llama-3 and Qwen2.5 ("Budgeted KV-Cache Repair", Sec. 13.2: native dense
+ * Llama/Qwen with default fixed RoPE).
+ * Constraints: head_dim == 128 (bf16) or 64/128 (f32); n_q_heads a multiple
+ * of n_kv_heads; d_model, n_q_heads*head_dim and ffn_dim multiples of 64. */
+typedef struct {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t ffn_dim;
+    double  rope_theta;     /* inv_freq_i = theta^(-2i/head_dim) */
+    float   rms_eps;
+    int32_t dtype;          /* kvr_dtype of weights, cache and hidden rows */
+    int32_t has_qkv_bias;   /* Qwen2.5 shapes carry q/k/v biases */
+} kvr_model_desc;
+
+/* One layer's weights: caller-owned device pointers in the model dtype,
+ * nn.Linear layout (row = output feature, contiguous over input features).
+ * All pointers 16-byte aligned. */
+typedef struct {
+    const void* w_qkv;      /* [(Hq + 2*Hkv)*dh, d]: Q heads, then K heads, then V heads */
+    const void* b_qkv;      /* [(Hq + 2*Hkv)*dh] or NULL */
+    const void* w_o;        /* [d, Hq*dh] */
+    const void* w_gate_up;  /* [2*F, d]: rows 0..F-1 gate, rows F..2F-1 up */
+    const void* w_down;     /* [d, F] */
+    const void* norm1;      /* [d] RMSNorm weight before attention */
+    const void* norm2;      /* [d] RMSNorm weight before the MLP */
+} kvr_layer_weights;
+
+typedef struct kvr_cache kvr_cache;   /* opaque */
+
+/* ---------------------------------------------------------------------------
+ * kvr_create_cache -- bind a mixed cache L[t, l] = (K_t,l, V_t,l, m_t)
+ * ("kv-cross-attention-reuse", Sec. 6.2).
+ *
+ *   m           model shape (copied).
+ *   batch       independent sequences sharing the weights (>= 1).
+ *   capacity    cache rows per sequence (>= n_tokens).
+ *   k_base, v_base  device, caller-owned, model dtype, layout
+ *               [batch][n_layers][n_kv_heads][capacity][head_dim], 16-byte
+ *               aligned.  Rows outside a selection are never written.
+ *   n_tokens    valid cache length per sequence; keys >= n_tokens are never
+ *               read.
+ *   suffix_start  retained prefix [0, suffix_start) is valid; only
+ *               positions in [suffix_start, n_tokens) are selectable
+ *               ("Budgeted KV-Cache Repair", Sec. 7.1).
+ *   local_bits, sink_bits  host, nullable (= all zero), uint32 words
+ *               [batch][ceil(capacity/32)], bit b of word w = position 32w+b:
+ *               type_t = local, and t in S' (spurious sinks).
+ *   alpha, beta  logit bias of local keys and of S' keys (operator F).
+ *   flags       KVR_SINK_STATIC.
+ *   out         receives the handle.
+ * Synchronous with respect to `stream` for the metadata upload.
+ * Errors: EINVAL (NULL, bad shape), EUNSUPPORTED, ENOMEM, ECUDA.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capacity,
+                            void* k_base, void* v_base, int32_t n_tokens, int32_t suffix_start,
+                            const uint32_t* local_bits, const uint32_t* sink_bits,
+                            float alpha, float beta, uint32_t flags, void* stream,
+                            kvr_cache** out);
+
+/* Free the library-owned buffers of `c` (never the caller's). NULL is a no-op.
+ * Synchronises the device first so no enqueued work still uses them. */
+kvr_status kvr_destroy_cache(kvr_cache* c);
+
+/* ---------------------------------------------------------------------------
+ * kvr_select -- fix the support of one refresh and pack its rows.
+ * ("Budgeted KV-Cache Repair", Sec. 7.1 Eq. 3 exact budget; Sec. 3.2 and
+ * Algorithm 1: sort the selected positions and coalesce adjacent ones into
+ * execution intervals; Sec. 13.2: gather the selected rows once into a
+ * compact B-row hidden buffer; Eqs. 23-24 reusable per-query-tile plan.)
+ *
+ *   positions   host int32, zero-based positions in any order, sequence-major:
+ *               counts[0] positions of sequence 0, then sequence 1, ...
+ *   counts      host int32 [batch]; 0 is allowed.
+ *   budget_percent  -1 skips the check; otherwise each count must equal
+ *               min(S, ceil(S*b/100)), S = n_tokens - suffix_start.
+ *   Row source (exactly one):
+ *     token_ids + embed_table: device int32 [batch][capacity] token ids and
+ *               device [vocab][d] embedding table (model dtype); row r gets
+ *               embed_table[token_ids[seq][u_r]]; vocab = rows of embed_table (a
+               token id outside [0, vocab) is reported as EDEVICE by
+               kvr_sync_status and its row is left unwritten).
+ *     hidden_src: device [batch][capacity][d] per-position layer-0 inputs.
+ *   hidden_out  device [sum(counts)][d] (model dtype), rows in sorted
+ *               position order, sequence-major.
+ *   n_rows_out, n_intervals_out  host, nullable: total rows and intervals.
+ * Host validation (before any launch): every position in
+ * [suffix_start, n_tokens) else ERANGE; no duplicates within a sequence
+ * else EINVAL; budget else EINVAL.  The device then builds the sorted list
+ * U, intervals, the selected / effective-local / effective-sink bit masks
+ * and the plan, and gathers the rows.  Replaces any previous selection.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* counts,
+                      int32_t budget_percent, const int32_t* token_ids, const void* embed_table,
+                      int32_t vocab, const void* hidden_src, void* hidden_out, int32_t* n_rows_out,
+                      int32_t* n_intervals_out, void* stream);
+
+/* Bytes of workspace kvr_refresh_layer / kvr_refresh / kvr_attend need for up
+ * to `max_rows` packed rows (0 = the current selection). */
+size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows);
+
+/* ---------------------------------------------------------------------------
+ * kvr_refresh_layer -- one layer of the packed refresh over the current
+ * selection ("Budgeted KV-Cache Repair", Sec. 13.2, Eqs. 21-22):
+ *   xn = RMSNorm(x); [q|k|v] = xn W_qkv^T (+ b); RoPE(q, k) at u_r;
+ *   K_l[u_r] <- k, V_l[u_r] <- v for every row r (before any attention);
+ *   o_r = softmax_j<=u_r(q_r k_j/sqrt(d_h) + alpha*loc_j + beta*snk_j) V_j,
+ *     loc_j = local_j & !selected_j, snk_j = sink_j & !selected_j (or sink_j
+ *     under KVR_SINK_STATIC): a selected key is fresh whenever it is read;
+ *   h = x + o W_o^T; x' = h + (silu(hn W_g^T) * (hn W_u^T)) W_d^T,
+ *     hn = RMSNorm(h).
+ *   layer       [0, n_layers) else ERANGE.
+ *   w           this layer's weights (host struct of device pointers).
+ *   hidden_inout  device [rows][d] model dtype, from kvr_select; updated.
+ *   workspace   device, >= kvr_workspace_bytes(c, 0) bytes, 256-byte aligned.
+ *   flags       KVR_COMMIT_META: after the layer, clear local (and sink unless
+ *               static) for the selected positions.
+ * Errors: ESTATE (no selection), ERANGE, EINVAL (NULL / small workspace),
+ * ECUDA.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_refresh_layer(kvr_cache* c, int32_t layer, const kvr_layer_weights* w,
+                             void* hidden_inout, void* workspace, size_t ws_bytes,
+                             uint32_t flags, void* stream);
+
+/* Layers [layer_begin, layer_end) in order, then the metadata commit when
+ * flags has KVR_COMMIT_META.  `w` is a host array indexed by layer
+ * (w[layer_begin] .. w[layer_end-1] are read).  Same errors as above. */
+kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_begin,
+                       int32_t layer_end, void* hidden_inout, void* workspace, size_t ws_bytes,
+                       uint32_t flags, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvr_attend -- inference mode of operator F ("kv-cross-attention-reuse",
+ * Sec. 6.4): attention only, no write-back, with the stored correction masks
+ * (type_j = local, j in S') as they are now.
+ *   q    device [rows][n_q_heads][head_dim], rotated, model dtype; row r is
+ *        the query at position u_r of the current selection.
+ *   out  device [rows][n_q_heads*head_dim], model dtype.
+ *   workspace as for kvr_refresh_layer.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream` and report device-side failures recorded since the
+ * last call (ETIMEOUT / EDEVICE), clearing them. */
+kvr_status kvr_sync_status(kvr_cache* c, void* stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* kvr_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Inspection (synchronous; copies device state to host buffers).
+ * kvr_read_selection: for sequence `seq` of the current selection:
+ *   U        int32 [count]           sorted positions
+ *   iv       int32 [n_intervals][2]  half-open intervals [a, b)
+ *   sel, eloc, esnk  uint32 [ceil(capacity/32)]: selected, effective local,
+ *            effective sink bit masks
+ *   plan     int32 [n_tiles][6] (row0, nrows, u_min, u_max, n_full, n_total)
+ *            over the attention kernel's query tiles of rows_per_tile rows and
+ *            keys_per_tile keys; n_tiles/rows_per_tile/keys_per_tile returned.
+ * Any output pointer may be NULL; caps bound what is written.
+ * kvr_read_meta: local and sink masks [batch][ceil(capacity/32)].
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_read_selection(kvr_cache* c, int32_t seq, int32_t* U, int32_t u_cap, int32_t* iv,
+                              int32_t iv_cap, uint32_t* sel, uint32_t* eloc, uint32_t* esnk,
+                              int32_t* plan, int32_t plan_cap, int32_t* n_tiles,
+                              int32_t* rows_per_tile, int32_t* keys_per_tile);
+kvr_status kvr_read_meta(kvr_cache* c, uint32_t* local_bits, uint32_t* sink_bits);
+
+/* ---------------------------------------------------------------------------
+ * Per-kernel timing.  When enabled, every launch of a library kernel on the
+ * call's stream is bracketed by CUDA events; kvr_profile_read returns, per
+ * kernel class (KVR_K_* below), the number of launches and the summed device
+ * time in milliseconds since the last read (synchronous), and resets them.
+ * ------------------------------------------------------------------------- */
+enum {
+    KVR_K_SELECT = 0, KVR_K_GATHER, KVR_K_RMSNORM, KVR_K_GEMM_QKV, KVR_K_EPI_QKV,
+    KVR_K_ATTN, KVR_K_GEMM_O, KVR_K_EPI_O, KVR_K_GEMM_GATEUP, KVR_K_EPI_GATEUP,
+    KVR_K_GEMM_DOWN, KVR_K_EPI_DOWN, KVR_K_COMMIT, KVR_K_COUNT
+};
+kvr_status kvr_profile_enable(kvr_cache* c, int32_t enable);
+kvr_status kvr_profile_read(kvr_cache* c, double* ms, int64_t* launches, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVR_H */

@@ -1,0 +1,874 @@
+// api.cu -- the C ABI (kvr.h): host-side validation, library-owned state,
+// and the per-layer launch sequence of the packed refresh.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kvr_internal.h"
+
+namespace kvr {
+
+namespace {
+thread_local std::string g_err;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode(std::string* why) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) {
+        if (why) *why = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int dtype_size(int dtype) { return dtype == KVR_BF16 ? 2 : 4; }
+
+struct WsLayout {
+    size_t xn, q, o, h, hn, act, part, total;
+};
+
+struct Gemms {
+    GemmPlan qkv, o, gu, down;
+};
+
+Gemms plan_all(const kvr_model_desc& m, int R) {
+    Gemms g;
+    const int hqd = m.n_q_heads * m.head_dim;
+    g.qkv = plan_gemm(m.dtype, (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, m.d_model, R);
+    g.o = plan_gemm(m.dtype, m.d_model, hqd, R);
+    g.gu = plan_gemm(m.dtype, 2 * m.ffn_dim, m.d_model, R);
+    g.down = plan_gemm(m.dtype, m.d_model, m.ffn_dim, R);
+    return g;
+}
+
+size_t part_bytes(const kvr_model_desc& m, int R) {
+    const Gemms g = plan_all(m, R);
+    return std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
+                    std::max(gemm_partial_bytes(g.gu), gemm_partial_bytes(g.down)));
+}
+
+WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
+    const size_t es = dtype_size(m.dtype);
+    const size_t hqd = (size_t)m.n_q_heads * m.head_dim;
+    WsLayout L{};
+    size_t off = 0;
+    L.xn = off; off = align256(off + (size_t)R * m.d_model * es);
+    L.q = off; off = align256(off + (size_t)R * hqd * es);
+    L.o = off; off = align256(off + (size_t)R * hqd * es);
+    L.h = off; off = align256(off + (size_t)R * m.d_model * 4);
+    L.hn = off; off = align256(off + (size_t)R * m.d_model * es);
+    L.act = off; off = align256(off + (size_t)R * m.ffn_dim * es);
+    L.part = off; off = align256(off + part);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------- profiling
+cudaEvent_t take_event(kvr_cache* c) {
+    if (!c->ev_pool.empty()) {
+        cudaEvent_t e = c->ev_pool.back();
+        c->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct Prof {
+    kvr_cache* c;
+    int kind;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr;
+    Prof(kvr_cache* c_, int k, cudaStream_t s_) : c(c_), kind(k), s(s_) {
+        if (c->profiling) {
+            a = take_event(c);
+            cudaEventRecord(a, s);
+        }
+    }
+    ~Prof() {
+        if (a) {
+            cudaEvent_t b = take_event(c);
+            cudaEventRecord(b, s);
+            c->prof.push_back({kind, a, b});
+        }
+    }
+};
+
+#define KVR_CHECK_LAUNCH(expr, what)                            \
+    do {                                                        \
+        cudaError_t e_ = (expr);                                \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what);      \
+    } while (0)
+
+kvr_status validate_desc(const kvr_model_desc* m) {
+    if (!m) {
+        set_error("model descriptor is NULL");
+        return KVR_EINVAL;
+    }
+    if (m->n_layers < 1 || m->d_model < 64 || m->n_q_heads < 1 || m->n_kv_heads < 1 || m->ffn_dim < 64 ||
+        m->n_q_heads % m->n_kv_heads != 0) {
+        set_error("model shape is malformed");
+        return KVR_EINVAL;
+    }
+    if (m->dtype != KVR_BF16 && m->dtype != KVR_F32) {
+        set_error("dtype must be KVR_F32 or KVR_BF16");
+        return KVR_EUNSUPPORTED;
+    }
+    if (m->d_model % 64 || m->ffn_dim % 64 || (m->n_q_heads * m->head_dim) % 64) {
+        set_error("d_model, ffn_dim and n_q_heads*head_dim must be multiples of 64");
+        return KVR_EUNSUPPORTED;
+    }
+    if (m->dtype == KVR_BF16) {
+        if (m->head_dim != 128 || m->d_model % 128) {
+            set_error("bf16 models need head_dim 128 and d_model a multiple of 128");
+            return KVR_EUNSUPPORTED;
+        }
+    } else if (m->head_dim != 64 && m->head_dim != 128) {
+        set_error("fp32 models need head_dim 64 or 128");
+        return KVR_EUNSUPPORTED;
+    }
+    if (!(m->rope_theta > 0.0) || !(m->rms_eps >= 0.f)) {
+        set_error("rope_theta must be > 0 and rms_eps >= 0");
+        return KVR_EINVAL;
+    }
+    return KVR_OK;
+}
+
+void free_cache(kvr_cache* c) {
+    cudaFree(c->d_local);
+    cudaFree(c->d_sink);
+    cudaFree(c->d_sel);
+    cudaFree(c->d_eloc);
+    cudaFree(c->d_esnk);
+    cudaFree(c->d_seqinfo);  // d_raw lives in the same allocation
+    cudaFree(c->d_U);
+    cudaFree(c->d_row_seq);
+    cudaFree(c->d_iv);
+    cudaFree(c->d_plan);
+    cudaFree(c->d_rope);
+    cudaFree(c->d_err);
+    if (c->h_stage) cudaFreeHost(c->h_stage);
+    if (c->stage_ev) cudaEventDestroy(c->stage_ev);
+    for (auto& r : c->prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    for (auto e : c->ev_pool) cudaEventDestroy(e);
+    delete c;
+}
+
+kvr_status check_layer_weights(const kvr_cache* c, const kvr_layer_weights* w) {
+    if (!w || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down || !w->norm1 || !w->norm2) {
+        set_error("layer weights: NULL pointer");
+        return KVR_EINVAL;
+    }
+    if (c->m.has_qkv_bias && !w->b_qkv) {
+        set_error("layer weights: the model has q/k/v biases but b_qkv is NULL");
+        return KVR_EINVAL;
+    }
+    const void* ps[] = {w->w_qkv, w->b_qkv, w->w_o, w->w_gate_up, w->w_down, w->norm1, w->norm2};
+    for (const void* p : ps)
+        if (p && !aligned16(p)) {
+            set_error("layer weights must be 16-byte aligned");
+            return KVR_EINVAL;
+        }
+    return KVR_OK;
+}
+
+// One layer of the packed refresh over the current selection.
+kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* hidden, uint8_t* ws,
+                     const WsLayout& L, cudaStream_t s) {
+    const kvr_model_desc& m = c->m;
+    const int R = c->sel.n_rows;
+    const int dt = m.dtype;
+    const Gemms g = plan_all(m, R);
+    void* xn = ws + L.xn;
+    void* q = ws + L.q;
+    void* o = ws + L.o;
+    float* h = reinterpret_cast<float*>(ws + L.h);
+    void* hn = ws + L.hn;
+    void* act = ws + L.act;
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    std::string why;
+
+    {
+        Prof p(c, KVR_K_RMSNORM, s);
+        KVR_CHECK_LAUNCH(launch_rmsnorm(dt, hidden, 0, w->norm1, xn, R, m.d_model, m.rms_eps, s), "rmsnorm");
+    }
+    {
+        Prof p(c, KVR_K_GEMM_QKV, s);
+        cudaError_t e = launch_gemm(dt, g.qkv, w->w_qkv, xn, part, c->d_err, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("qkv projection " + why).c_str());
+    }
+    {
+        Prof p(c, KVR_K_EPI_QKV, s);
+        QkvEpi a{};
+        a.part = part;
+        a.splits = g.qkv.splits;
+        a.R = R;
+        a.n_q_heads = m.n_q_heads;
+        a.n_kv_heads = m.n_kv_heads;
+        a.head_dim = m.head_dim;
+        a.bias = m.has_qkv_bias ? w->b_qkv : nullptr;
+        a.rope = c->d_rope;
+        a.U = c->d_U;
+        a.row_seq = c->d_row_seq;
+        a.q_out = q;
+        a.k_base = c->k_base;
+        a.v_base = c->v_base;
+        a.layer = layer;
+        a.n_layers = m.n_layers;
+        a.capacity = c->capacity;
+        a.err = c->d_err;
+        KVR_CHECK_LAUNCH(launch_epi_qkv(dt, a, s), "qkv epilogue");
+    }
+    {
+        Prof p(c, KVR_K_ATTN, s);
+        AttnLaunch a{};
+        a.q = q;
+        a.out = o;
+        a.k_base = c->k_base;
+        a.v_base = c->v_base;
+        a.U = c->d_U;
+        a.plan = c->d_plan;
+        a.loc = c->d_eloc;
+        a.snk = c->d_esnk;
+        a.n_tiles = c->sel.n_tiles;
+        a.n_q_heads = m.n_q_heads;
+        a.n_kv_heads = m.n_kv_heads;
+        a.head_dim = m.head_dim;
+        a.layer = layer;
+        a.n_layers = m.n_layers;
+        a.capacity = c->capacity;
+        a.n_tokens = c->n_tokens;
+        a.words = c->words;
+        a.batch = c->batch;
+        a.alpha = c->alpha;
+        a.beta = c->beta;
+        a.err = c->d_err;
+        cudaError_t e = launch_attention(dt, a, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
+    }
+    {
+        Prof p(c, KVR_K_GEMM_O, s);
+        cudaError_t e = launch_gemm(dt, g.o, w->w_o, o, part, c->d_err, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("output projection " + why).c_str());
+    }
+    {
+        Prof p(c, KVR_K_EPI_O, s);
+        KVR_CHECK_LAUNCH(launch_epi_residual_f32(dt, part, g.o.splits, R, m.d_model, hidden, h, s), "o epilogue");
+    }
+    {
+        Prof p(c, KVR_K_RMSNORM, s);
+        KVR_CHECK_LAUNCH(launch_rmsnorm(dt, h, 1, w->norm2, hn, R, m.d_model, m.rms_eps, s), "rmsnorm");
+    }
+    {
+        Prof p(c, KVR_K_GEMM_GATEUP, s);
+        cudaError_t e = launch_gemm(dt, g.gu, w->w_gate_up, hn, part, c->d_err, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("gate/up projection " + why).c_str());
+    }
+    {
+        Prof p(c, KVR_K_EPI_GATEUP, s);
+        KVR_CHECK_LAUNCH(launch_epi_swiglu(dt, part, g.gu.splits, R, m.ffn_dim, act, s), "swiglu epilogue");
+    }
+    {
+        Prof p(c, KVR_K_GEMM_DOWN, s);
+        cudaError_t e = launch_gemm(dt, g.down, w->w_down, act, part, c->d_err, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("down projection " + why).c_str());
+    }
+    {
+        Prof p(c, KVR_K_EPI_DOWN, s);
+        KVR_CHECK_LAUNCH(launch_epi_down(dt, part, g.down.splits, R, m.d_model, h, hidden, s), "down epilogue");
+    }
+    return KVR_OK;
+}
+
+kvr_status commit(kvr_cache* c, cudaStream_t s) {
+    Prof p(c, KVR_K_COMMIT, s);
+    KVR_CHECK_LAUNCH(launch_commit(c->d_local, c->d_sink, c->d_sel, c->batch * c->words,
+                                   (c->flags & KVR_SINK_STATIC) ? 1 : 0, s),
+                     "metadata commit");
+    return KVR_OK;
+}
+
+kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_bytes, WsLayout* L) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (!c->sel.valid) {
+        set_error("no selection: call kvr_select first");
+        return KVR_ESTATE;
+    }
+    const int R = c->sel.n_rows;
+    *L = layout(c->m, R, part_bytes(c->m, R));
+    if (R == 0) return KVR_OK;
+    if (!hidden || !ws) {
+        set_error("hidden rows or workspace is NULL");
+        return KVR_EINVAL;
+    }
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) || !aligned16(hidden)) {
+        set_error("workspace must be 256-byte aligned and hidden rows 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    if (ws_bytes < L->total) {
+        set_error("workspace too small: need " + std::to_string(L->total) + " bytes");
+        return KVR_EINVAL;
+    }
+    return KVR_OK;
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_err = msg; }
+
+kvr_status cuda_fail(cudaError_t e, const char* what) {
+    set_error(std::string(what) + ": " + cudaGetErrorString(e));
+    return KVR_ECUDA;
+}
+
+bool make_tmap_2d_bf16(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows, std::string* why) {
+    if (!get_encode(why)) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled failed with " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                       std::string* why) {
+    if (!get_encode(why)) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled failed with " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace kvr
+
+using namespace kvr;
+
+extern "C" {
+
+const char* kvr_last_error(void) { return g_err.c_str(); }
+
+kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capacity, void* k_base, void* v_base,
+                            int32_t n_tokens, int32_t suffix_start, const uint32_t* local_bits,
+                            const uint32_t* sink_bits, float alpha, float beta, uint32_t flags, void* stream,
+                            kvr_cache** out) {
+    if (!out) {
+        set_error("out is NULL");
+        return KVR_EINVAL;
+    }
+    *out = nullptr;
+    kvr_status st = validate_desc(m);
+    if (st != KVR_OK) return st;
+    if (batch < 1 || capacity < 1 || n_tokens < 1 || n_tokens > capacity || suffix_start < 0 ||
+        suffix_start > n_tokens) {
+        set_error("need batch >= 1 and 0 <= suffix_start <= n_tokens <= capacity");
+        return KVR_EINVAL;
+    }
+    if (!k_base || !v_base || !aligned16(k_base) || !aligned16(v_base)) {
+        set_error("K/V cache pointers must be non-NULL and 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) {
+        set_error("alpha and beta must be finite");
+        return KVR_EINVAL;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    kvr_cache* c = new kvr_cache();
+    c->m = *m;
+    c->batch = batch;
+    c->capacity = capacity;
+    c->n_tokens = n_tokens;
+    c->suffix_start = suffix_start;
+    c->words = (capacity + 31) / 32;
+    c->alpha = alpha;
+    c->beta = beta;
+    c->flags = flags;
+    c->k_base = k_base;
+    c->v_base = v_base;
+    cudaGetDevice(&c->device);
+
+    int rpt = 0, kpt = 0;
+    attention_tiling(m->dtype, m->n_q_heads, m->n_kv_heads, &rpt, &kpt);
+    const size_t rows = (size_t)batch * capacity;
+    c->max_tiles = (int)(rows / rpt + batch + 1);
+    const size_t wbytes = (size_t)batch * c->words * sizeof(uint32_t);
+    const int half = m->head_dim / 2;
+    c->stage_elems = (size_t)batch * 8 + rows;
+    cudaError_t e = cudaSuccess;
+    auto A = [&](void** p, size_t n) {
+        if (e == cudaSuccess) e = cudaMalloc(p, n);
+    };
+    A((void**)&c->d_local, wbytes);
+    A((void**)&c->d_sink, wbytes);
+    A((void**)&c->d_sel, wbytes);
+    A((void**)&c->d_eloc, wbytes);
+    A((void**)&c->d_esnk, wbytes);
+    A((void**)&c->d_seqinfo, c->stage_elems * sizeof(int32_t));
+    A((void**)&c->d_U, rows * sizeof(int32_t));
+    A((void**)&c->d_row_seq, rows * sizeof(int32_t));
+    A((void**)&c->d_iv, rows * 2 * sizeof(int32_t));
+    A((void**)&c->d_plan, (size_t)c->max_tiles * 8 * sizeof(int32_t));
+    A((void**)&c->d_rope, (size_t)capacity * half * sizeof(float2));
+    A((void**)&c->d_err, 4 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMallocHost((void**)&c->h_stage, c->stage_elems * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        set_error(std::string("allocation failed: ") + cudaGetErrorString(e));
+        free_cache(c);
+        return KVR_ENOMEM;
+    }
+    c->d_raw = c->d_seqinfo + (size_t)batch * 8;
+
+    // rotary table: angle u * theta^(-2i/d_h) formed in double, stored as fp32 (cos, sin)
+    std::vector<float2> rope((size_t)capacity * half);
+    for (int i = 0; i < half; ++i) {
+        const double inv = std::pow(m->rope_theta, -2.0 * i / (double)m->head_dim);
+        for (int u = 0; u < capacity; ++u) {
+            const double a = (double)u * inv;
+            rope[(size_t)u * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+        }
+    }
+    std::vector<uint32_t> zeros((size_t)batch * c->words, 0u);
+    e = cudaMemcpyAsync(c->d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->d_local, local_bits ? local_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->d_sink, sink_bits ? sink_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_err, 0, 4 * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_sel, 0, wbytes, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_eloc, c->d_local, wbytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_esnk, c->d_sink, wbytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        kvr_status r = cuda_fail(e, "cache set-up");
+        free_cache(c);
+        return r;
+    }
+    *out = c;
+    return KVR_OK;
+}
+
+kvr_status kvr_destroy_cache(kvr_cache* c) {
+    if (!c) return KVR_OK;
+    cudaDeviceSynchronize();
+    free_cache(c);
+    return KVR_OK;
+}
+
+kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
+                      const int32_t* token_ids, const void* embed_table, int32_t vocab, const void* hidden_src,
+                      void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out, void* stream) {
+    if (!c || !counts) {
+        set_error("cache or counts is NULL");
+        return KVR_EINVAL;
+    }
+    const bool use_ids = token_ids || embed_table;
+    if (use_ids == (hidden_src != nullptr) || (use_ids && (!token_ids || !embed_table))) {
+        set_error("give exactly one row source: token_ids + embed_table, or hidden_src");
+        return KVR_EINVAL;
+    }
+    if (use_ids && vocab < 1) {
+        set_error("vocab must be >= 1 with an embedding table");
+        return KVR_EINVAL;
+    }
+    if (budget_percent > 100 || budget_percent < -1) {
+        set_error("budget_percent must be -1 or in [0, 100]");
+        return KVR_EINVAL;
+    }
+    const int B = c->batch;
+    Selection sel;
+    sel.counts.assign(counts, counts + B);
+    int64_t total = 0;
+    for (int i = 0; i < B; ++i) {
+        if (counts[i] < 0 || counts[i] > c->n_tokens - c->suffix_start) {
+            set_error("count for sequence " + std::to_string(i) + " is outside [0, suffix length]");
+            return counts[i] < 0 ? KVR_EINVAL : KVR_ERANGE;
+        }
+        total += counts[i];
+    }
+    if (total > 0 && (!positions || !hidden_out)) {
+        set_error("positions or hidden_out is NULL");
+        return KVR_EINVAL;
+    }
+    if (hidden_out && !aligned16(hidden_out)) {
+        set_error("hidden_out must be 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    const int S = c->n_tokens - c->suffix_start;
+    if (budget_percent >= 0) {
+        const int want = std::min(S, (int)(((int64_t)S * budget_percent + 99) / 100));
+        for (int i = 0; i < B; ++i)
+            if (counts[i] != want) {
+                set_error("sequence " + std::to_string(i) + " selects " + std::to_string(counts[i]) +
+                          " positions; the exact budget is " + std::to_string(want));
+                return KVR_EINVAL;
+            }
+    }
+    // validation: range, duplicates; interval count from the membership map
+    std::vector<uint8_t> mark(c->n_tokens);
+    int64_t off = 0;
+    sel.row_off.resize(B);
+    sel.iv_count.resize(B);
+    sel.iv_off.resize(B);
+    sel.tile_count.resize(B);
+    sel.tile_off.resize(B);
+    attention_tiling(c->m.dtype, c->m.n_q_heads, c->m.n_kv_heads, &sel.rows_per_tile, &sel.keys_per_tile);
+    int rows = 0, ivs = 0, tiles = 0;
+    for (int i = 0; i < B; ++i) {
+        std::fill(mark.begin(), mark.end(), 0);
+        for (int k = 0; k < counts[i]; ++k) {
+            const int p = positions[off + k];
+            if (p < c->suffix_start || p >= c->n_tokens) {
+                set_error("position " + std::to_string(p) + " is outside the retained suffix [" +
+                          std::to_string(c->suffix_start) + ", " + std::to_string(c->n_tokens) + ")");
+                return KVR_ERANGE;
+            }
+            if (mark[p]) {
+                set_error("duplicate position " + std::to_string(p) + " in sequence " + std::to_string(i));
+                return KVR_EINVAL;
+            }
+            mark[p] = 1;
+        }
+        int iv = 0;
+        for (int t = c->suffix_start; t < c->n_tokens; ++t)
+            if (mark[t] && (t == 0 || !mark[t - 1])) ++iv;
+        sel.row_off[i] = rows;
+        sel.iv_off[i] = ivs;
+        sel.iv_count[i] = iv;
+        sel.tile_off[i] = tiles;
+        sel.tile_count[i] = (counts[i] + sel.rows_per_tile - 1) / sel.rows_per_tile;
+        rows += counts[i];
+        ivs += iv;
+        tiles += sel.tile_count[i];
+        off += counts[i];
+    }
+    if (tiles > c->max_tiles) {
+        set_error("internal: plan capacity exceeded");
+        return KVR_EINVAL;
+    }
+    sel.n_rows = rows;
+    sel.n_intervals = ivs;
+    sel.n_tiles = tiles;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the staging buffer may still feed the previous upload
+    cudaError_t e = cudaEventSynchronize(c->stage_ev);
+    if (e != cudaSuccess) return cuda_fail(e, "staging wait");
+    int32_t* st = c->h_stage;
+    for (int i = 0, raw = 0; i < B; ++i) {
+        int32_t* info = st + 8 * i;
+        info[0] = counts[i];
+        info[1] = sel.row_off[i];
+        info[2] = sel.iv_off[i];
+        info[3] = sel.tile_off[i];
+        info[4] = sel.tile_count[i];
+        info[5] = raw;
+        info[6] = 0;
+        info[7] = 0;
+        raw += counts[i];
+    }
+    if (total) std::memcpy(st + 8 * B, positions, (size_t)total * sizeof(int32_t));
+    e = cudaMemcpyAsync(c->d_seqinfo, st, (8 * B + total) * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "position upload");
+    e = cudaEventRecord(c->stage_ev, s);
+    if (e != cudaSuccess) return cuda_fail(e, "position upload");
+
+    SelectLaunch a{};
+    a.raw = c->d_raw;
+    a.seqinfo = c->d_seqinfo;
+    a.local = c->d_local;
+    a.sink = c->d_sink;
+    a.sel = c->d_sel;
+    a.eloc = c->d_eloc;
+    a.esnk = c->d_esnk;
+    a.U = c->d_U;
+    a.row_seq = c->d_row_seq;
+    a.iv = c->d_iv;
+    a.plan = c->d_plan;
+    a.err = c->d_err;
+    a.words = c->words;
+    a.suffix_start = c->suffix_start;
+    a.n_tokens = c->n_tokens;
+    a.rows_per_tile = sel.rows_per_tile;
+    a.keys_per_tile = sel.keys_per_tile;
+    a.sink_static = (c->flags & KVR_SINK_STATIC) ? 1 : 0;
+    {
+        Prof p(c, KVR_K_SELECT, s);
+        KVR_CHECK_LAUNCH(launch_select(a, B, s), "select");
+    }
+    {
+        Prof p(c, KVR_K_GATHER, s);
+        KVR_CHECK_LAUNCH(launch_gather(c->m.dtype, c->d_U, c->d_row_seq, rows, c->m.d_model, c->capacity, token_ids,
+                                       embed_table, hidden_src, hidden_out, c->d_err, vocab, s),
+                         "row gather");
+    }
+    sel.valid = true;
+    c->sel = sel;
+    if (n_rows_out) *n_rows_out = rows;
+    if (n_intervals_out) *n_intervals_out = ivs;
+    return KVR_OK;
+}
+
+size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
+    if (!c) return 0;
+    int R = max_rows > 0 ? max_rows : c->sel.n_rows;
+    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R)).total;
+    // the split choice changes with the row-tile count: take the largest partial
+    // region over every row count up to max_rows (it peaks at tile-count edges)
+    const int step = c->m.dtype == KVR_BF16 ? 256 : 64;
+    size_t part = 0;
+    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R)));
+    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r));
+    return layout(c->m, R, part).total;
+}
+
+kvr_status kvr_refresh_layer(kvr_cache* c, int32_t layer, const kvr_layer_weights* w, void* hidden_inout,
+                             void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
+    WsLayout L;
+    kvr_status st = check_refresh_args(c, hidden_inout, workspace, ws_bytes, &L);
+    if (st != KVR_OK) return st;
+    if (layer < 0 || layer >= c->m.n_layers) {
+        set_error("layer " + std::to_string(layer) + " is outside [0, n_layers)");
+        return KVR_ERANGE;
+    }
+    if ((st = check_layer_weights(c, w)) != KVR_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c->sel.n_rows > 0) {
+        st = run_layer(c, layer, w, hidden_inout, static_cast<uint8_t*>(workspace), L, s);
+        if (st != KVR_OK) return st;
+    }
+    if (flags & KVR_COMMIT_META) return commit(c, s);
+    return KVR_OK;
+}
+
+kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_begin, int32_t layer_end,
+                       void* hidden_inout, void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
+    WsLayout L;
+    kvr_status st = check_refresh_args(c, hidden_inout, workspace, ws_bytes, &L);
+    if (st != KVR_OK) return st;
+    if (layer_begin < 0 || layer_end > c->m.n_layers || layer_begin > layer_end) {
+        set_error("layer range outside [0, n_layers]");
+        return KVR_ERANGE;
+    }
+    if (!w && layer_end > layer_begin) {
+        set_error("weights array is NULL");
+        return KVR_EINVAL;
+    }
+    for (int l = layer_begin; l < layer_end; ++l)
+        if ((st = check_layer_weights(c, &w[l])) != KVR_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c->sel.n_rows > 0) {
+        for (int l = layer_begin; l < layer_end; ++l) {
+            st = run_layer(c, l, &w[l], hidden_inout, static_cast<uint8_t*>(workspace), L, s);
+            if (st != KVR_OK) return st;
+        }
+    }
+    if (flags & KVR_COMMIT_META) return commit(c, s);
+    return KVR_OK;
+}
+
+kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, void* workspace, size_t ws_bytes,
+                      void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (!c->sel.valid) {
+        set_error("no selection: call kvr_select first");
+        return KVR_ESTATE;
+    }
+    if (layer < 0 || layer >= c->m.n_layers) {
+        set_error("layer outside [0, n_layers)");
+        return KVR_ERANGE;
+    }
+    if (c->sel.n_rows == 0) return KVR_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) {
+        set_error("q and out must be non-NULL and 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    AttnLaunch a{};
+    a.q = q;
+    a.out = out;
+    a.k_base = c->k_base;
+    a.v_base = c->v_base;
+    a.U = c->d_U;
+    a.plan = c->d_plan;
+    a.loc = c->d_local;
+    a.snk = c->d_sink;
+    a.n_tiles = c->sel.n_tiles;
+    a.n_q_heads = c->m.n_q_heads;
+    a.n_kv_heads = c->m.n_kv_heads;
+    a.head_dim = c->m.head_dim;
+    a.layer = layer;
+    a.n_layers = c->m.n_layers;
+    a.capacity = c->capacity;
+    a.n_tokens = c->n_tokens;
+    a.words = c->words;
+    a.batch = c->batch;
+    a.alpha = c->alpha;
+    a.beta = c->beta;
+    a.err = c->d_err;
+    std::string why;
+    Prof p(c, KVR_K_ATTN, s);
+    cudaError_t e = launch_attention(c->m.dtype, a, s, &why);
+    if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
+    return KVR_OK;
+}
+
+kvr_status kvr_sync_status(kvr_cache* c, void* stream) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int32_t w[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(w, c->d_err, sizeof(w), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "error word read");
+    if (w[0] == 0) return KVR_OK;
+    cudaMemset(c->d_err, 0, sizeof(w));
+    if (w[0] & DEV_ERR_TIMEOUT) {
+        set_error("a device-side wait timed out");
+        return KVR_ETIMEOUT;
+    }
+    set_error(std::string("device-side check failed:") + ((w[0] & DEV_ERR_INDEX) ? " index out of range" : "") +
+              ((w[0] & DEV_ERR_DUPLICATE) ? " duplicate position" : ""));
+    return KVR_EDEVICE;
+}
+
+kvr_status kvr_read_selection(kvr_cache* c, int32_t seq, int32_t* U, int32_t u_cap, int32_t* iv, int32_t iv_cap,
+                              uint32_t* sel, uint32_t* eloc, uint32_t* esnk, int32_t* plan, int32_t plan_cap,
+                              int32_t* n_tiles, int32_t* rows_per_tile, int32_t* keys_per_tile) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (!c->sel.valid) {
+        set_error("no selection");
+        return KVR_ESTATE;
+    }
+    if (seq < 0 || seq >= c->batch) {
+        set_error("sequence index out of range");
+        return KVR_ERANGE;
+    }
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "synchronize");
+    const Selection& S = c->sel;
+    const size_t wb = (size_t)c->words * sizeof(uint32_t);
+    auto cp = [&](void* dst, const void* src, size_t n) {
+        if (dst && n && e == cudaSuccess) e = cudaMemcpy(dst, src, n, cudaMemcpyDeviceToHost);
+    };
+    cp(U, c->d_U + S.row_off[seq], (size_t)std::min(u_cap, S.counts[seq]) * sizeof(int32_t));
+    cp(iv, c->d_iv + 2 * (size_t)S.iv_off[seq], (size_t)std::min(iv_cap, S.iv_count[seq]) * 2 * sizeof(int32_t));
+    cp(sel, c->d_sel + (size_t)seq * c->words, wb);
+    cp(eloc, c->d_eloc + (size_t)seq * c->words, wb);
+    cp(esnk, c->d_esnk + (size_t)seq * c->words, wb);
+    if (plan) {
+        const int nt = std::min(plan_cap, S.tile_count[seq]);
+        std::vector<int32_t> p8((size_t)nt * 8);
+        cp(p8.data(), c->d_plan + 8 * (size_t)S.tile_off[seq], p8.size() * sizeof(int32_t));
+        for (int t = 0; t < nt; ++t) {
+            for (int k = 0; k < 6; ++k) plan[6 * t + k] = p8[8 * t + k];
+            plan[6 * t] -= S.row_off[seq];
+        }
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "selection read");
+    if (n_tiles) *n_tiles = S.tile_count[seq];
+    if (rows_per_tile) *rows_per_tile = S.rows_per_tile;
+    if (keys_per_tile) *keys_per_tile = S.keys_per_tile;
+    return KVR_OK;
+}
+
+kvr_status kvr_read_meta(kvr_cache* c, uint32_t* local_bits, uint32_t* sink_bits) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    cudaError_t e = cudaDeviceSynchronize();
+    const size_t wb = (size_t)c->batch * c->words * sizeof(uint32_t);
+    if (e == cudaSuccess && local_bits) e = cudaMemcpy(local_bits, c->d_local, wb, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && sink_bits) e = cudaMemcpy(sink_bits, c->d_sink, wb, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "metadata read");
+    return KVR_OK;
+}
+
+kvr_status kvr_profile_enable(kvr_cache* c, int32_t enable) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    c->profiling = enable != 0;
+    return KVR_OK;
+}
+
+kvr_status kvr_profile_read(kvr_cache* c, double* ms, int64_t* launches, int32_t n) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    for (auto& r : c->prof) {
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        float t = 0.f;
+        cudaEventElapsedTime(&t, r.a, r.b);
+        c->prof_ms[r.kind] += t;
+        c->prof_n[r.kind] += 1;
+        c->ev_pool.push_back(r.a);
+        c->ev_pool.push_back(r.b);
+    }
+    c->prof.clear();
+    for (int k = 0; k < n && k < KVR_K_COUNT; ++k) {
+        if (ms) ms[k] = c->prof_ms[k];
+        if (launches) launches[k] = c->prof_n[k];
+    }
+    for (int k = 0; k < KVR_K_COUNT; ++k) {
+        c->prof_ms[k] = 0.0;
+        c->prof_n[k] = 0;
+    }
+    return KVR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// kvr_internal.h -- library-private state and kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/kvr.h"
+
+namespace kvr {
+
+// device error word bits (err[0]); err[1] holds the first failing detail
+enum : int {
+    DEV_ERR_TIMEOUT = 1,     // a bounded wait gave up
+    DEV_ERR_INDEX = 2,       // an index failed its device-side bounds check
+    DEV_ERR_DUPLICATE = 4,   // duplicate position reached the device
+};
+
+constexpr int kNumSMs = 152;          // GB300
+constexpr int kAttnKeysPerTile = 128; // K/V tile of the tensor-core attention
+constexpr int kSimtRowsPerTile = 16;  // query positions per CTA of the SIMT attention
+constexpr int kSimtKeysPerTile = 64;
+
+struct Selection {
+    int32_t n_rows = 0, n_intervals = 0, n_tiles = 0;
+    int32_t rows_per_tile = 0, keys_per_tile = 0;
+    std::vector<int32_t> counts, row_off, iv_count, iv_off, tile_count, tile_off;
+    bool valid = false;
+};
+
+struct ProfRec {
+    int kind;
+    cudaEvent_t a, b;
+};
+
+struct kvr_cache_impl {
+    kvr_model_desc m{};
+    int32_t batch = 0, capacity = 0, n_tokens = 0, suffix_start = 0, words = 0;
+    float alpha = 0.f, beta = 0.f;
+    uint32_t flags = 0;
+    void* k_base = nullptr;
+    void* v_base = nullptr;
+    int device = 0;
+
+    // library-owned device buffers
+    uint32_t* d_local = nullptr;   // [batch][words]
+    uint32_t* d_sink = nullptr;
+    uint32_t* d_sel = nullptr;
+    uint32_t* d_eloc = nullptr;
+    uint32_t* d_esnk = nullptr;
+    int32_t* d_raw = nullptr;      // [batch*capacity] uploaded positions
+    int32_t* d_U = nullptr;        // [batch*capacity] sorted positions, all sequences
+    int32_t* d_row_seq = nullptr;  // [batch*capacity]
+    int32_t* d_iv = nullptr;       // [batch*capacity][2]
+    int32_t* d_plan = nullptr;     // [max_tiles][8]
+    int32_t* d_seqinfo = nullptr;  // [batch][8]: count, row_off, iv_off, tile_off, n_tiles
+    float2* d_rope = nullptr;      // [capacity][head_dim/2] (cos, sin)
+    int32_t* d_err = nullptr;      // [4]
+    int32_t max_tiles = 0;
+
+    // pinned staging for the position upload
+    int32_t* h_stage = nullptr;
+    size_t stage_elems = 0;
+    cudaEvent_t stage_ev = nullptr;
+
+    Selection sel;
+
+    bool profiling = false;
+    std::vector<ProfRec> prof;
+    std::vector<cudaEvent_t> ev_pool;
+    double prof_ms[KVR_K_COUNT] = {};
+    int64_t prof_n[KVR_K_COUNT] = {};
+};
+
+// ---------------------------------------------------------------- host helpers
+void set_error(const std::string& msg);
+kvr_status cuda_fail(cudaError_t e, const char* what);
+
+// Tensor maps (driver entry point fetched through the runtime).
+bool make_tmap_2d_bf16(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, std::string* why);
+bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                       std::string* why);
+
+// ---------------------------------------------------------------- launchers
+struct SelectLaunch {
+    const int32_t* raw;        // uploaded positions, sequence-major
+    const int32_t* seqinfo;    // [batch][8]
+    const uint32_t* local;
+    const uint32_t* sink;
+    uint32_t* sel;
+    uint32_t* eloc;
+    uint32_t* esnk;
+    int32_t* U;
+    int32_t* row_seq;
+    int32_t* iv;
+    int32_t* plan;
+    int32_t* err;
+    int32_t words, suffix_start, n_tokens, rows_per_tile, keys_per_tile, sink_static;
+};
+cudaError_t launch_select(const SelectLaunch& a, int batch, cudaStream_t s);
+
+cudaError_t launch_gather(int dtype, const int32_t* U, const int32_t* row_seq, int n_rows, int d,
+                          int capacity, const int32_t* token_ids, const void* embed, const void* hidden_src,
+                          void* out, int32_t* err, int vocab_guard, cudaStream_t s);
+
+cudaError_t launch_commit(uint32_t* local, uint32_t* sink, const uint32_t* sel, int total_words, int sink_static,
+                          cudaStream_t s);
+
+// RMSNorm: in is model dtype (in_f32 = 0) or fp32 (in_f32 = 1), out model dtype.
+cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w, void* out, int rows, int d,
+                           float eps, cudaStream_t s);
+
+// GEMM partials: part[split][r][f] = sum_{k in split} x[r][k] * w[f][k]
+struct GemmPlan {
+    int n_out, K, R;
+    int m_tiles, n_tiles, BN, splits, stages;
+};
+GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
+size_t gemm_partial_bytes(const GemmPlan& p);
+cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
+                        cudaStream_t s, std::string* why);
+
+// Epilogues (sum split partials in split order, then the fused op).
+struct QkvEpi {
+    const float* part;
+    int splits, R, n_q_heads, n_kv_heads, head_dim;
+    const void* bias;          // nullable
+    const float2* rope;        // [capacity][head_dim/2]
+    const int32_t* U;
+    const int32_t* row_seq;
+    void* q_out;               // [R][Hq][dh]
+    void* k_base;
+    void* v_base;
+    int layer, n_layers, capacity;
+    int32_t* err;
+};
+cudaError_t launch_epi_qkv(int dtype, const QkvEpi& a, cudaStream_t s);
+cudaError_t launch_epi_residual_f32(int dtype, const float* part, int splits, int R, int d, const void* x,
+                                    float* h_out, cudaStream_t s);
+cudaError_t launch_epi_swiglu(int dtype, const float* part, int splits, int R, int F, void* act_out,
+                              cudaStream_t s);
+cudaError_t launch_epi_down(int dtype, const float* part, int splits, int R, int d, const float* h, void* x_out,
+                            cudaStream_t s);
+
+// Attention over the mixed cache.
+struct AttnLaunch {
+    const void* q;             // [R][Hq][dh]
+    void* out;                 // [R][Hq*dh]
+    const void* k_base;
+    const void* v_base;
+    const int32_t* U;
+    const int32_t* plan;       // [n_tiles][8]
+    const uint32_t* loc;       // [batch][words]
+    const uint32_t* snk;
+    int n_tiles, n_q_heads, n_kv_heads, head_dim, layer, n_layers, capacity, n_tokens, words, batch;
+    float alpha, beta;
+    int32_t* err;
+};
+cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why);
+// Query tile geometry of the attention kernel for a model.
+void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile);
+
+}  // namespace kvr
+
+struct kvr_cache : public kvr::kvr_cache_impl {};

@@ -1,0 +1,92 @@
+"""Device-side set-up of a refresh workload: allocates the weights, cache,
+metadata and row sources with torch, binds them to a libkvr cache handle and
+drives the C entry points.  Shared by the GPU tests and bench.py; it holds
+none of the method's arithmetic (that runs in libkvr's kernels)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import kvr
+from . import workloads as wl
+
+
+class Setup:
+    """One workload bound to a libkvr cache on the current CUDA device.
+
+    cache: "random" (seeded N(0, 1) K/V) or a (K, V) pair of device tensors in
+    the [batch, L, H_kv, capacity, d_h] layout.  positions: override of the
+    selection (list of int arrays, one per sequence)."""
+
+    def __init__(self, w: wl.Workload, cache="random", positions=None, weights=None, flags=0,
+                 local=None, sink=None, device="cuda"):
+        self.w = w
+        self.shape = w.model
+        self.device = device
+        self.layers = weights if weights is not None else wl.make_layer_weights(w, device)
+        self.warr = kvr.layer_weights_array(self.layers)
+        if isinstance(cache, str):
+            self.K, self.V = wl.make_random_cache(w, device)
+        else:
+            self.K, self.V = cache
+        lm, sm = wl.make_metadata(w)
+        if local is not None:
+            lm = local
+        if sink is not None:
+            sm = sink
+        self.local_mask, self.sink_mask = lm, sm
+        self.flags = flags
+        self.handle = kvr.kvr_create_cache(
+            kvr.model_desc(self.shape), w.batch, w.capacity, self.K, self.V, w.n_tokens, w.suffix_start,
+            np.ascontiguousarray(wl.pack_bits(lm)), np.ascontiguousarray(wl.pack_bits(sm)),
+            w.alpha, w.beta, flags)
+        self.words = (w.capacity + 31) // 32
+        if w.uses_embeddings:
+            self.embed = wl.make_embeddings(w, device)
+            self.ids = wl.make_token_ids(w, device)
+            self.hidden_src = None
+        else:
+            self.embed = self.ids = None
+            self.hidden_src = wl.make_hidden_inputs(w, device)
+        self.positions = positions if positions is not None else wl.make_positions(w)
+        self.pos_host = np.ascontiguousarray(np.concatenate(self.positions).astype(np.int32))
+        self.counts = np.array([len(p) for p in self.positions], np.int32)
+        self.n_rows = int(self.counts.sum())
+        self.hidden = torch.empty((max(self.n_rows, 1), self.shape.d_model), dtype=self.shape.torch_dtype,
+                                  device=device)
+        self.ws_bytes = 0
+        self.ws = None
+
+    def select(self, budget_percent=-1, stream=None):
+        n = int(np.asarray(self.counts).sum())
+        if n > self.hidden.shape[0]:
+            self.hidden = torch.empty((n, self.shape.d_model), dtype=self.shape.torch_dtype, device=self.device)
+        self.n_rows = n
+        rows, ivs = kvr.kvr_select(
+            self.handle, self.pos_host, self.counts, budget_percent,
+            token_ids=self.ids, embed_table=self.embed, vocab=self.shape.vocab if self.embed is not None else 0,
+            hidden_src=self.hidden_src, hidden_out=self.hidden, stream=stream)
+        need = kvr.kvr_workspace_bytes(self.handle, 0)
+        if self.ws is None or need > self.ws_bytes:
+            self.ws_bytes = max(need, 256)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        return rows, ivs
+
+    def refresh(self, layer_begin=0, layer_end=None, flags=kvr.KVR_COMMIT_META, stream=None):
+        L = self.shape.n_layers if layer_end is None else layer_end
+        kvr.kvr_refresh(self.handle, self.warr, layer_begin, L, self.hidden, self.ws, self.ws_bytes, flags,
+                        stream=stream)
+
+    def sync(self, stream=None):
+        kvr.kvr_sync_status(self.handle, stream)
+
+    def close(self):
+        if self.handle:
+            kvr.kvr_destroy_cache(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

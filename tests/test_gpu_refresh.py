@@ -1,0 +1,141 @@
+"""GPU parity of the packed refresh through the C ABI against the float64
+oracle: refreshed hidden rows and written-back K/V within the stated
+tolerance, every unselected K/V row bit-identical, metadata bit-exact."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_kv_cache_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+kvr = pytest.importorskip("selective_kv_cache_gb300.kvr")
+from selective_kv_cache_gb300.harness import Setup  # noqa: E402
+from helpers import TOL, LazyWeights, assert_close, f64, oracle_spec, small_bf16  # noqa: E402
+
+
+def run_and_compare(s: Setup, W_oracle, Ks0, Vs0, X_src_seqs, tol, sink_static=False, check_layers=None):
+    """Refresh on the GPU, then the oracle per sequence; compare."""
+    w = s.w
+    spec = oracle_spec(w)
+    K_in = s.K.clone()
+    V_in = s.V.clone()
+    s.select()
+    s.refresh()
+    s.sync()
+    worst = {}
+    off = 0
+    local_after, sink_after = kvr.kvr_read_meta(s.handle, w.batch, s.words)
+    for seq, pos in enumerate(s.positions):
+        n = len(pos)
+        U = oracle.sorted_positions(pos)
+        X, K, V, loc2, snk2 = oracle.refresh_packed(
+            spec, W_oracle, Ks0[seq], Vs0[seq], s.local_mask[seq], s.sink_mask[seq], pos, X_src_seqs[seq],
+            w.alpha, w.beta, sink_static)
+        worst["hidden"] = max(worst.get("hidden", 0), assert_close(f64(s.hidden[off:off + n]), X, tol, "hidden"))
+        layers = range(w.model.n_layers) if check_layers is None else check_layers
+        for l in layers:
+            Kg = f64(s.K[seq, l][:, torch.from_numpy(U)])
+            Vg = f64(s.V[seq, l][:, torch.from_numpy(U)])
+            worst["K"] = max(worst.get("K", 0), assert_close(Kg, K[l][:, U], tol, f"K layer {l}"))
+            worst["V"] = max(worst.get("V", 0), assert_close(Vg, V[l][:, U], tol, f"V layer {l}"))
+        # unselected rows: bit-identical to the input cache
+        keep = torch.ones(w.capacity, dtype=torch.bool, device=s.K.device)
+        keep[torch.from_numpy(U).to(s.K.device)] = False
+        assert torch.equal(s.K[seq][:, :, keep], K_in[seq][:, :, keep])
+        assert torch.equal(s.V[seq][:, :, keep], V_in[seq][:, :, keep])
+        np.testing.assert_array_equal(local_after[seq], oracle.bitmask_words(loc2)[:s.words])
+        np.testing.assert_array_equal(sink_after[seq], oracle.bitmask_words(snk2)[:s.words])
+        off += n
+    return worst
+
+
+def test_tiny_fp32_against_oracle_prefill_cache():
+    """Tiny fp32 workload: stale cache from the oracle's prefill of the dirty
+    sequence, refresh with the clean inputs, tolerance 1e-4."""
+    w = wl.WORKLOADS["tiny"]
+    spec = oracle_spec(w)
+    layers_cpu = wl.make_layer_weights(w, "cpu")
+    W = [{k: f64(v) for k, v in L.items()} for L in layers_cpu]
+    dirty = f64(wl.make_hidden_inputs(w, "cpu", dirty=True))[0]
+    clean = f64(wl.make_hidden_inputs(w, "cpu"))[0]
+    _, Ks, Vs = oracle.prefill(spec, W, dirty)
+    Kt = torch.from_numpy(Ks[None]).float().cuda().contiguous()
+    Vt = torch.from_numpy(Vs[None]).float().cuda().contiguous()
+    layers = [{k: (v.cuda() if v is not None else None) for k, v in L.items()} for L in layers_cpu]
+    s = Setup(w, cache=(Kt, Vt), weights=layers)
+    worst = run_and_compare(s, W, Ks[None], Vs[None], [clean], TOL["f32"])
+    s.close()
+    print("tiny worst scaled errors", worst)
+
+
+@pytest.mark.parametrize("selection,alpha,beta,sink_static", [
+    ("units", 0.0, 0.0, False),
+    ("units", -2.0, -4.0, False),
+    ("isolated", -2.0, -4.0, True),
+    ("isolated", 1.0, -3.0, False),
+])
+def test_bf16_small_against_oracle(selection, alpha, beta, sink_static):
+    """Small bf16 model (head_dim 128, 4 query heads per K/V head, q/k/v
+    bias), several query tiles with a ragged tail, random local/sink masks."""
+    w = small_bf16(selection=selection, alpha=alpha, beta=beta)
+    rng = np.random.default_rng(11)
+    local = rng.random((1, w.capacity)) < 0.6
+    sink = rng.random((1, w.capacity)) < 0.2
+    layers = wl.make_layer_weights(w, "cuda")
+    s = Setup(w, weights=layers, local=local, sink=sink,
+              flags=kvr.KVR_SINK_STATIC if sink_static else 0)
+    W = LazyWeights(layers)
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = f64(s.embed)
+    ids = s.ids.cpu().numpy()
+    X_src = [emb[ids[b]] for b in range(w.batch)]
+    worst = run_and_compare(s, W, Ks0, Vs0, X_src, TOL["bf16"], sink_static=sink_static)
+    s.close()
+    print(selection, alpha, beta, "worst scaled errors", worst)
+
+
+def test_bf16_batch_of_sequences():
+    """Independent sequences sharing weights (seq-major rows, per-sequence
+    caches and plans)."""
+    w = small_bf16(batch=3, selection="isolated", n_select=70, alpha=-1.0, beta=0.0)
+    layers = wl.make_layer_weights(w, "cuda")
+    s = Setup(w, weights=layers)
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = f64(s.embed)
+    ids = s.ids.cpu().numpy()
+    worst = run_and_compare(s, LazyWeights(layers), Ks0, Vs0, [emb[ids[b]] for b in range(3)], TOL["bf16"])
+    s.close()
+    print("batch worst", worst)
+
+
+def test_empty_selection_is_a_no_op():
+    w = small_bf16(n_layers=1)
+    s = Setup(w, positions=[np.array([], np.int32)])
+    K_in = s.K.clone()
+    s.select()
+    s.refresh()
+    s.sync()
+    assert torch.equal(s.K, K_in)
+    s.close()
+
+
+@pytest.mark.slow
+def test_llama8b_full_size_against_oracle():
+    """The Llama-3-8B-shaped workload at full size (32 layers, N = 7680,
+    282 positions in units of 32-64), the launch configuration the benchmark
+    times: every refreshed row and every written K/V row at every layer."""
+    w = wl.WORKLOADS["llama8b"]
+    s = Setup(w)
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = s.embed
+    ids = s.ids.cpu().numpy()
+    U = oracle.sorted_positions(s.positions[0])
+    X_src = np.zeros((w.capacity, w.model.d_model))
+    X_src[U] = f64(emb[torch.from_numpy(ids[0][U].astype(np.int64)).cuda()])
+    worst = run_and_compare(s, LazyWeights(s.layers), Ks0, Vs0, [X_src], TOL["bf16"])
+    s.close()
+    print("llama8b worst scaled errors", worst)
