@@ -1,22 +1,28 @@
 // attention.cu -- picks the attention kernel for the model dtype and reports
-// its query-tile geometry (the plan is built over these tiles).
+// its query-tile geometry (the plan is built over these tiles): the
+// tensor-core kernel for bf16 models, the CUDA-core kernel for fp32 models.
 #include "kvr_internal.h"
 
 namespace kvr {
 
-size_t attn_simt_smem(int head_dim);
 int attn_simt_rows_per_tile(int n_q_heads, int n_kv_heads);
-cudaError_t launch_attention_simt(int dtype, const AttnLaunch& a, cudaStream_t s);
+cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s);
+int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads);
+cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why);
 
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile) {
-    (void)dtype;
-    *rows_per_tile = attn_simt_rows_per_tile(n_q_heads, n_kv_heads);
-    *keys_per_tile = kSimtKeysPerTile;
+    if (dtype == KVR_BF16) {
+        *rows_per_tile = attn_tc_rows_per_tile(n_q_heads, n_kv_heads);
+        *keys_per_tile = kAttnKeysPerTile;
+    } else {
+        *rows_per_tile = attn_simt_rows_per_tile(n_q_heads, n_kv_heads);
+        *keys_per_tile = kSimtKeysPerTile;
+    }
 }
 
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why) {
-    (void)why;
-    return launch_attention_simt(dtype, a, s);
+    if (dtype == KVR_BF16) return launch_attention_tc(a, s, why);
+    return launch_attention_simt(a, s);
 }
 
 }  // namespace kvr

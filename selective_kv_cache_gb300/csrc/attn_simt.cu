@@ -1,5 +1,6 @@
 // attn_simt.cu -- biased causal grouped-query attention over the mixed cache,
-// CUDA-core version (fp32 storage: the fp32 model path).
+// CUDA-core version for fp32 models (fp32 storage needs fp32 products; the
+// bf16 path runs on the tensor cores, attn_tc.cu).
 //
 //   s_ij = <q_i, k_j>/sqrt(d_h) + alpha*loc_j + beta*snk_j,  j <= g_i
 //   o_i  = sum_j softmax_j(s_ij) v_j
@@ -22,9 +23,7 @@ constexpr int kThreads = 256;
 constexpr int kMaxPairs = 64;
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
-__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void stf(float* p, float v) { *p = v; }
-__device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnLaunch a) {
@@ -141,21 +140,14 @@ int attn_simt_rows_per_tile(int n_q_heads, int n_kv_heads) {
     return kMaxPairs / G >= 1 ? kMaxPairs / G : 1;
 }
 
-cudaError_t launch_attention_simt(int dtype, const AttnLaunch& a, cudaStream_t s) {
+cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s) {
     if (a.n_tiles <= 0) return cudaSuccess;
     const size_t smem = attn_simt_smem(a.head_dim);
     dim3 grid(a.n_tiles, a.n_kv_heads);
-    if (dtype == KVR_BF16) {
-        cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attn_simt_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(a);
-    } else {
-        cudaError_t e =
-            cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attn_simt_kernel<float><<<grid, kThreads, smem, s>>>(a);
-    }
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_simt_kernel<float><<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,375 @@
+// attn_tc.cu -- biased causal grouped-query attention over the mixed cache on
+// the sm_103a tensor cores (bf16 storage, fp32 softmax and accumulation).
+//
+//   s_ij = <q_i, k_j>/sqrt(d_h) + alpha*loc_j + beta*snk_j,   j <= g_i
+//   o_i  = sum_j softmax_j(s_ij) v_j
+// ("kv-cross-attention-reuse", Sec. 6.4, Logit form; "Budgeted KV-Cache
+// Repair for Evolving Contexts", Sec. 13.2, Eq. 22, and Eqs. 23-24 for the
+// per-query-tile K/V tile counts that bound the loop.)
+//
+// One CTA per (query tile, K/V head).  The 128 MMA rows are the tile's
+// positions times the G query heads of that K/V head (row = p*G + i), so all
+// of them read the same K/V tiles and one causal limit g_p serves a whole
+// group.  Per 128-key tile:
+//   warp 0      TMA: K and V tiles (two 64-column boxes each, 128-B swizzle)
+//               into a 2-stage ring; keys >= n_tokens arrive as zeros;
+//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers,
+//               then O += P V into the TMEM output accumulator (V read
+//               MN-major straight from its cache layout);
+//   warps 2-5   one thread per row: scores from TMEM, scale + bias + causal
+//               mask, online softmax in base 2 (the running max is only
+//               raised, and O rescaled in TMEM, when it grows by more than
+//               2^8, so P stays <= 256), P as bf16 into shared memory for the
+//               PV product; at the end O / l to global memory.
+// Tiles below the plan's n_full are wholly visible to every row and skip the
+// causal test.  Every wait is bounded; on a timeout the CTA records the error,
+// drains its copies and MMAs, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "kvr_internal.h"
+#include "ptx.cuh"
+
+namespace kvr {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
+constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffP = kTile;
+constexpr uint32_t kOffK = 2 * kTile;           // 2 stages
+constexpr uint32_t kOffV = 4 * kTile;           // 2 stages
+constexpr uint32_t kOffBar = 6 * kTile;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// one lane polls, the whole warp follows (keeps tcgen05 .sync.aligned ops converged)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// address of 16-byte chunk c (0..15, 8 elements each) of row m in a 128 x 128
+// bf16 tile stored as two K-major 128-B-swizzled halves
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int m, int c) {
+    return base + (uint32_t)(c >> 3) * kHalf + (uint32_t)m * 128u + ((uint32_t)((c & 7) ^ (m & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnLaunch a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* k_full = bars + 0;     // [2]
+    uint64_t* v_full = bars + 2;     // [2]
+    uint64_t* kv_empty = bars + 4;   // [2]
+    uint64_t* s_full = bars + 6;     // [2]
+    uint64_t* s_free = bars + 8;     // [2]
+    uint64_t* p_full = bars + 10;
+    uint64_t* o_done = bars + 11;
+    uint64_t* mma_done = bars + 12;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int* plan = a.plan + 8 * tile;
+    const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], n_total = plan[5], seq = plan[6];
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int P = 128 / G;
+    const int head_index = (seq * a.n_layers + a.layer) * a.n_kv_heads + h;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    bool ok = true;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+
+    // rows of this thread (softmax warps): m = 32 * (warp % 4) + lane
+    const int m = 32 * (warp & 3) + lane;
+    const int p = m / G, gi = m % G;
+    const bool row_valid = warp >= 2 && m < P * G && p < nrows;
+    int g = umin;
+    if (warp >= 2) {
+        const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
+        if (row_valid) g = a.U[row0 + p];
+        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
+            st_shared_v4(tile_chunk(sbase + kOffQ, m, c), v);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < n_total; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(&kv_empty[st], ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* kd = smem + kOffK + st * kTile;
+                uint8_t* vd = smem + kOffV + st * kTile;
+                mbar_arrive_expect_tx(&k_full[st], kTile);
+                tma_load_3d(kd, &tmK, &k_full[st], 0, j * 128, head_index);
+                tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, j * 128, head_index);
+                mbar_arrive_expect_tx(&v_full[st], kTile);
+                tma_load_3d(vd, &tmV, &v_full[st], 0, j * 128, head_index);
+                tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, j * 128, head_index);
+                ++issued;
+            }
+            if (!ok) {
+                for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+                    mbar_wait(&k_full[j & 1], (uint32_t)(j >> 1) & 1u);
+                    mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+            const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);   // V is MN-major
+            auto issue_s = [&](int j) -> bool {
+                const int st = j & 1;
+                if (!mbar_wait(&k_full[st], (uint32_t)(j >> 1) & 1u)) return false;
+                if (j >= 2 && !mbar_wait(&s_free[st], (uint32_t)((j - 2) >> 1) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + st * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16(tmem + (uint32_t)st * 128u, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                             idesc_s, kk > 0);
+                }
+                mma_commit(&s_full[st]);
+                return true;
+            };
+            ok = n_total > 0 && issue_s(0);
+            for (int j = 0; ok && j < n_total; ++j) {
+                if (j + 1 < n_total && !issue_s(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                const int st = j & 1;
+                if (!mbar_wait(p_full, (uint32_t)j & 1u) || !mbar_wait(&v_full[st], (uint32_t)(j >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pa = sbase + kOffP, va = sbase + kOffV + st * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16(tmem + 256u, sdesc_sw128(pa + off, 16, 1024),
+                             sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
+                }
+                mma_commit(o_done);
+                mma_commit(&kv_empty[st]);
+            }
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const float sl2 = 1.4426950408889634f / sqrtf(128.0f);
+        const float al2 = a.alpha * 1.4426950408889634f, bl2 = a.beta * 1.4426950408889634f;
+        const bool biased = a.alpha != 0.f || a.beta != 0.f;
+        const uint32_t* loc = a.loc + (size_t)seq * a.words;
+        const uint32_t* snk = a.snk + (size_t)seq * a.words;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < n_total; ++j) {
+            const int sb = j & 1;
+            if (!warp_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) tmem_ld16(tmem + lane_base + (uint32_t)sb * 128u + (uint32_t)c * 16u, s + c * 16);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+
+            const int key0 = j * 128;
+            uint32_t lw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
+            if (biased) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int wd = (key0 >> 5) + t;
+                    if (wd < a.words) {
+                        lw[t] = loc[wd];
+                        sw[t] = snk[wd];
+                    }
+                }
+            }
+            const bool masked = j >= n_full;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 128; ++k) {
+                float x = s[k] * sl2;
+                if (biased) {
+                    x += ((lw[k >> 5] >> (k & 31)) & 1u) ? al2 : 0.f;
+                    x += ((sw[k >> 5] >> (k & 31)) & 1u) ? bl2 : 0.f;
+                }
+                if (masked && key0 + k > g) x = -INFINITY;
+                s[k] = x;
+                mt = fmaxf(mt, x);
+            }
+            // the previous PV must finish before P is overwritten or O rescaled
+            if (j > 0) {
+                if (!warp_wait(o_done, (uint32_t)(j - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const bool raise = mt > m_run + kRescale;
+            if (__any_sync(0xffffffffu, raise && j > 0)) {
+                const float f = raise ? ex2(m_run - mt) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float o[16];
+                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) o[t] *= f;
+                    tmem_st16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                }
+                if (raise) l_run *= f;
+            }
+            if (raise) m_run = mt;
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                float e[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    // l sums the probabilities as the PV product sees them (bf16)
+                    e[t] = __bfloat162float(__float2bfloat16_rn(ex2(s[c * 8 + t] - m_run)));
+                    ls += e[t];
+                }
+                uint4 v;
+                v.x = pack_bf16(e[0], e[1]);
+                v.y = pack_bf16(e[2], e[3]);
+                v.z = pack_bf16(e[4], e[5]);
+                v.w = pack_bf16(e[6], e[7]);
+                st_shared_v4(tile_chunk(sbase + kOffP, m, c), v);
+            }
+            l_run += ls;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && n_total > 0) {
+            if (!warp_wait(o_done, (uint32_t)(n_total - 1) & 1u)) {
+                ok = false;
+            } else {
+                tc_fence_after();
+                const float inv = 1.0f / l_run;
+                __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float o[16];
+                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                    if (row_valid) {
+                        uint4 v0, v1;
+                        v0.x = pack_bf16(o[0] * inv, o[1] * inv);
+                        v0.y = pack_bf16(o[2] * inv, o[3] * inv);
+                        v0.z = pack_bf16(o[4] * inv, o[5] * inv);
+                        v0.w = pack_bf16(o[6] * inv, o[7] * inv);
+                        v1.x = pack_bf16(o[8] * inv, o[9] * inv);
+                        v1.y = pack_bf16(o[10] * inv, o[11] * inv);
+                        v1.z = pack_bf16(o[12] * inv, o[13] * inv);
+                        v1.w = pack_bf16(o[14] * inv, o[15] * inv);
+                        reinterpret_cast<uint4*>(out + c * 16)[0] = v0;
+                        reinterpret_cast<uint4*>(out + c * 16)[1] = v1;
+                    }
+                }
+            }
+        }
+    }
+    if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads) { return 128 / (n_q_heads / n_kv_heads); }
+
+cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
+    if (a.n_tiles <= 0) return cudaSuccess;
+    if (a.head_dim != 128 || a.n_q_heads / a.n_kv_heads > 128) {
+        if (why) *why = "tensor-core attention needs head_dim 128";
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap tk, tv;
+    const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
+    const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
+    if (!make_tmap_3d_bf16(&tk, a.k_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_3d_bf16(&tv, a.v_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
+        return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(a.n_tiles, a.n_kv_heads);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -100,6 +100,10 @@ WORKLOADS = {
                             alpha=-2.0, beta=-4.0, selection="seams"),
     "qwen1p5b_drift": Workload("qwen1p5b_drift", 4, QWEN1P5B, 4, 32768, 32768, 8192, 492,
                                selection="isolated", range_layers=(10, 15), lora_rank=16),
+    # the Llama-3-8B-shaped refresh cut to 2 layers: a small case (about 1.2 GB
+    # on the device) for kernel profiles of the same launch configuration
+    "llama8b_2l": Workload("llama8b_2l", 1, dataclasses.replace(LLAMA8B, n_layers=2), 1, 8192, 7680, 2048, 282,
+                           selection="units"),
 }
 
 

@@ -123,19 +123,65 @@ def test_empty_selection_is_a_no_op():
     s.close()
 
 
+def scaled_err(got, want):
+    return np.abs(np.asarray(got) - np.asarray(want)) / np.maximum(1.0, np.abs(np.asarray(want)))
+
+
 @pytest.mark.slow
 def test_llama8b_full_size_against_oracle():
     """The Llama-3-8B-shaped workload at full size (32 layers, N = 7680,
     282 positions in units of 32-64), the launch configuration the benchmark
-    times: every refreshed row and every written K/V row at every layer."""
+    times.
+
+    Elementwise tolerance on the K/V rows of the first two layers.  Deeper,
+    this random-weight stack amplifies any rounding difference (in the oracle
+    itself, one bf16 ulp on 1 % of the layer-0 inputs grows to a 1.9 scaled
+    error after 32 layers), so every layer's K/V rows and the final hidden rows
+    are held to a budget instead: the GPU's distance to the exact (unrounded
+    float64) recurrence may be at most twice the bf16 oracle's own distance to
+    it, in RMS and in max (the 2x-native-error budget of the pages' FP32
+    control, Budgeted KV-Cache Repair Sec. 13.5)."""
     w = wl.WORKLOADS["llama8b"]
     s = Setup(w)
-    Ks0, Vs0 = f64(s.K), f64(s.V)
+    Ks0, Vs0 = f64(s.K[0]), f64(s.V[0])
     emb = s.embed
     ids = s.ids.cpu().numpy()
     U = oracle.sorted_positions(s.positions[0])
     X_src = np.zeros((w.capacity, w.model.d_model))
     X_src[U] = f64(emb[torch.from_numpy(ids[0][U].astype(np.int64)).cuda()])
-    worst = run_and_compare(s, LazyWeights(s.layers), Ks0, Vs0, [X_src], TOL["bf16"])
+    K_in, V_in = s.K.clone(), s.V.clone()
+    s.select()
+    s.refresh()
+    s.sync()
+    spec = oracle_spec(w)
+    exact = dataclasses.replace(spec, dtype="f64")
+    W = LazyWeights(s.layers)
+    Xb, Kb, Vb, lb, sb = oracle.refresh_packed(spec, W, Ks0, Vs0, s.local_mask[0], s.sink_mask[0], U, X_src)
+    Xe, Ke, Ve, _, _ = oracle.refresh_packed(exact, W, Ks0, Vs0, s.local_mask[0], s.sink_mask[0], U, X_src)
+    Ut = torch.from_numpy(U)
+    report = []
+    for l in range(w.model.n_layers):
+        for name, G, B, E in (("K", s.K, Kb, Ke), ("V", s.V, Vb, Ve)):
+            g = f64(G[0, l][:, Ut])
+            b, e = B[l][:, U], E[l][:, U]
+            if l < 2:
+                assert_close(g, b, TOL["bf16"], f"{name} layer {l}")
+            eg, eo = scaled_err(g, e), scaled_err(b, e)
+            rg, ro = float(np.sqrt(np.mean(eg ** 2))), float(np.sqrt(np.mean(eo ** 2)))
+            report.append((l, name, rg, ro, float(eg.max()), float(eo.max())))
+            assert rg <= 2 * ro + 1e-4, f"{name} layer {l}: rms error {rg:.3e} vs oracle {ro:.3e}"
+            assert eg.max() <= 2 * eo.max() + 1e-3, f"{name} layer {l}: max error {eg.max():.3e} vs {eo.max():.3e}"
+    g = f64(s.hidden[:len(U)])
+    eg, eo = scaled_err(g, Xe), scaled_err(Xb, Xe)
+    rg, ro = float(np.sqrt(np.mean(eg ** 2))), float(np.sqrt(np.mean(eo ** 2)))
+    print("hidden rms/max gpu", rg, eg.max(), "oracle", ro, eo.max())
+    for r in report[::8]:
+        print("layer %d %s rms gpu %.3e oracle %.3e max gpu %.3e oracle %.3e" % r)
+    assert rg <= 2 * ro + 1e-4 and eg.max() <= 2 * eo.max() + 1e-3
+    keep = torch.ones(w.capacity, dtype=torch.bool, device=s.K.device)
+    keep[Ut.to(s.K.device)] = False
+    assert torch.equal(s.K[0][:, :, keep], K_in[0][:, :, keep])
+    assert torch.equal(s.V[0][:, :, keep], V_in[0][:, :, keep])
+    local_after, sink_after = kvr.kvr_read_meta(s.handle, 1, s.words)
+    np.testing.assert_array_equal(local_after[0], oracle.bitmask_words(lb)[:s.words])
     s.close()
-    print("llama8b worst scaled errors", worst)
