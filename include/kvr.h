@@ -197,6 +197,27 @@ kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_b
                        uint32_t flags, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvr_refresh_layer_noalloc -- kvr_refresh_layer without a caller workspace
+ * and without any allocation.  The paper has no counterpart: this entry point
+ * exists for callers that cannot hand the library scratch memory when they
+ * refresh (a host framework whose allocator owns all device memory, a
+ * serving loop that must not allocate after start-up).
+ *   The layer's scratch lives in one fixed 64 MiB array in device global
+ *   memory inside the library image; every GPU that loads the image holds it
+ *   until the process exits.  A selection whose scratch is larger
+ *   (kvr_workspace_bytes(c, 0) > 64 MiB) is rejected with EINVAL before
+ *   anything is enqueued.
+ *   The first call on a device looks up the array's address; make that call
+ *   before any stream capture on the device.  Calls share the array: calls
+ *   whose GPU work overlaps race on it and must be serialised by the caller.
+ *   The array keeps the last call's contents; a layer never reads scratch it
+ *   has not written in the same call.
+ *   Arguments, results and errors otherwise as kvr_refresh_layer.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_refresh_layer_noalloc(kvr_cache* c, int32_t layer, const kvr_layer_weights* w,
+                                     void* hidden_inout, uint32_t flags, void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvr_attend -- inference mode of operator F ("kv-cross-attention-reuse",
  * Sec. 6.4): attention only, no write-back, with the stored correction masks
  * (type_j = local, j in S') as they are now.

@@ -31,7 +31,8 @@ KVR_K_COUNT = len(KERNELS)
 
 EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace_bytes",
            "kvr_refresh_layer", "kvr_refresh", "kvr_attend", "kvr_sync_status", "kvr_last_error",
-           "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read"]
+           "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read",
+           "kvr_refresh_layer_noalloc"]
 
 
 class kvr_model_desc(C.Structure):
@@ -61,6 +62,7 @@ lib.kvr_select.argtypes = [P, P, P, I32, P, P, I32, P, P, P, P, P]
 lib.kvr_workspace_bytes.argtypes = [P, I32]
 lib.kvr_workspace_bytes.restype = C.c_size_t
 lib.kvr_refresh_layer.argtypes = [P, I32, C.POINTER(kvr_layer_weights), P, P, C.c_size_t, C.c_uint32, P]
+lib.kvr_refresh_layer_noalloc.argtypes = [P, I32, C.POINTER(kvr_layer_weights), P, C.c_uint32, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
@@ -151,6 +153,14 @@ def kvr_refresh_layer(c: int, layer: int, weights: kvr_layer_weights, hidden_ino
                       flags: int = 0, stream=None):
     _check(lib.kvr_refresh_layer(c, layer, C.byref(weights), _ptr(hidden_inout), _ptr(workspace), ws_bytes, flags,
                                  _stream(stream)), "kvr_refresh_layer")
+
+
+def kvr_refresh_layer_noalloc(c: int, layer: int, weights: kvr_layer_weights, hidden_inout, flags: int = 0,
+                              stream=None):
+    """kvr_refresh_layer with the library's fixed 64 MiB device scratch instead of
+    a caller workspace (nothing is allocated)."""
+    _check(lib.kvr_refresh_layer_noalloc(c, layer, C.byref(weights), _ptr(hidden_inout), flags, _stream(stream)),
+           "kvr_refresh_layer_noalloc")
 
 
 def kvr_refresh(c: int, weights_array, layer_begin: int, layer_end: int, hidden_inout, workspace, ws_bytes: int,
