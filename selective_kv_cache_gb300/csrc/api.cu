@@ -40,7 +40,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int dtype_size(int dtype) { return dtype == KVR_BF16 ? 2 : 4; }
 
 struct WsLayout {
-    size_t xn, q, o, h, hn, act, part, total;
+    size_t xn, q, o, h, hn, act, part, part_size, total;
 };
 
 struct Gemms {
@@ -57,10 +57,13 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
     return g;
 }
 
-size_t part_bytes(const kvr_model_desc& m, int R) {
+// The projections' split-K partials and the attention's split-K/V partials
+// share one region: they are never live at the same time.
+size_t part_bytes(const kvr_model_desc& m, int R, int n_tiles, int n_tokens) {
     const Gemms g = plan_all(m, R);
-    return std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
-                    std::max(gemm_partial_bytes(g.gu), gemm_partial_bytes(g.down)));
+    const size_t gemm = std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
+                                 std::max(gemm_partial_bytes(g.gu), gemm_partial_bytes(g.down)));
+    return std::max(gemm, attention_scratch_bytes(m.dtype, n_tiles, m.n_kv_heads, n_tokens));
 }
 
 WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
@@ -75,6 +78,7 @@ WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
     L.hn = off; off = align256(off + (size_t)R * m.d_model * es);
     L.act = off; off = align256(off + (size_t)R * m.ffn_dim * es);
     L.part = off; off = align256(off + part);
+    L.part_size = part;
     L.total = off;
     return L;
 }
@@ -192,6 +196,17 @@ kvr_status check_layer_weights(const kvr_cache* c, const kvr_layer_weights* w) {
     return KVR_OK;
 }
 
+// Point the attention at its split-K/V scratch when the region holds it.
+void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr_cache* c) {
+    const size_t need = attention_scratch_bytes(c->m.dtype, c->sel.n_tiles, c->m.n_kv_heads, c->n_tokens);
+    a->part_o = nullptr;
+    a->part_ml = nullptr;
+    if (need == 0 || !region || bytes < need) return;
+    const size_t o_floats = need / sizeof(float) / 130 * 128;
+    a->part_o = region;
+    a->part_ml = region + o_floats;
+}
+
 // One layer of the packed refresh over the current selection.
 kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* hidden, uint8_t* ws,
                      const WsLayout& L, cudaStream_t s) {
@@ -263,6 +278,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.alpha = c->alpha;
         a.beta = c->beta;
         a.err = c->d_err;
+        set_attention_scratch(&a, part, L.part_size, c);
         cudaError_t e = launch_attention(dt, a, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     }
@@ -318,7 +334,7 @@ kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_by
         return KVR_ESTATE;
     }
     const int R = c->sel.n_rows;
-    *L = layout(c->m, R, part_bytes(c->m, R));
+    *L = layout(c->m, R, part_bytes(c->m, R, c->sel.n_tiles, c->n_tokens));
     if (R == 0) return KVR_OK;
     if (!hidden || !ws) {
         set_error("hidden rows or workspace is NULL");
@@ -651,13 +667,19 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
 size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
     if (!c) return 0;
     int R = max_rows > 0 ? max_rows : c->sel.n_rows;
-    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R)).total;
-    // the split choice changes with the row-tile count: take the largest partial
-    // region over every row count up to max_rows (it peaks at tile-count edges)
+    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R, c->sel.n_tiles, c->n_tokens)).total;
+    // the split choices change with the row count: take the largest partial
+    // region over every row count up to max_rows (the projections' peaks sit at
+    // row-tile edges); query tiles are bounded by R / rows_per_tile + batch
+    int rpt = 1, kpt = 1;
+    attention_tiling(c->m.dtype, c->m.n_q_heads, c->m.n_kv_heads, &rpt, &kpt);
+    auto tiles_for = [&](int r) { return (r + rpt - 1) / rpt + c->batch; };
     const int step = c->m.dtype == KVR_BF16 ? 256 : 64;
     size_t part = 0;
-    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R)));
-    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r));
+    for (int r = step; r < R + step; r += step)
+        part = std::max(part, part_bytes(c->m, std::min(r, R), tiles_for(std::min(r, R)), c->n_tokens));
+    for (int r = 1; r <= std::min(R, 2 * step); ++r)
+        part = std::max(part, part_bytes(c->m, r, tiles_for(r), c->n_tokens));
     return layout(c->m, R, part).total;
 }
 
@@ -708,8 +730,6 @@ kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_b
 
 kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, void* workspace, size_t ws_bytes,
                       void* stream) {
-    (void)workspace;
-    (void)ws_bytes;
     if (!c) {
         set_error("cache is NULL");
         return KVR_EINVAL;
@@ -750,6 +770,8 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
     a.alpha = c->alpha;
     a.beta = c->beta;
     a.err = c->d_err;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+        set_attention_scratch(&a, static_cast<float*>(workspace), ws_bytes, c);
     std::string why;
     Prof p(c, KVR_K_ATTN, s);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);

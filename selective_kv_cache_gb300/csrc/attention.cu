@@ -9,6 +9,11 @@ int attn_simt_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s);
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why);
+size_t attn_tc_scratch_bytes(int n_tiles, int n_kv_heads, int n_tokens);
+
+size_t attention_scratch_bytes(int dtype, int n_tiles, int n_kv_heads, int n_tokens) {
+    return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_tiles, n_kv_heads, n_tokens) : 0;
+}
 
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile) {
     if (dtype == KVR_BF16) {

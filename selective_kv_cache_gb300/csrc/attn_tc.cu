@@ -26,6 +26,8 @@
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kvr_internal.h"
 #include "ptx.cuh"
 
@@ -88,9 +90,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* mma_done = bars + 12;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
 
-    const int tile = blockIdx.x, h = blockIdx.y;
+    const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
-    const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], n_total = plan[5], seq = plan[6];
+    const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], seq = plan[6];
+    // this CTA's share of the query tile's K/V tiles [0, n_total)
+    const int jb = (int)((long long)split * plan[5] / n_split);
+    const int n_total = (int)((long long)(split + 1) * plan[5] / n_split) - jb;   // tiles handled here
     const int G = a.n_q_heads / a.n_kv_heads;
     const int P = 128 / G;
     const int head_index = (seq * a.n_layers + a.layer) * a.n_kv_heads + h;
@@ -153,11 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* kd = smem + kOffK + st * kTile;
                 uint8_t* vd = smem + kOffV + st * kTile;
                 mbar_arrive_expect_tx(&k_full[st], kTile);
-                tma_load_3d(kd, &tmK, &k_full[st], 0, j * 128, head_index);
-                tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, j * 128, head_index);
+                tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + j) * 128, head_index);
+                tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + j) * 128, head_index);
                 mbar_arrive_expect_tx(&v_full[st], kTile);
-                tma_load_3d(vd, &tmV, &v_full[st], 0, j * 128, head_index);
-                tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, j * 128, head_index);
+                tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
+                tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
                 ++issued;
             }
             if (!ok) {
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s_full[st]);
                 return true;
             };
-            ok = n_total > 0 && issue_s(0);
+            if (n_total > 0) ok = issue_s(0);
             for (int j = 0; ok && j < n_total; ++j) {
                 if (j + 1 < n_total && !issue_s(j + 1)) {
                     ok = false;
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[sb]);
 
-            const int key0 = j * 128;
+            const int key0 = (jb + j) * 128;
             uint32_t lw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
             if (biased) {
 #pragma unroll
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            const bool masked = j >= n_full;
+            const bool masked = jb + j >= n_full;
             float mt = -INFINITY;
 #pragma unroll
             for (int k = 0; k < 128; ++k) {
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && n_total > 0) {
             if (!warp_wait(o_done, (uint32_t)(n_total - 1) & 1u)) {
                 ok = false;
-            } else {
+            } else if (n_split == 1) {
                 tc_fence_after();
                 const float inv = 1.0f / l_run;
                 __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
@@ -330,7 +335,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         reinterpret_cast<uint4*>(out + c * 16)[1] = v1;
                     }
                 }
+            } else {
+                // unnormalised fp32 partial plus (running max in base 2, sum) for the combine
+                tc_fence_after();
+                const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
+                float* po = a.part_o + (slot * 128 + m) * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float o[16];
+                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        reinterpret_cast<float4*>(po + c * 16)[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+                }
+                a.part_ml[(slot * 128 + m) * 2] = m_run;
+                a.part_ml[(slot * 128 + m) * 2 + 1] = l_run;
             }
+        } else if (ok && n_split > 1) {
+            // no K/V tile for this split: an empty partial
+            const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
+            a.part_ml[(slot * 128 + m) * 2] = -INFINITY;
+            a.part_ml[(slot * 128 + m) * 2 + 1] = 0.f;
         }
     }
     if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
@@ -343,9 +368,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Merge the split partials of one (query tile, K/V head): one warp per MMA
+// row, 4 output dimensions per lane.  Splits that saw no key are skipped.
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnLaunch a, int n_tiles, int n_split) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int rows_total = n_tiles * a.n_kv_heads * 128;
+    if (warp >= rows_total) return;
+    const int m = warp & 127;
+    const int h = (warp >> 7) % a.n_kv_heads;
+    const int tile = (warp >> 7) / a.n_kv_heads;
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int p = m / G, gi = m % G;
+    const int* plan = a.plan + 8 * tile;
+    if (m >= (128 / G) * G || p >= plan[1]) return;
+    float mx = -INFINITY;
+    for (int s = 0; s < n_split; ++s) {
+        const size_t slot = ((size_t)s * n_tiles + tile) * a.n_kv_heads + h;
+        mx = fmaxf(mx, a.part_ml[(slot * 128 + m) * 2]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+    for (int s = 0; s < n_split; ++s) {
+        const size_t slot = ((size_t)s * n_tiles + tile) * a.n_kv_heads + h;
+        const float ms = a.part_ml[(slot * 128 + m) * 2];
+        if (ms == -INFINITY) continue;
+        const float w = ex2(ms - mx);
+        l += w * a.part_ml[(slot * 128 + m) * 2 + 1];
+        const float4 o = reinterpret_cast<const float4*>(a.part_o + (slot * 128 + m) * 128)[lane];
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+    }
+    const float inv = 1.0f / l;
+    __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan[0] + p) * a.n_q_heads + h * G + gi) * 128;
+    uint2 v;
+    v.x = pack_bf16(acc.x * inv, acc.y * inv);
+    v.y = pack_bf16(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(out)[lane] = v;
+}
+
 }  // namespace
 
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads) { return 128 / (n_q_heads / n_kv_heads); }
+
+// K/V splits per (query tile, head): enough CTAs for two per SM, each split
+// keeping at least four K/V tiles
+int attn_tc_splits(int n_tiles, int n_kv_heads, int n_tokens) {
+    const int pairs = n_tiles * n_kv_heads;
+    const int max_kv_tiles = (n_tokens + 127) / 128;
+    int s = (2 * kNumSMs + pairs - 1) / pairs;
+    s = std::min(s, std::max(1, max_kv_tiles / 4));
+    return std::max(1, std::min(s, 16));
+}
+
+size_t attn_tc_scratch_bytes(int n_tiles, int n_kv_heads, int n_tokens) {
+    const int s = attn_tc_splits(n_tiles, n_kv_heads, n_tokens);
+    if (s <= 1) return 0;
+    return (size_t)s * n_tiles * n_kv_heads * 128 * (128 + 2) * sizeof(float);
+}
 
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
     if (a.n_tiles <= 0) return cudaSuccess;
@@ -353,6 +434,7 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         if (why) *why = "tensor-core attention needs head_dim 128";
         return cudaErrorInvalidValue;
     }
+    int n_split = a.part_o ? attn_tc_splits(a.n_tiles, a.n_kv_heads, a.n_tokens) : 1;
     CUtensorMap tk, tv;
     const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
     const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
@@ -367,8 +449,12 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid(a.n_tiles, a.n_kv_heads);
+    dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
     attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_split == 1) return e;
+    const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
+    attn_combine_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a, a.n_tiles, n_split);
     return cudaGetLastError();
 }
 

@@ -24,46 +24,61 @@
 namespace kvr {
 namespace {
 
-constexpr int kBK = 64;                 // K elements per stage (128 B of bf16)
-constexpr int kTileABytes = 128 * 128;  // 128 rows x 128 B
+constexpr int kBK = 64;                 // K elements per swizzle atom (128 B of bf16)
+constexpr int kTileABytes = 128 * 128;  // 128 rows x 128 B: one atom of A
 constexpr int kGemmThreads = 192;       // warp0 TMA, warp1 MMA, warps2-5 epilogue
 constexpr int kSmemBudget = 227 * 1024;
 
 struct GemmDev {
     float* part;
     int32_t* err;
-    int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols;
+    int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols, items, atoms, packed;
 };
 
+// work item -> (feature tile, row tile, K range); row tiles of one feature tile
+// are consecutive items, so CTAs that run at the same time share weight tiles in L2
+__device__ __forceinline__ void item_coords(const GemmDev& g, int item, int& m_t, int& n_t, int& split, int& kb0,
+                                            int& kb1) {
+    n_t = item % g.n_tiles;
+    const int rest = item / g.n_tiles;
+    m_t = rest % g.m_tiles;
+    split = rest / g.m_tiles;
+    const int KB = g.K / (kBK * g.atoms);
+    kb0 = (int)((long long)split * KB / g.splits);
+    kb1 = (int)((long long)(split + 1) * KB / g.splits);
+}
+
+// Persistent: one CTA per SM walks items blockIdx.x, +gridDim.x, ...  The TMA
+// ring runs across item boundaries, and the TMEM accumulator is double
+// buffered, so the epilogue of one item overlaps the main loop of the next.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmDev g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int BN = g.BN, stages = g.stages;
-    const int tileB = BN * 128;
+    const int BN = g.BN, stages = g.stages, atoms = g.atoms;
+    const int tileB = BN * 128;                    // one atom of B
+    const int stA = atoms * kTileABytes, stB = atoms * tileB;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + (size_t)stages * kTileABytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)stages * tileB);
+    uint8_t* sB = smem + (size_t)stages * stA;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)stages * stB);
     uint64_t* empty = full + stages;
-    uint64_t* accum = empty + stages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
-
-    const int bid = blockIdx.x;
-    const int n_t = bid % g.n_tiles;
-    const int m_t = (bid / g.n_tiles) % g.m_tiles;
-    const int split = bid / (g.n_tiles * g.m_tiles);
-    const int KB = g.K / kBK;
-    const int kb0 = (int)((long long)split * KB / g.splits);
-    const int kb1 = (int)((long long)(split + 1) * KB / g.splits);
-    const int nk = kb1 - kb0;
+    uint64_t* acc_full = empty + stages;   // [2]
+    uint64_t* acc_empty = acc_full + 2;    // [2]
+    uint64_t* mma_done = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t acc_stride = (uint32_t)g.tmem_cols / 2u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(mma_done, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -81,70 +96,108 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
 
     if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % stages;
-                const uint32_t ph = (uint32_t)(i / stages) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u)) {
-                    ok = false;
-                    break;
+            int it = 0;
+            for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+                int m_t, n_t, split, kb0, kb1;
+                item_coords(g, item, m_t, n_t, split, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % stages;
+                    if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(stA + stB));
+                    for (int a = 0; a < atoms; ++a) {
+                        const int kx = (kb * atoms + a) * kBK;
+                        if (g.packed)   // tile (m_t, kx/64) is one contiguous 16 KB block
+                            tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], 0,
+                                        (m_t * (g.K / kBK) + kx / kBK) * 128);
+                        else
+                            tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], kx, m_t * 128);
+                        tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], kx, n_t * BN);
+                    }
                 }
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(kTileABytes + tileB));
-                tma_load_2d(sA + (size_t)s * kTileABytes, &tmA, &full[s], (kb0 + i) * kBK, m_t * 128);
-                tma_load_2d(sB + (size_t)s * tileB, &tmB, &full[s], (kb0 + i) * kBK, n_t * BN);
-                ++issued;
             }
             if (!ok) {  // let every copy still in flight land before the CTA exits
-                for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i)
+                for (int i = (it > stages ? it - stages : 0); i < it; ++i)
                     mbar_wait(&full[i % stages], (uint32_t)(i / stages) & 1u);
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(128, BN, 0, 0);
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % stages;
-                const uint32_t ph = (uint32_t)(i / stages) & 1u;
-                if (!mbar_wait(&full[s], ph)) {
+            int it = 0, local = 0;
+            for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x, ++local) {
+                int m_t, n_t, split, kb0, kb1;
+                item_coords(g, item, m_t, n_t, split, kb0, kb1);
+                const int ab = local & 1;
+                if (!mbar_wait(&acc_empty[ab], ((uint32_t)(local >> 1) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + (size_t)s * kTileABytes);
-                const uint32_t b0 = smem_u32(sB + (size_t)s * tileB);
+                const uint32_t d = tmem + (uint32_t)ab * acc_stride;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % stages;
+                    if (!mbar_wait(&full[s], (uint32_t)(it / stages) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int a = 0; a < atoms; ++a) {
+                        const uint32_t a0 = smem_u32(sA + (size_t)s * stA + a * kTileABytes);
+                        const uint32_t b0 = smem_u32(sB + (size_t)s * stB + a * tileB);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    mma_bf16(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
-                             (i | kk) != 0);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            mma_bf16(d, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
+                                     idesc, (kb > kb0 || a > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&empty[s]);
                 }
-                mma_commit(&empty[s]);
+                if (!ok) break;
+                mma_commit(&acc_full[ab]);
             }
-            mma_commit(accum);
-            if (!ok) mbar_wait(accum, 0);
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0);
         }
     } else {
-        // one lane polls, the warp follows it: tcgen05.ld needs a converged warp
-        int got = 0;
-        if (lane == 0) got = mbar_wait(accum, 0) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-            ok = false;
-        } else {
+        // ------------------------------------------------------------ epilogue: TMEM -> fp32 partials
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        for (int item = blockIdx.x; item < g.items; item += gridDim.x, ++local) {
+            int m_t, n_t, split, kb0, kb1;
+            item_coords(g, item, m_t, n_t, split, kb0, kb1);
+            const int ab = local & 1;
+            // one lane polls, the warp follows: tcgen05.ld needs a converged warp
+            int got = 0;
+            if (lane == 0) got = mbar_wait(&acc_full[ab], (uint32_t)(local >> 1) & 1u) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const int q = warp & 3;
             const int feat = m_t * 128 + q * 32 + lane;
-            float* out = g.part + (size_t)split * g.R * g.n_out;
+            float* out = g.part + (size_t)split * g.R * g.n_out + feat;
             const int tok0 = n_t * BN;
+            const uint32_t src = tmem + lane_base + (uint32_t)ab * acc_stride;
             for (int c = 0; c < BN; c += 16) {
                 float v[16];
-                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+                tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int tok = tok0 + c + j;
-                    if (tok < g.R) out[(size_t)tok * g.n_out + feat] = v[j];
+                    if (tok < g.R) out[(size_t)tok * g.n_out] = v[j];
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
         }
     }
     if (!ok) atomicOr(g.err, DEV_ERR_TIMEOUT);
@@ -205,6 +258,22 @@ __global__ void __launch_bounds__(256) gemm_f32_simt_kernel(const float* __restr
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+// packed[((m * KB + kb) * 128 + r) * 64 + c] = w[(m * 128 + r) * K + kb * 64 + c]: every
+// 128 x 64 tile of a weight matrix becomes one contiguous 16 KB block, so the
+// projection's TMA reads stream whole blocks instead of 128-B pieces of 128 rows
+__global__ void pack_weight_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int n_out, int K) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // 16-B chunk of the output
+    const long long total = (long long)n_out * K / 8;
+    if (i >= total) return;
+    const int c8 = (int)(i & 7);                 // 8 chunks per 64-element tile row
+    const long long row = i >> 3;                // packed row = (m * KB + kb) * 128 + r
+    const int r = (int)(row & 127);
+    const long long tile = row >> 7;
+    const int KB = K / 64;
+    const int kb = (int)(tile % KB), m = (int)(tile / KB);
+    out[i] = w[((long long)(m * 128 + r) * K + kb * 64) / 8 + c8];
+}
+
 }  // namespace
 
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
@@ -220,35 +289,45 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
         const int ctas = p.m_tiles * p.n_tiles;
         p.splits = std::max(1, std::min(KB / 4, (2 * kNumSMs) / std::max(1, ctas)));
         p.stages = 0;
+        p.atoms = 1;
         return p;
     }
     p.m_tiles = n_out / 128;
     p.n_tiles = std::max(1, (R + 255) / 256);
     p.BN = std::max(16, round_up((R + p.n_tiles - 1) / p.n_tiles, 16));
-    const int KB = K / kBK;
-    // pick the number of K splits that best fills whole waves of CTAs
-    const int tiles = p.m_tiles * p.n_tiles;
+    // K depth per pipeline stage: up to 4 swizzle atoms (256 elements, 512 B
+    // of each weight row), so each TMA round reads longer runs of every row
+    p.atoms = (K % (2 * kBK) == 0) ? 2 : 1;
+    const int KB = K / (kBK * p.atoms);
     const int tileB = p.BN * 128;
-    int stages = std::min(8, (kSmemBudget - 1024 - 256) / (kTileABytes + tileB));
-    const int per_sm = (2 * (kTileABytes + tileB) * 3 + 2048 <= kSmemBudget && p.BN <= 128) ? 2 : 1;
-    if (per_sm == 2) stages = 3;
-    p.stages = stages;
-    const int slots = kNumSMs * per_sm;
+    p.stages = std::min(8, (kSmemBudget - 1024 - 256) / (p.atoms * (kTileABytes + tileB)));
+    // K splits from a cost model fitted to measurements on GB300: one item
+    // streams its (128 + BN) x (K / S) operand tiles at ~100 GB/s per SM, the
+    // persistent grid runs ceil(items / 152) rounds, and every split adds an
+    // fp32 partial round trip of R x n_out at ~6 TB/s.
+    const int tiles = p.m_tiles * p.n_tiles;
     int best = 1;
-    double best_eff = 0.0;
+    double best_t = 1e30;
     const int max_split = std::max(1, std::min(KB / 2, 16));
     for (int s = 1; s <= max_split; ++s) {
-        const long long ctas = (long long)tiles * s;
-        const long long waves = (ctas + slots - 1) / slots;
-        const double eff = (double)ctas / (double)(waves * slots);
-        // each extra split costs a partial tile round trip: prefer fewer when close
-        if (eff > best_eff + 0.05) {
-            best_eff = eff;
+        const long long items = (long long)tiles * s;
+        const long long rounds = (items + kNumSMs - 1) / kNumSMs;
+        const double t = (double)rounds * (128.0 + p.BN) * ((double)K / s) * 2.0 / 100e9 +
+                         2.0 * s * (double)R * n_out * 4.0 / 6e12;
+        if (t < best_t * 0.97) {
+            best_t = t;
             best = s;
         }
     }
     p.splits = best;
     return p;
+}
+
+cudaError_t launch_pack_weight(const void* w, void* packed, int n_out, int K, cudaStream_t s) {
+    const long long chunks = (long long)n_out * K / 8;
+    if (chunks <= 0) return cudaSuccess;
+    pack_weight_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, s>>>((const uint4*)w, (uint4*)packed, n_out, K);
+    return cudaGetLastError();
 }
 
 size_t gemm_partial_bytes(const GemmPlan& p) { return (size_t)p.splits * p.R * p.n_out * sizeof(float); }
@@ -263,8 +342,12 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         return cudaGetLastError();
     }
     CUtensorMap ta, tb;
-    if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why))
+    if (p.packed) {
+        if (!make_tmap_2d_bf16(&ta, w, kBK, (uint64_t)p.n_out * (p.K / kBK), kBK * 2, kBK, 128, why))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why)) {
         return cudaErrorInvalidValue;
+    }
     if (!make_tmap_2d_bf16(&tb, x, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.K * 2, kBK, (uint32_t)p.BN, why))
         return cudaErrorInvalidValue;
     GemmDev g;
@@ -278,10 +361,14 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     g.n_tiles = p.n_tiles;
     g.splits = p.splits;
     g.stages = p.stages;
+    g.items = p.m_tiles * p.n_tiles * p.splits;
+    g.atoms = p.atoms;
+    g.packed = p.packed;
     int cols = 32;
-    while (cols < p.BN) cols <<= 1;
+    while (cols < 2 * p.BN) cols <<= 1;   // two accumulators
     g.tmem_cols = cols;
-    const size_t smem = 1024 + (size_t)p.stages * (kTileABytes + p.BN * 128) + (2 * p.stages + 1) * 8 + 16;
+    const size_t smem =
+        1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + (2 * p.stages + 5) * 8 + 16;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -289,7 +376,7 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const unsigned grid = (unsigned)(p.m_tiles * p.n_tiles * p.splits);
+    const unsigned grid = (unsigned)std::min(g.items, kNumSMs);
     gemm_bf16_tc_kernel<<<grid, kGemmThreads, smem, s>>>(ta, tb, g);
     return cudaGetLastError();
 }

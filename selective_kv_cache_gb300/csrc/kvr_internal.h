@@ -118,10 +118,12 @@ cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w,
 // GEMM partials: part[split][r][f] = sum_{k in split} x[r][k] * w[f][k]
 struct GemmPlan {
     int n_out, K, R;
-    int m_tiles, n_tiles, BN, splits, stages;
+    int m_tiles, n_tiles, BN, splits, stages, atoms;
+    int packed;   // weights in the tile-contiguous layout of kvr_pack_weight
 };
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
 size_t gemm_partial_bytes(const GemmPlan& p);
+cudaError_t launch_pack_weight(const void* w, void* packed, int n_out, int K, cudaStream_t s);
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
                         cudaStream_t s, std::string* why);
 
@@ -160,10 +162,14 @@ struct AttnLaunch {
     int n_tiles, n_q_heads, n_kv_heads, head_dim, layer, n_layers, capacity, n_tokens, words, batch;
     float alpha, beta;
     int32_t* err;
+    float* part_o;             // nullable: split-K/V partials [splits][tiles][H_kv][128][128]
+    float* part_ml;            // [splits][tiles][H_kv][128][2] (running max in base 2, sum)
 };
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why);
 // Query tile geometry of the attention kernel for a model.
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile);
+// Scratch bytes the attention kernel uses for its split-K/V partials (0 = unsplit).
+size_t attention_scratch_bytes(int dtype, int n_tiles, int n_kv_heads, int n_tokens);
 
 }  // namespace kvr
 

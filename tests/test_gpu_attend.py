@@ -32,11 +32,16 @@ def test_attend_matches_oracle(dtype, alpha, beta):
     m = w.model
     q = torch.randn(R, m.n_q_heads, m.head_dim, device="cuda").to(m.torch_dtype)
     out = torch.empty(R, m.n_q_heads * m.head_dim, device="cuda", dtype=m.torch_dtype)
+    ws = torch.empty(kvr.kvr_workspace_bytes(s.handle, 0), dtype=torch.uint8, device="cuda")
     for layer in range(m.n_layers):
-        kvr.kvr_attend(s.handle, layer, q, out)
-        s.sync()
         want = oracle.attend(f64(q), f64(s.K[0, layer]), f64(s.V[0, layer]), s.positions[0],
                              local[0], sink[0], alpha, beta).reshape(R, -1)
-        assert_close(f64(out), want, TOL[dtype], f"attend layer {layer}")
+        # without a workspace the kernel runs unsplit; with one it may split each
+        # query tile's K/V range over several CTAs and merge their partials
+        for workspace in (None, ws):
+            out.zero_()
+            kvr.kvr_attend(s.handle, layer, q, out, workspace, 0 if workspace is None else ws.numel())
+            s.sync()
+            assert_close(f64(out), want, TOL[dtype], f"attend layer {layer} workspace={workspace is not None}")
     assert torch.equal(s.K, K_in)
     s.close()

@@ -133,11 +133,13 @@ def test_llama8b_full_size_against_oracle():
     282 positions in units of 32-64), the launch configuration the benchmark
     times.
 
-    Elementwise tolerance on the K/V rows of the first two layers.  Deeper,
-    this random-weight stack amplifies any rounding difference (in the oracle
-    itself, one bf16 ulp on 1 % of the layer-0 inputs grows to a 1.9 scaled
-    error after 32 layers), so every layer's K/V rows and the final hidden rows
-    are held to a budget instead: the GPU's distance to the exact (unrounded
+    Elementwise tolerance on the K/V rows of layer 0, whose inputs are the
+    same embedding rows on both sides.  From layer 1 on, each side reads its
+    own rounded layer outputs, and this random-weight stack amplifies any
+    rounding difference (in the oracle itself, one bf16 ulp on 1 % of the
+    layer-0 inputs is already 2.3e-2 at layer 1 and grows to a 1.9 scaled
+    error after 32 layers).  So every layer's K/V rows and the final hidden
+    rows are held to a budget: the GPU's distance to the exact (unrounded
     float64) recurrence may be at most twice the bf16 oracle's own distance to
     it, in RMS and in max (the 2x-native-error budget of the pages' FP32
     control, Budgeted KV-Cache Repair Sec. 13.5)."""
@@ -164,7 +166,7 @@ def test_llama8b_full_size_against_oracle():
         for name, G, B, E in (("K", s.K, Kb, Ke), ("V", s.V, Vb, Ve)):
             g = f64(G[0, l][:, Ut])
             b, e = B[l][:, U], E[l][:, U]
-            if l < 2:
+            if l == 0:
                 assert_close(g, b, TOL["bf16"], f"{name} layer {l}")
             eg, eo = scaled_err(g, e), scaled_err(b, e)
             rg, ro = float(np.sqrt(np.mean(eg ** 2))), float(np.sqrt(np.mean(eo ** 2)))
