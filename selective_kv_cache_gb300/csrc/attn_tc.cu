@@ -234,8 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             float s[128];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) tmem_ld16(tmem + lane_base + (uint32_t)sb * 128u + (uint32_t)c * 16u, s + c * 16);
+            tmem_ld32x4(tmem + lane_base + (uint32_t)sb * 128u, s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[sb]);
@@ -287,23 +286,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (raise) l_run *= f;
             }
             if (raise) m_run = mt;
-            float ls = 0.f;
+            float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                float e[8];
+                uint32_t pk[4];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    // l sums the probabilities as the PV product sees them (bf16)
-                    e[t] = __bfloat162float(__float2bfloat16_rn(ex2(s[c * 8 + t] - m_run)));
-                    ls += e[t];
+                for (int t = 0; t < 4; ++t) {
+                    pk[t] = pack_bf16(ex2(s[c * 8 + 2 * t] - m_run), ex2(s[c * 8 + 2 * t + 1] - m_run));
+                    // l sums the probabilities exactly as the PV product sees them (bf16)
+                    ls0 += __uint_as_float(pk[t] << 16);
+                    ls1 += __uint_as_float(pk[t] & 0xffff0000u);
                 }
-                uint4 v;
-                v.x = pack_bf16(e[0], e[1]);
-                v.y = pack_bf16(e[2], e[3]);
-                v.z = pack_bf16(e[4], e[5]);
-                v.w = pack_bf16(e[6], e[7]);
-                st_shared_v4(tile_chunk(sbase + kOffP, m, c), v);
+                st_shared_v4(tile_chunk(sbase + kOffP, m, c), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
+            const float ls = ls0 + ls1;
             l_run += ls;
             fence_proxy_async_smem();
             tc_fence_before();

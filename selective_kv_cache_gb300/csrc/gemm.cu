@@ -32,7 +32,7 @@ constexpr int kSmemBudget = 227 * 1024;
 struct GemmDev {
     float* part;
     int32_t* err;
-    int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols, items, atoms, packed;
+    int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols, items, atoms;
 };
 
 // work item -> (feature tile, row tile, K range); row tiles of one feature tile
@@ -111,11 +111,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(stA + stB));
                     for (int a = 0; a < atoms; ++a) {
                         const int kx = (kb * atoms + a) * kBK;
-                        if (g.packed)   // tile (m_t, kx/64) is one contiguous 16 KB block
-                            tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], 0,
-                                        (m_t * (g.K / kBK) + kx / kBK) * 128);
-                        else
-                            tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], kx, m_t * 128);
+                        tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], kx, m_t * 128);
                         tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], kx, n_t * BN);
                     }
                 }
@@ -258,22 +254,6 @@ __global__ void __launch_bounds__(256) gemm_f32_simt_kernel(const float* __restr
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// packed[((m * KB + kb) * 128 + r) * 64 + c] = w[(m * 128 + r) * K + kb * 64 + c]: every
-// 128 x 64 tile of a weight matrix becomes one contiguous 16 KB block, so the
-// projection's TMA reads stream whole blocks instead of 128-B pieces of 128 rows
-__global__ void pack_weight_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int n_out, int K) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // 16-B chunk of the output
-    const long long total = (long long)n_out * K / 8;
-    if (i >= total) return;
-    const int c8 = (int)(i & 7);                 // 8 chunks per 64-element tile row
-    const long long row = i >> 3;                // packed row = (m * KB + kb) * 128 + r
-    const int r = (int)(row & 127);
-    const long long tile = row >> 7;
-    const int KB = K / 64;
-    const int kb = (int)(tile % KB), m = (int)(tile / KB);
-    out[i] = w[((long long)(m * 128 + r) * K + kb * 64) / 8 + c8];
-}
-
 }  // namespace
 
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
@@ -323,13 +303,6 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
     return p;
 }
 
-cudaError_t launch_pack_weight(const void* w, void* packed, int n_out, int K, cudaStream_t s) {
-    const long long chunks = (long long)n_out * K / 8;
-    if (chunks <= 0) return cudaSuccess;
-    pack_weight_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, s>>>((const uint4*)w, (uint4*)packed, n_out, K);
-    return cudaGetLastError();
-}
-
 size_t gemm_partial_bytes(const GemmPlan& p) { return (size_t)p.splits * p.R * p.n_out * sizeof(float); }
 
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
@@ -342,12 +315,8 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         return cudaGetLastError();
     }
     CUtensorMap ta, tb;
-    if (p.packed) {
-        if (!make_tmap_2d_bf16(&ta, w, kBK, (uint64_t)p.n_out * (p.K / kBK), kBK * 2, kBK, 128, why))
-            return cudaErrorInvalidValue;
-    } else if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why)) {
+    if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why))
         return cudaErrorInvalidValue;
-    }
     if (!make_tmap_2d_bf16(&tb, x, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.K * 2, kBK, (uint32_t)p.BN, why))
         return cudaErrorInvalidValue;
     GemmDev g;
@@ -363,7 +332,6 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     g.stages = p.stages;
     g.items = p.m_tiles * p.n_tiles * p.splits;
     g.atoms = p.atoms;
-    g.packed = p.packed;
     int cols = 32;
     while (cols < 2 * p.BN) cols <<= 1;   // two accumulators
     g.tmem_cols = cols;

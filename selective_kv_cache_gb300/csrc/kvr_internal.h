@@ -119,11 +119,9 @@ cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w,
 struct GemmPlan {
     int n_out, K, R;
     int m_tiles, n_tiles, BN, splits, stages, atoms;
-    int packed;   // weights in the tile-contiguous layout of kvr_pack_weight
 };
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
 size_t gemm_partial_bytes(const GemmPlan& p);
-cudaError_t launch_pack_weight(const void* w, void* packed, int n_out, int K, cudaStream_t s);
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
                         cudaStream_t s, std::string* why);
 
