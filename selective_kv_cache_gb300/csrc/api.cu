@@ -59,11 +59,15 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
 
 // The projections' split-K partials and the attention's split-K/V partials
 // share one region: they are never live at the same time.
-size_t part_bytes(const kvr_model_desc& m, int R, int n_tiles, int n_tokens) {
+size_t part_bytes(const kvr_model_desc& m, int R, size_t attn_scratch) {
     const Gemms g = plan_all(m, R);
     const size_t gemm = std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
                                  std::max(gemm_partial_bytes(g.gu), gemm_partial_bytes(g.down)));
-    return std::max(gemm, attention_scratch_bytes(m.dtype, n_tiles, m.n_kv_heads, n_tokens));
+    return std::max(gemm, attn_scratch);
+}
+
+size_t sel_attn_scratch(const kvr_cache* c) {
+    return attention_scratch_bytes(c->m.dtype, c->sel.attn_split, c->sel.n_tiles, c->m.n_kv_heads);
 }
 
 WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
@@ -198,9 +202,11 @@ kvr_status check_layer_weights(const kvr_cache* c, const kvr_layer_weights* w) {
 
 // Point the attention at its split-K/V scratch when the region holds it.
 void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr_cache* c) {
-    const size_t need = attention_scratch_bytes(c->m.dtype, c->sel.n_tiles, c->m.n_kv_heads, c->n_tokens);
+    const size_t need = sel_attn_scratch(c);
     a->part_o = nullptr;
     a->part_ml = nullptr;
+    a->chunk = c->sel.attn_chunk;
+    a->n_split = c->sel.attn_split;
     if (need == 0 || !region || bytes < need) return;
     const size_t o_floats = need / sizeof(float) / 130 * 128;
     a->part_o = region;
@@ -334,7 +340,7 @@ kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_by
         return KVR_ESTATE;
     }
     const int R = c->sel.n_rows;
-    *L = layout(c->m, R, part_bytes(c->m, R, c->sel.n_tiles, c->n_tokens));
+    *L = layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c)));
     if (R == 0) return KVR_OK;
     if (!hidden || !ws) {
         set_error("hidden rows or workspace is NULL");
@@ -569,6 +575,7 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
     sel.tile_off.resize(B);
     attention_tiling(c->m.dtype, c->m.n_q_heads, c->m.n_kv_heads, &sel.rows_per_tile, &sel.keys_per_tile);
     int rows = 0, ivs = 0, tiles = 0;
+    std::vector<int> tile_kv;
     for (int i = 0; i < B; ++i) {
         std::fill(mark.begin(), mark.end(), 0);
         for (int k = 0; k < counts[i]; ++k) {
@@ -584,9 +591,15 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
             }
             mark[p] = 1;
         }
-        int iv = 0;
-        for (int t = c->suffix_start; t < c->n_tokens; ++t)
-            if (mark[t] && (t == 0 || !mark[t - 1])) ++iv;
+        int iv = 0, row = 0;
+        for (int t = c->suffix_start; t < c->n_tokens; ++t) {
+            if (!mark[t]) continue;
+            if (t == 0 || !mark[t - 1]) ++iv;
+            // K/V tiles the attention walks for each query tile: up to its last row
+            if (row % sel.rows_per_tile == sel.rows_per_tile - 1 || row == counts[i] - 1)
+                tile_kv.push_back((t + 1 + sel.keys_per_tile - 1) / sel.keys_per_tile);
+            ++row;
+        }
         sel.row_off[i] = rows;
         sel.iv_off[i] = ivs;
         sel.iv_count[i] = iv;
@@ -604,6 +617,7 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
     sel.n_rows = rows;
     sel.n_intervals = ivs;
     sel.n_tiles = tiles;
+    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split);
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the staging buffer may still feed the previous upload
@@ -667,19 +681,16 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
 size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
     if (!c) return 0;
     int R = max_rows > 0 ? max_rows : c->sel.n_rows;
-    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R, c->sel.n_tiles, c->n_tokens)).total;
-    // the split choices change with the row count: take the largest partial
-    // region over every row count up to max_rows (the projections' peaks sit at
-    // row-tile edges); query tiles are bounded by R / rows_per_tile + batch
-    int rpt = 1, kpt = 1;
-    attention_tiling(c->m.dtype, c->m.n_q_heads, c->m.n_kv_heads, &rpt, &kpt);
-    auto tiles_for = [&](int r) { return (r + rpt - 1) / rpt + c->batch; };
+    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c))).total;
+    // the projections' split choice changes with the row count: take the
+    // largest partial region over every row count up to max_rows (it peaks at
+    // row-tile edges); a split attention never uses more than kAttnMaxSplitCTAs
+    // CTAs' worth of partials
+    const size_t attn = c->m.dtype == KVR_BF16 ? (size_t)kAttnMaxSplitCTAs * 128 * 130 * sizeof(float) : 0;
     const int step = c->m.dtype == KVR_BF16 ? 256 : 64;
     size_t part = 0;
-    for (int r = step; r < R + step; r += step)
-        part = std::max(part, part_bytes(c->m, std::min(r, R), tiles_for(std::min(r, R)), c->n_tokens));
-    for (int r = 1; r <= std::min(R, 2 * step); ++r)
-        part = std::max(part, part_bytes(c->m, r, tiles_for(r), c->n_tokens));
+    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R), attn));
+    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r, attn));
     return layout(c->m, R, part).total;
 }
 

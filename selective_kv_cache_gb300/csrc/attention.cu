@@ -1,6 +1,8 @@
 // attention.cu -- picks the attention kernel for the model dtype and reports
 // its query-tile geometry (the plan is built over these tiles): the
 // tensor-core kernel for bf16 models, the CUDA-core kernel for fp32 models.
+#include <algorithm>
+
 #include "kvr_internal.h"
 
 namespace kvr {
@@ -9,10 +11,37 @@ int attn_simt_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s);
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why);
-size_t attn_tc_scratch_bytes(int n_tiles, int n_kv_heads, int n_tokens);
+size_t attn_tc_scratch_bytes(int n_split, int n_tiles, int n_kv_heads);
 
-size_t attention_scratch_bytes(int dtype, int n_tiles, int n_kv_heads, int n_tokens) {
-    return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_tiles, n_kv_heads, n_tokens) : 0;
+size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_heads) {
+    return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_split, n_tiles, n_kv_heads) : 0;
+}
+
+// Pick the chunk size C that minimises the modelled time: CTAs run one per
+// SM, a CTA costs ~6 tile-times of set-up plus one per K/V tile of its chunk,
+// and a launch takes ceil(CTAs / SMs) rounds of its longest chunk; a split
+// adds the merge.  tile_kv[t] = K/V tiles of query tile t.
+void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
+    *chunk = 1 << 30;
+    *n_split = 1;
+    if (dtype != KVR_BF16 || tile_kv.empty()) return;
+    int max_kv = 1;
+    for (int v : tile_kv) max_kv = std::max(max_kv, v);
+    double best = 1e30;
+    for (int C = max_kv; C >= 2; --C) {
+        long long ctas = 0;
+        for (int v : tile_kv) ctas += (long long)n_kv_heads * ((v + C - 1) / C);
+        const int splits = (max_kv + C - 1) / C;
+        if (splits > 1 && (long long)splits * (long long)tile_kv.size() * n_kv_heads > kAttnMaxSplitCTAs) break;
+        const long long rounds = (ctas + kNumSMs - 1) / kNumSMs;
+        const double t = (double)rounds * (std::min(C, max_kv) + 6.0) + (splits > 1 ? 2.0 : 0.0);
+        if (t < best * 0.98) {
+            best = t;
+            *chunk = C;
+            *n_split = splits;
+        }
+    }
+    if (*n_split == 1) *chunk = 1 << 30;
 }
 
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile) {

@@ -37,11 +37,13 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
+constexpr int kKStages = 3;                     // K runs ahead of V: S needs K first
+constexpr int kVStages = 2;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffP = kTile;
-constexpr uint32_t kOffK = 2 * kTile;           // 2 stages
-constexpr uint32_t kOffV = 4 * kTile;           // 2 stages
-constexpr uint32_t kOffBar = 6 * kTile;
+constexpr uint32_t kOffK = 2 * kTile;
+constexpr uint32_t kOffV = kOffK + kKStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
 
@@ -80,22 +82,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* k_full = bars + 0;     // [2]
-    uint64_t* v_full = bars + 2;     // [2]
-    uint64_t* kv_empty = bars + 4;   // [2]
-    uint64_t* s_full = bars + 6;     // [2]
-    uint64_t* s_free = bars + 8;     // [2]
-    uint64_t* p_full = bars + 10;
-    uint64_t* o_done = bars + 11;
-    uint64_t* mma_done = bars + 12;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    uint64_t* k_full = bars + 0;     // [3]
+    uint64_t* k_empty = bars + 3;    // [3]
+    uint64_t* v_full = bars + 6;     // [2]
+    uint64_t* v_empty = bars + 8;    // [2]
+    uint64_t* s_full = bars + 10;    // [2]
+    uint64_t* s_free = bars + 12;    // [2]
+    uint64_t* p_full = bars + 14;
+    uint64_t* o_done = bars + 15;
+    uint64_t* mma_done = bars + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
 
     const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
     const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], seq = plan[6];
-    // this CTA's share of the query tile's K/V tiles [0, n_total)
-    const int jb = (int)((long long)split * plan[5] / n_split);
-    const int n_total = (int)((long long)(split + 1) * plan[5] / n_split) - jb;   // tiles handled here
+    // this CTA's chunk of the query tile's K/V tiles [0, plan n_total)
+    const int jb = split * a.chunk;
+    const int n_total = min(plan[5], jb + a.chunk) - jb;   // tiles handled here
+    if (n_split > 1 && n_total <= 0) {
+        // nothing to read: an empty partial for the merge, and no set-up at all
+        if (threadIdx.x < 128) {
+            const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
+            a.part_ml[(slot * 128 + threadIdx.x) * 2] = -INFINITY;
+            a.part_ml[(slot * 128 + threadIdx.x) * 2 + 1] = 0.f;
+        }
+        return;
+    }
     const int G = a.n_q_heads / a.n_kv_heads;
     const int P = 128 / G;
     const int head_index = (seq * a.n_layers + a.layer) * a.n_kv_heads + h;
@@ -103,10 +115,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
         }
@@ -147,29 +162,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // issue order K_0, K_1 V_0, K_2 V_1, ...: K stays one tile ahead of V
         if (lane == 0) {
-            int issued = 0;
-            for (int j = 0; j < n_total; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(&kv_empty[st], ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
-                    ok = false;
-                    break;
+            int k_issued = 0, v_issued = 0;
+            for (int t = 0; t <= n_total && ok; ++t) {
+                if (t < n_total) {
+                    const int st = t % kKStages;
+                    if (!mbar_wait(&k_empty[st], ((uint32_t)(t / kKStages) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* kd = smem + kOffK + st * kTile;
+                    mbar_arrive_expect_tx(&k_full[st], kTile);
+                    tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + t) * 128, head_index);
+                    tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + t) * 128, head_index);
+                    ++k_issued;
                 }
-                uint8_t* kd = smem + kOffK + st * kTile;
-                uint8_t* vd = smem + kOffV + st * kTile;
-                mbar_arrive_expect_tx(&k_full[st], kTile);
-                tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + j) * 128, head_index);
-                tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + j) * 128, head_index);
-                mbar_arrive_expect_tx(&v_full[st], kTile);
-                tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
-                tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
-                ++issued;
+                if (t >= 1) {
+                    const int j = t - 1, st = j % kVStages;
+                    if (!mbar_wait(&v_empty[st], ((uint32_t)(j / kVStages) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* vd = smem + kOffV + st * kTile;
+                    mbar_arrive_expect_tx(&v_full[st], kTile);
+                    tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
+                    tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
+                    ++v_issued;
+                }
             }
-            if (!ok) {
-                for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-                    mbar_wait(&k_full[j & 1], (uint32_t)(j >> 1) & 1u);
-                    mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
-                }
+            if (!ok) {  // let every copy still in flight land before the CTA exits
+                for (int j = (k_issued > kKStages ? k_issued - kKStages : 0); j < k_issued; ++j)
+                    mbar_wait(&k_full[j % kKStages], (uint32_t)(j / kKStages) & 1u);
+                for (int j = (v_issued > kVStages ? v_issued - kVStages : 0); j < v_issued; ++j)
+                    mbar_wait(&v_full[j % kVStages], (uint32_t)(j / kVStages) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -178,18 +204,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);   // V is MN-major
             auto issue_s = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!mbar_wait(&k_full[st], (uint32_t)(j >> 1) & 1u)) return false;
-                if (j >= 2 && !mbar_wait(&s_free[st], (uint32_t)((j - 2) >> 1) & 1u)) return false;
+                const int kst = j % kKStages, sb = j & 1;
+                if (!mbar_wait(&k_full[kst], (uint32_t)(j / kKStages) & 1u)) return false;
+                if (j >= 2 && !mbar_wait(&s_free[sb], (uint32_t)((j - 2) >> 1) & 1u)) return false;
                 tc_fence_after();
-                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + st * kTile;
+                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + kst * kTile;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16(tmem + (uint32_t)st * 128u, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                    mma_bf16(tmem + (uint32_t)sb * 128u, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
                              idesc_s, kk > 0);
                 }
-                mma_commit(&s_full[st]);
+                mma_commit(&s_full[sb]);
+                mma_commit(&k_empty[kst]);
                 return true;
             };
             if (n_total > 0) ok = issue_s(0);
@@ -198,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int st = j & 1;
-                if (!mbar_wait(p_full, (uint32_t)j & 1u) || !mbar_wait(&v_full[st], (uint32_t)(j >> 1) & 1u)) {
+                const int st = j % kVStages;
+                if (!mbar_wait(p_full, (uint32_t)j & 1u) || !mbar_wait(&v_full[st], (uint32_t)(j / kVStages) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -212,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
                 }
                 mma_commit(o_done);
-                mma_commit(&kv_empty[st]);
+                mma_commit(&v_empty[st]);
             }
             mma_commit(mma_done);
             mbar_wait(mma_done, 0);
@@ -408,20 +435,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnLaunch a, int n_t
 
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads) { return 128 / (n_q_heads / n_kv_heads); }
 
-// K/V splits per (query tile, head): enough CTAs for two per SM, each split
-// keeping at least four K/V tiles
-int attn_tc_splits(int n_tiles, int n_kv_heads, int n_tokens) {
-    const int pairs = n_tiles * n_kv_heads;
-    const int max_kv_tiles = (n_tokens + 127) / 128;
-    int s = (2 * kNumSMs + pairs - 1) / pairs;
-    s = std::min(s, std::max(1, max_kv_tiles / 4));
-    return std::max(1, std::min(s, 16));
-}
-
-size_t attn_tc_scratch_bytes(int n_tiles, int n_kv_heads, int n_tokens) {
-    const int s = attn_tc_splits(n_tiles, n_kv_heads, n_tokens);
-    if (s <= 1) return 0;
-    return (size_t)s * n_tiles * n_kv_heads * 128 * (128 + 2) * sizeof(float);
+size_t attn_tc_scratch_bytes(int n_split, int n_tiles, int n_kv_heads) {
+    if (n_split <= 1) return 0;
+    return (size_t)n_split * n_tiles * n_kv_heads * 128 * (128 + 2) * sizeof(float);
 }
 
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
@@ -430,7 +446,9 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         if (why) *why = "tensor-core attention needs head_dim 128";
         return cudaErrorInvalidValue;
     }
-    int n_split = a.part_o ? attn_tc_splits(a.n_tiles, a.n_kv_heads, a.n_tokens) : 1;
+    const int n_split = (a.part_o && a.n_split > 1) ? a.n_split : 1;
+    AttnLaunch b = a;
+    if (n_split == 1) b.chunk = 1 << 30;   // one CTA walks the whole range
     CUtensorMap tk, tv;
     const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
     const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
@@ -446,11 +464,11 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         attr = true;
     }
     dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, a);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n_split == 1) return e;
     const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
-    attn_combine_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a, a.n_tiles, n_split);
+    attn_combine_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(b, a.n_tiles, n_split);
     return cudaGetLastError();
 }
 
