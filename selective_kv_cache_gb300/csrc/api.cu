@@ -53,6 +53,8 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
     g.qkv = plan_gemm(m.dtype, (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, m.d_model, R);
     g.o = plan_gemm(m.dtype, m.d_model, hqd, R);
     g.gu = plan_gemm(m.dtype, 2 * m.ffn_dim, m.d_model, R);
+    // one K split: the gate/up projection writes silu(g) * u directly (no partials)
+    if (m.dtype == KVR_BF16 && g.gu.splits == 1 && m.ffn_dim % 64 == 0) g.gu.swiglu_F = m.ffn_dim;
     g.down = plan_gemm(m.dtype, m.d_model, m.ffn_dim, R);
     return g;
 }
@@ -61,8 +63,9 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
 // share one region: they are never live at the same time.
 size_t part_bytes(const kvr_model_desc& m, int R, size_t attn_scratch) {
     const Gemms g = plan_all(m, R);
+    const size_t gu = g.gu.swiglu_F ? 0 : gemm_partial_bytes(g.gu);
     const size_t gemm = std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
-                                 std::max(gemm_partial_bytes(g.gu), gemm_partial_bytes(g.down)));
+                                 std::max(gu, gemm_partial_bytes(g.down)));
     return std::max(gemm, attn_scratch);
 }
 
@@ -303,10 +306,10 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
     }
     {
         Prof p(c, KVR_K_GEMM_GATEUP, s);
-        cudaError_t e = launch_gemm(dt, g.gu, w->w_gate_up, hn, part, c->d_err, s, &why);
+        cudaError_t e = launch_gemm(dt, g.gu, w->w_gate_up, hn, part, c->d_err, s, &why, act);
         if (e != cudaSuccess) return cuda_fail(e, ("gate/up projection " + why).c_str());
     }
-    {
+    if (!g.gu.swiglu_F) {
         Prof p(c, KVR_K_EPI_GATEUP, s);
         KVR_CHECK_LAUNCH(launch_epi_swiglu(dt, part, g.gu.splits, R, m.ffn_dim, act, s), "swiglu epilogue");
     }

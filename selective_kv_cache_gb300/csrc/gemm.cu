@@ -33,7 +33,26 @@ struct GemmDev {
     float* part;
     int32_t* err;
     int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols, items, atoms;
+    // fused SwiGLU (swiglu_F > 0, one K split): a tile holds 64 gate rows and the
+    // 64 matching up rows; the epilogue writes act[r][f] = silu(g) * u in bf16
+    int swiglu_F;
+    __nv_bfloat16* act;
 };
+
+// all four epilogue warps (128 threads) on named barrier 2; returns the AND of pred
+__device__ __forceinline__ bool epi_bar_and(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // work item -> (feature tile, row tile, K range); row tiles of one feature tile
 // are consecutive items, so CTAs that run at the same time share weight tiles in L2
@@ -66,6 +85,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* acc_empty = acc_full + 2;    // [2]
     uint64_t* mma_done = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);   // [64][16] up values
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t acc_stride = (uint32_t)g.tmem_cols / 2u;
 
@@ -111,7 +131,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(stA + stB));
                     for (int a = 0; a < atoms; ++a) {
                         const int kx = (kb * atoms + a) * kBK;
-                        tma_load_2d(sA + (size_t)s * stA + a * kTileABytes, &tmA, &full[s], kx, m_t * 128);
+                        uint8_t* da = sA + (size_t)s * stA + a * kTileABytes;
+                        if (g.swiglu_F) {   // gate rows f0..f0+63, then up rows F+f0..
+                            tma_load_2d(da, &tmA, &full[s], kx, m_t * 64);
+                            tma_load_2d(da + kTileABytes / 2, &tmA, &full[s], kx, g.swiglu_F + m_t * 64);
+                        } else {
+                            tma_load_2d(da, &tmA, &full[s], kx, m_t * 128);
+                        }
                         tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], kx, n_t * BN);
                     }
                 }
@@ -161,7 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(mma_done, 0);
         }
     } else {
-        // ------------------------------------------------------------ epilogue: TMEM -> fp32 partials
+        // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int local = 0;
@@ -173,22 +199,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int got = 0;
             if (lane == 0) got = mbar_wait(&acc_full[ab], (uint32_t)(local >> 1) & 1u) ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
+            if (g.swiglu_F) got = epi_bar_and(got != 0);   // the four warps decide together
             if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int feat = m_t * 128 + q * 32 + lane;
-            float* out = g.part + (size_t)split * g.R * g.n_out + feat;
             const int tok0 = n_t * BN;
             const uint32_t src = tmem + lane_base + (uint32_t)ab * acc_stride;
-            for (int c = 0; c < BN; c += 16) {
-                float v[16];
-                tmem_ld16(src + (uint32_t)c, v);
+            if (!g.swiglu_F) {
+                // TMEM -> fp32 partials part[split][token][feature]
+                const int feat = m_t * 128 + q * 32 + lane;
+                float* out = g.part + (size_t)split * g.R * g.n_out + feat;
+                for (int c = 0; c < BN; c += 16) {
+                    float v[16];
+                    tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int tok = tok0 + c + j;
-                    if (tok < g.R) out[(size_t)tok * g.n_out] = v[j];
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = tok0 + c + j;
+                        if (tok < g.R) out[(size_t)tok * g.n_out] = v[j];
+                    }
+                }
+            } else {
+                // lanes 0-63 (warps of quarters 0, 1) hold gate, lanes 64-127 the matching up
+                const int f = m_t * 64 + (q & 1) * 32 + lane;
+                float* row = xch + ((q & 1) * 32 + lane) * 16;
+                for (int c = 0; c < BN; c += 16) {
+                    float v[16];
+                    tmem_ld16(src + (uint32_t)c, v);
+                    if (q >= 2) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            reinterpret_cast<float4*>(row)[t] = make_float4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+                    }
+                    epi_bar();
+                    if (q < 2) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int tok = tok0 + c + j;
+                            const float gv = v[j];
+                            const float a = gv / (1.0f + __expf(-gv)) * row[j];
+                            if (tok < g.R) g.act[(size_t)tok * g.swiglu_F + f] = __float2bfloat16_rn(a);
+                        }
+                    }
+                    epi_bar();
                 }
             }
             tc_fence_before();
@@ -280,7 +334,8 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
     p.atoms = (K % (2 * kBK) == 0) ? 2 : 1;
     const int KB = K / (kBK * p.atoms);
     const int tileB = p.BN * 128;
-    p.stages = std::min(8, (kSmemBudget - 1024 - 256) / (p.atoms * (kTileABytes + tileB)));
+    p.stages = std::min(8, (kSmemBudget - 1024 - 1024 - 4096) / (p.atoms * (kTileABytes + tileB)));
+    p.swiglu_F = 0;
     // K splits from a cost model fitted to measurements on GB300: one item
     // streams its (128 + BN) x (K / S) operand tiles at ~100 GB/s per SM, the
     // persistent grid runs ceil(items / 152) rounds, and every split adds an
@@ -306,7 +361,7 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
 size_t gemm_partial_bytes(const GemmPlan& p) { return (size_t)p.splits * p.R * p.n_out * sizeof(float); }
 
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
-                        cudaStream_t s, std::string* why) {
+                        cudaStream_t s, std::string* why, void* act) {
     if (p.R <= 0) return cudaSuccess;
     if (dtype == KVR_F32) {
         dim3 grid(p.m_tiles, p.n_tiles, p.splits);
@@ -315,7 +370,8 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         return cudaGetLastError();
     }
     CUtensorMap ta, tb;
-    if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why))
+    if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, p.swiglu_F ? 64 : 128,
+                           why))
         return cudaErrorInvalidValue;
     if (!make_tmap_2d_bf16(&tb, x, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.K * 2, kBK, (uint32_t)p.BN, why))
         return cudaErrorInvalidValue;
@@ -332,11 +388,17 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     g.stages = p.stages;
     g.items = p.m_tiles * p.n_tiles * p.splits;
     g.atoms = p.atoms;
+    g.swiglu_F = p.swiglu_F;
+    g.act = (__nv_bfloat16*)act;
+    if (p.swiglu_F && (p.splits != 1 || !act || p.swiglu_F % 64 || p.n_out != 2 * p.swiglu_F)) {
+        if (why) *why = "fused SwiGLU needs one K split and an output buffer";
+        return cudaErrorInvalidValue;
+    }
     int cols = 32;
     while (cols < 2 * p.BN) cols <<= 1;   // two accumulators
     g.tmem_cols = cols;
-    const size_t smem =
-        1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + (2 * p.stages + 5) * 8 + 16;
+    // pipeline ring, barriers (1 KB) and the SwiGLU exchange area (4 KB)
+    const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + 1024 + 64 * 16 * 4;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

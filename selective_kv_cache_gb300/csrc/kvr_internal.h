@@ -120,11 +120,12 @@ cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w,
 struct GemmPlan {
     int n_out, K, R;
     int m_tiles, n_tiles, BN, splits, stages, atoms;
+    int swiglu_F;   // > 0: gate/up projection with the SwiGLU fused (act output, no partials)
 };
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
 size_t gemm_partial_bytes(const GemmPlan& p);
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
-                        cudaStream_t s, std::string* why);
+                        cudaStream_t s, std::string* why, void* act = nullptr);
 
 // Epilogues (sum split partials in split order, then the fused op).
 struct QkvEpi {
