@@ -142,6 +142,10 @@ kvr_status validate_desc(const kvr_model_desc* m) {
         set_error("dtype must be KVR_F32 or KVR_BF16");
         return KVR_EUNSUPPORTED;
     }
+    if (m->d_model > 8192) {
+        set_error("d_model above 8192 is not supported (row kernels keep a row in registers)");
+        return KVR_EUNSUPPORTED;
+    }
     if (m->d_model % 64 || m->ffn_dim % 64 || (m->n_q_heads * m->head_dim) % 64) {
         set_error("d_model, ffn_dim and n_q_heads*head_dim must be multiples of 64");
         return KVR_EUNSUPPORTED;
@@ -217,8 +221,11 @@ void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr
 }
 
 // One layer of the packed refresh over the current selection.
+// xn_ready: the previous layer's down epilogue already wrote this layer's
+// normalised rows into the workspace; next_norm1: fuse the next layer's first
+// RMSNorm into this layer's down epilogue (NULL for the last layer run).
 kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* hidden, uint8_t* ws,
-                     const WsLayout& L, cudaStream_t s) {
+                     const WsLayout& L, cudaStream_t s, bool xn_ready = false, const void* next_norm1 = nullptr) {
     const kvr_model_desc& m = c->m;
     const int R = c->sel.n_rows;
     const int dt = m.dtype;
@@ -232,7 +239,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
     float* part = reinterpret_cast<float*>(ws + L.part);
     std::string why;
 
-    {
+    if (!xn_ready) {
         Prof p(c, KVR_K_RMSNORM, s);
         KVR_CHECK_LAUNCH(launch_rmsnorm(dt, hidden, 0, w->norm1, xn, R, m.d_model, m.rms_eps, s), "rmsnorm");
     }
@@ -298,11 +305,9 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
     }
     {
         Prof p(c, KVR_K_EPI_O, s);
-        KVR_CHECK_LAUNCH(launch_epi_residual_f32(dt, part, g.o.splits, R, m.d_model, hidden, h, s), "o epilogue");
-    }
-    {
-        Prof p(c, KVR_K_RMSNORM, s);
-        KVR_CHECK_LAUNCH(launch_rmsnorm(dt, h, 1, w->norm2, hn, R, m.d_model, m.rms_eps, s), "rmsnorm");
+        KVR_CHECK_LAUNCH(launch_epi_residual_norm(dt, part, g.o.splits, R, m.d_model, hidden, h, w->norm2, hn,
+                                                  m.rms_eps, s),
+                         "o epilogue");
     }
     {
         Prof p(c, KVR_K_GEMM_GATEUP, s);
@@ -320,7 +325,12 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
     }
     {
         Prof p(c, KVR_K_EPI_DOWN, s);
-        KVR_CHECK_LAUNCH(launch_epi_down(dt, part, g.down.splits, R, m.d_model, h, hidden, s), "down epilogue");
+        if (next_norm1)
+            KVR_CHECK_LAUNCH(launch_epi_down_norm(dt, part, g.down.splits, R, m.d_model, h, hidden, next_norm1, xn,
+                                                  m.rms_eps, s),
+                             "down epilogue");
+        else
+            KVR_CHECK_LAUNCH(launch_epi_down(dt, part, g.down.splits, R, m.d_model, h, hidden, s), "down epilogue");
     }
     return KVR_OK;
 }
@@ -734,7 +744,8 @@ kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_b
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (c->sel.n_rows > 0) {
         for (int l = layer_begin; l < layer_end; ++l) {
-            st = run_layer(c, l, &w[l], hidden_inout, static_cast<uint8_t*>(workspace), L, s);
+            st = run_layer(c, l, &w[l], hidden_inout, static_cast<uint8_t*>(workspace), L, s, l > layer_begin,
+                           l + 1 < layer_end ? w[l + 1].norm1 : nullptr);
             if (st != KVR_OK) return st;
         }
     }

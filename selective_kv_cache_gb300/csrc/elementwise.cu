@@ -190,6 +190,104 @@ __global__ void epi_down_kernel(const float* __restrict__ part, int splits, int 
     store8<T>(x + i8, v);
 }
 
+// ------------------------------------------------------------------ residual + RMSNorm, one CTA per row
+// Each thread keeps up to kRowChunks 8-element chunks of its row in registers
+// between the sum-of-squares pass and the normalisation.
+constexpr int kRowThreads = 256;
+constexpr int kRowChunks = 4;   // rows up to 256 * 4 * 8 = 8192 elements
+
+__device__ __forceinline__ float row_rstd(float ss, int d, float eps) {
+    __shared__ float red[kRowThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRowThreads / 32; ++i) tot += red[i];
+    return 1.0f / sqrtf(tot / (float)d + eps);
+}
+
+__device__ __forceinline__ float round_to(float v, float*) { return v; }
+__device__ __forceinline__ float round_to(float v, __nv_bfloat16*) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// h = x + sum of the O projection's partials (fp32), then hn = RMSNorm(h) * w
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) epi_residual_norm_kernel(const float* __restrict__ part, int splits,
+                                                                        int R, int d, const T* __restrict__ x,
+                                                                        float* __restrict__ h, const T* __restrict__ w,
+                                                                        T* __restrict__ hn, float eps) {
+    const int r = blockIdx.x;
+    float v[kRowChunks][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowChunks; ++k) {
+        const int i = (threadIdx.x + k * kRowThreads) * 8;
+        if (i < d) {
+            float xv[8];
+            sum_parts8(part, (size_t)R * d, splits, (size_t)r * d + i, v[k]);
+            load8<T>(x + (size_t)r * d + i, xv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[k][j] += xv[j];
+                ss += v[k][j] * v[k][j];
+            }
+            store8<float>(h + (size_t)r * d + i, v[k]);
+        }
+    }
+    const float rstd = row_rstd(ss, d, eps);
+#pragma unroll
+    for (int k = 0; k < kRowChunks; ++k) {
+        const int i = (threadIdx.x + k * kRowThreads) * 8;
+        if (i < d) {
+            float g[8];
+            load8<T>(w + i, g);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[k][j] = v[k][j] * rstd * g[j];
+            store8<T>(hn + (size_t)r * d + i, v[k]);
+        }
+    }
+}
+
+// x' = h + sum of the down projection's partials, stored in T; then the next
+// layer's xn = RMSNorm(x') * w_next from the stored (rounded) x'
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) epi_down_norm_kernel(const float* __restrict__ part, int splits, int R,
+                                                                    int d, const float* __restrict__ h,
+                                                                    T* __restrict__ x, const T* __restrict__ w_next,
+                                                                    T* __restrict__ xn, float eps) {
+    const int r = blockIdx.x;
+    float v[kRowChunks][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowChunks; ++k) {
+        const int i = (threadIdx.x + k * kRowThreads) * 8;
+        if (i < d) {
+            float hv[8];
+            sum_parts8(part, (size_t)R * d, splits, (size_t)r * d + i, v[k]);
+            load8<float>(h + (size_t)r * d + i, hv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[k][j] = round_to(v[k][j] + hv[j], (T*)nullptr);
+                ss += v[k][j] * v[k][j];
+            }
+            store8<T>(x + (size_t)r * d + i, v[k]);
+        }
+    }
+    const float rstd = row_rstd(ss, d, eps);
+#pragma unroll
+    for (int k = 0; k < kRowChunks; ++k) {
+        const int i = (threadIdx.x + k * kRowThreads) * 8;
+        if (i < d) {
+            float g[8];
+            load8<T>(w_next + i, g);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[k][j] = v[k][j] * rstd * g[j];
+            store8<T>(xn + (size_t)r * d + i, v[k]);
+        }
+    }
+}
+
 inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
 
 }  // namespace
@@ -252,6 +350,32 @@ cudaError_t launch_epi_down(int dtype, const float* part, int splits, int R, int
                                                                           (__nv_bfloat16*)x_out);
     else
         epi_down_kernel<float><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, d, h, (float*)x_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epi_residual_norm(int dtype, const float* part, int splits, int R, int d, const void* x, float* h,
+                                     const void* w, void* hn, float eps, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    if (d > kRowThreads * kRowChunks * 8) return cudaErrorInvalidValue;
+    if (dtype == KVR_BF16)
+        epi_residual_norm_kernel<__nv_bfloat16><<<R, kRowThreads, 0, s>>>(
+            part, splits, R, d, (const __nv_bfloat16*)x, h, (const __nv_bfloat16*)w, (__nv_bfloat16*)hn, eps);
+    else
+        epi_residual_norm_kernel<float><<<R, kRowThreads, 0, s>>>(part, splits, R, d, (const float*)x, h,
+                                                                  (const float*)w, (float*)hn, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epi_down_norm(int dtype, const float* part, int splits, int R, int d, const float* h, void* x,
+                                 const void* w_next, void* xn, float eps, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    if (d > kRowThreads * kRowChunks * 8) return cudaErrorInvalidValue;
+    if (dtype == KVR_BF16)
+        epi_down_norm_kernel<__nv_bfloat16><<<R, kRowThreads, 0, s>>>(
+            part, splits, R, d, h, (__nv_bfloat16*)x, (const __nv_bfloat16*)w_next, (__nv_bfloat16*)xn, eps);
+    else
+        epi_down_norm_kernel<float><<<R, kRowThreads, 0, s>>>(part, splits, R, d, h, (float*)x,
+                                                              (const float*)w_next, (float*)xn, eps);
     return cudaGetLastError();
 }
 

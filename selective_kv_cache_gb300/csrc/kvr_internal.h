@@ -148,6 +148,12 @@ cudaError_t launch_epi_swiglu(int dtype, const float* part, int splits, int R, i
                               cudaStream_t s);
 cudaError_t launch_epi_down(int dtype, const float* part, int splits, int R, int d, const float* h, void* x_out,
                             cudaStream_t s);
+// h = x + O partials (fp32) and hn = RMSNorm(h) * w in one pass per row
+cudaError_t launch_epi_residual_norm(int dtype, const float* part, int splits, int R, int d, const void* x, float* h,
+                                     const void* w, void* hn, float eps, cudaStream_t s);
+// x' = h + down partials (model dtype) and the next layer's xn = RMSNorm(x') * w_next
+cudaError_t launch_epi_down_norm(int dtype, const float* part, int splits, int R, int d, const float* h, void* x,
+                                 const void* w_next, void* xn, float eps, cudaStream_t s);
 
 // Attention over the mixed cache.
 struct AttnLaunch {
