@@ -197,6 +197,56 @@ kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_b
                        uint32_t flags, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvr_refresh_interval_wise -- the interval-major schedule ("Budgeted KV-Cache
+ * Repair", Sec. 7.1, sequential maximal-interval replay): each maximal
+ * interval of selected positions, sequence by sequence in position order, is
+ * forwarded through layers [layer_begin, layer_end) against the cache as the
+ * earlier intervals left it, then committed (KVR_COMMIT_META in flags) before
+ * the next interval starts.  In real arithmetic this equals the packed
+ * refresh ([BKR] Sec. 13.2); it is the comparator for the packed executor.
+ *   Selection arguments as kvr_select (validated as a whole first); `w` as
+ *   kvr_refresh.  hidden_out: device [sum(counts)][d], rows in sorted position
+ *   order.  workspace >= kvr_workspace_bytes(c, longest interval).
+ *   n_intervals_out: host, nullable.  Leaves the last interval selected.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_refresh_interval_wise(kvr_cache* c, const int32_t* positions, const int32_t* counts,
+                                     int32_t budget_percent, const int32_t* token_ids, const void* embed_table,
+                                     int32_t vocab, const void* hidden_src, const kvr_layer_weights* w,
+                                     int32_t layer_begin, int32_t layer_end, void* hidden_out, void* workspace,
+                                     size_t ws_bytes, uint32_t flags, int32_t* n_intervals_out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvr_reselect -- switch the selection mid-refresh, carrying rows over
+ * ("CacheReforge", Bounded Recovery, "Executable restart": a layer range is
+ * recomputed over the whole affected suffix from the hidden states stored at
+ * the range's first layer, while the positions refreshed so far keep their
+ * current state).  New positions/counts as kvr_select (no budget check).
+ *   carry_rows  device [current rows][d]: the current selection's rows (as the
+ *               last refresh left them); a new row whose position was
+ *               selected takes its row from here.
+ *   fill_rows   device [batch][capacity][d]: per-position rows for every other
+ *               new position (e.g. the stored boundary states).
+ *   hidden_out  device [sum(counts)][d]; must not be carry_rows.
+ * Metadata bits are untouched until a commit.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_reselect(kvr_cache* c, const int32_t* positions, const int32_t* counts, const void* carry_rows,
+                        const void* fill_rows, void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * kvr_lora_merge -- fold a low-rank adapter into a projection
+ * ("CacheReforge", Implementation: a LoRA on the cache-producing projections):
+ *   w_out[i][k] = w[i][k] + scale * sum_j b[i - row_begin][j] * a[j][k]
+ * for rows [row_begin, row_begin + row_count) of the [n_out, K] matrix
+ * (nn.Linear layout); other rows are copied.  w_out may equal w.
+ *   a: device [rank][K], b: device [row_count][rank], model dtype; fp32
+ *   accumulation, one rounding to the dtype.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, int32_t row_begin,
+                          int32_t row_count, const void* a, const void* b, int32_t rank, float scale, int32_t dtype,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvr_refresh_layer_noalloc -- kvr_refresh_layer without a caller workspace
  * and without any allocation.  The paper has no counterpart: this entry point
  * exists for callers that cannot hand the library scratch memory when they

@@ -47,6 +47,16 @@ struct Gemms {
     GemmPlan qkv, o, gu, down;
 };
 
+// Where the rows of a new selection come from.
+struct RowSource {
+    const int32_t* token_ids = nullptr;   // with embed: embed[token_ids[seq][u]]
+    const void* embed = nullptr;
+    int vocab = 0;
+    const void* hidden_src = nullptr;     // per-position rows [batch][capacity][d]
+    const void* carry = nullptr;          // rows of the current selection (kept for positions in both)
+    const void* fill = nullptr;           // per-position rows for the other positions
+};
+
 Gemms plan_all(const kvr_model_desc& m, int R) {
     Gemms g;
     const int hqd = m.n_q_heads * m.head_dim;
@@ -179,6 +189,7 @@ void free_cache(kvr_cache* c) {
     cudaFree(c->d_plan);
     cudaFree(c->d_rope);
     cudaFree(c->d_err);
+    cudaFree(c->d_map);
     if (c->h_stage) cudaFreeHost(c->h_stage);
     if (c->stage_ev) cudaEventDestroy(c->stage_ev);
     for (auto& r : c->prof) {
@@ -414,137 +425,9 @@ bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t
     return true;
 }
 
-}  // namespace kvr
-
-using namespace kvr;
-
-extern "C" {
-
-const char* kvr_last_error(void) { return g_err.c_str(); }
-
-kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capacity, void* k_base, void* v_base,
-                            int32_t n_tokens, int32_t suffix_start, const uint32_t* local_bits,
-                            const uint32_t* sink_bits, float alpha, float beta, uint32_t flags, void* stream,
-                            kvr_cache** out) {
-    if (!out) {
-        set_error("out is NULL");
-        return KVR_EINVAL;
-    }
-    *out = nullptr;
-    kvr_status st = validate_desc(m);
-    if (st != KVR_OK) return st;
-    if (batch < 1 || capacity < 1 || n_tokens < 1 || n_tokens > capacity || suffix_start < 0 ||
-        suffix_start > n_tokens) {
-        set_error("need batch >= 1 and 0 <= suffix_start <= n_tokens <= capacity");
-        return KVR_EINVAL;
-    }
-    if (!k_base || !v_base || !aligned16(k_base) || !aligned16(v_base)) {
-        set_error("K/V cache pointers must be non-NULL and 16-byte aligned");
-        return KVR_EINVAL;
-    }
-    if (!std::isfinite(alpha) || !std::isfinite(beta)) {
-        set_error("alpha and beta must be finite");
-        return KVR_EINVAL;
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    kvr_cache* c = new kvr_cache();
-    c->m = *m;
-    c->batch = batch;
-    c->capacity = capacity;
-    c->n_tokens = n_tokens;
-    c->suffix_start = suffix_start;
-    c->words = (capacity + 31) / 32;
-    c->alpha = alpha;
-    c->beta = beta;
-    c->flags = flags;
-    c->k_base = k_base;
-    c->v_base = v_base;
-    cudaGetDevice(&c->device);
-
-    int rpt = 0, kpt = 0;
-    attention_tiling(m->dtype, m->n_q_heads, m->n_kv_heads, &rpt, &kpt);
-    const size_t rows = (size_t)batch * capacity;
-    c->max_tiles = (int)(rows / rpt + batch + 1);
-    const size_t wbytes = (size_t)batch * c->words * sizeof(uint32_t);
-    const int half = m->head_dim / 2;
-    c->stage_elems = (size_t)batch * 8 + rows;
-    cudaError_t e = cudaSuccess;
-    auto A = [&](void** p, size_t n) {
-        if (e == cudaSuccess) e = cudaMalloc(p, n);
-    };
-    A((void**)&c->d_local, wbytes);
-    A((void**)&c->d_sink, wbytes);
-    A((void**)&c->d_sel, wbytes);
-    A((void**)&c->d_eloc, wbytes);
-    A((void**)&c->d_esnk, wbytes);
-    A((void**)&c->d_seqinfo, c->stage_elems * sizeof(int32_t));
-    A((void**)&c->d_U, rows * sizeof(int32_t));
-    A((void**)&c->d_row_seq, rows * sizeof(int32_t));
-    A((void**)&c->d_iv, rows * 2 * sizeof(int32_t));
-    A((void**)&c->d_plan, (size_t)c->max_tiles * 8 * sizeof(int32_t));
-    A((void**)&c->d_rope, (size_t)capacity * half * sizeof(float2));
-    A((void**)&c->d_err, 4 * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMallocHost((void**)&c->h_stage, c->stage_elems * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev, cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-        set_error(std::string("allocation failed: ") + cudaGetErrorString(e));
-        free_cache(c);
-        return KVR_ENOMEM;
-    }
-    c->d_raw = c->d_seqinfo + (size_t)batch * 8;
-
-    // rotary table: angle u * theta^(-2i/d_h) formed in double, stored as fp32 (cos, sin)
-    std::vector<float2> rope((size_t)capacity * half);
-    for (int i = 0; i < half; ++i) {
-        const double inv = std::pow(m->rope_theta, -2.0 * i / (double)m->head_dim);
-        for (int u = 0; u < capacity; ++u) {
-            const double a = (double)u * inv;
-            rope[(size_t)u * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
-        }
-    }
-    std::vector<uint32_t> zeros((size_t)batch * c->words, 0u);
-    e = cudaMemcpyAsync(c->d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(c->d_local, local_bits ? local_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(c->d_sink, sink_bits ? sink_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_err, 0, 4 * sizeof(int32_t), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_sel, 0, wbytes, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_eloc, c->d_local, wbytes, cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_esnk, c->d_sink, wbytes, cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-        kvr_status r = cuda_fail(e, "cache set-up");
-        free_cache(c);
-        return r;
-    }
-    *out = c;
-    return KVR_OK;
-}
-
-kvr_status kvr_destroy_cache(kvr_cache* c) {
-    if (!c) return KVR_OK;
-    cudaDeviceSynchronize();
-    free_cache(c);
-    return KVR_OK;
-}
-
-kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
-                      const int32_t* token_ids, const void* embed_table, int32_t vocab, const void* hidden_src,
-                      void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out, void* stream) {
-    if (!c || !counts) {
-        set_error("cache or counts is NULL");
-        return KVR_EINVAL;
-    }
-    const bool use_ids = token_ids || embed_table;
-    if (use_ids == (hidden_src != nullptr) || (use_ids && (!token_ids || !embed_table))) {
-        set_error("give exactly one row source: token_ids + embed_table, or hidden_src");
-        return KVR_EINVAL;
-    }
-    if (use_ids && vocab < 1) {
-        set_error("vocab must be >= 1 with an embedding table");
-        return KVR_EINVAL;
-    }
+kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
+                     const RowSource& src, void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out,
+                     cudaStream_t s) {
     if (budget_percent > 100 || budget_percent < -1) {
         set_error("budget_percent must be -1 or in [0, 100]");
         return KVR_EINVAL;
@@ -632,7 +515,6 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
     sel.n_tiles = tiles;
     attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split);
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the staging buffer may still feed the previous upload
     cudaError_t e = cudaEventSynchronize(c->stage_ev);
     if (e != cudaSuccess) return cuda_fail(e, "staging wait");
@@ -674,20 +556,278 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
     a.rows_per_tile = sel.rows_per_tile;
     a.keys_per_tile = sel.keys_per_tile;
     a.sink_static = (c->flags & KVR_SINK_STATIC) ? 1 : 0;
+    if (src.carry) {
+        // position -> row map of the selection being replaced (rows carry over)
+        const size_t map_bytes = (size_t)c->batch * c->capacity * sizeof(int32_t);
+        KVR_CHECK_LAUNCH(cudaMemsetAsync(c->d_map, 0xff, map_bytes, s), "row map");
+        if (c->sel.valid)
+            KVR_CHECK_LAUNCH(launch_map_rows(c->d_U, c->d_row_seq, c->sel.n_rows, c->capacity, c->d_map, s),
+                             "row map");
+    }
     {
         Prof p(c, KVR_K_SELECT, s);
         KVR_CHECK_LAUNCH(launch_select(a, B, s), "select");
     }
     {
         Prof p(c, KVR_K_GATHER, s);
-        KVR_CHECK_LAUNCH(launch_gather(c->m.dtype, c->d_U, c->d_row_seq, rows, c->m.d_model, c->capacity, token_ids,
-                                       embed_table, hidden_src, hidden_out, c->d_err, vocab, s),
-                         "row gather");
+        if (src.carry)
+            KVR_CHECK_LAUNCH(launch_gather_carry(c->m.dtype, c->d_U, c->d_row_seq, rows, c->m.d_model, c->capacity,
+                                                 c->d_map, src.carry, src.fill, hidden_out, s),
+                             "row gather");
+        else
+            KVR_CHECK_LAUNCH(launch_gather(c->m.dtype, c->d_U, c->d_row_seq, rows, c->m.d_model, c->capacity,
+                                           src.token_ids, src.embed, src.hidden_src, hidden_out, c->d_err, src.vocab,
+                                           s),
+                             "row gather");
     }
     sel.valid = true;
     c->sel = sel;
     if (n_rows_out) *n_rows_out = rows;
     if (n_intervals_out) *n_intervals_out = ivs;
+    return KVR_OK;
+}
+
+}  // namespace kvr
+
+using namespace kvr;
+
+extern "C" {
+
+const char* kvr_last_error(void) { return g_err.c_str(); }
+
+kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capacity, void* k_base, void* v_base,
+                            int32_t n_tokens, int32_t suffix_start, const uint32_t* local_bits,
+                            const uint32_t* sink_bits, float alpha, float beta, uint32_t flags, void* stream,
+                            kvr_cache** out) {
+    if (!out) {
+        set_error("out is NULL");
+        return KVR_EINVAL;
+    }
+    *out = nullptr;
+    kvr_status st = validate_desc(m);
+    if (st != KVR_OK) return st;
+    if (batch < 1 || capacity < 1 || n_tokens < 1 || n_tokens > capacity || suffix_start < 0 ||
+        suffix_start > n_tokens) {
+        set_error("need batch >= 1 and 0 <= suffix_start <= n_tokens <= capacity");
+        return KVR_EINVAL;
+    }
+    if (!k_base || !v_base || !aligned16(k_base) || !aligned16(v_base)) {
+        set_error("K/V cache pointers must be non-NULL and 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) {
+        set_error("alpha and beta must be finite");
+        return KVR_EINVAL;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    kvr_cache* c = new kvr_cache();
+    c->m = *m;
+    c->batch = batch;
+    c->capacity = capacity;
+    c->n_tokens = n_tokens;
+    c->suffix_start = suffix_start;
+    c->words = (capacity + 31) / 32;
+    c->alpha = alpha;
+    c->beta = beta;
+    c->flags = flags;
+    c->k_base = k_base;
+    c->v_base = v_base;
+    cudaGetDevice(&c->device);
+
+    int rpt = 0, kpt = 0;
+    attention_tiling(m->dtype, m->n_q_heads, m->n_kv_heads, &rpt, &kpt);
+    const size_t rows = (size_t)batch * capacity;
+    c->max_tiles = (int)(rows / rpt + batch + 1);
+    const size_t wbytes = (size_t)batch * c->words * sizeof(uint32_t);
+    const int half = m->head_dim / 2;
+    c->stage_elems = (size_t)batch * 8 + rows;
+    cudaError_t e = cudaSuccess;
+    auto A = [&](void** p, size_t n) {
+        if (e == cudaSuccess) e = cudaMalloc(p, n);
+    };
+    A((void**)&c->d_local, wbytes);
+    A((void**)&c->d_sink, wbytes);
+    A((void**)&c->d_sel, wbytes);
+    A((void**)&c->d_eloc, wbytes);
+    A((void**)&c->d_esnk, wbytes);
+    A((void**)&c->d_seqinfo, c->stage_elems * sizeof(int32_t));
+    A((void**)&c->d_U, rows * sizeof(int32_t));
+    A((void**)&c->d_row_seq, rows * sizeof(int32_t));
+    A((void**)&c->d_iv, rows * 2 * sizeof(int32_t));
+    A((void**)&c->d_plan, (size_t)c->max_tiles * 8 * sizeof(int32_t));
+    A((void**)&c->d_rope, (size_t)capacity * half * sizeof(float2));
+    A((void**)&c->d_err, 4 * sizeof(int32_t));
+    A((void**)&c->d_map, rows * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMallocHost((void**)&c->h_stage, c->stage_elems * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        set_error(std::string("allocation failed: ") + cudaGetErrorString(e));
+        free_cache(c);
+        return KVR_ENOMEM;
+    }
+    c->d_raw = c->d_seqinfo + (size_t)batch * 8;
+
+    // rotary table: angle u * theta^(-2i/d_h) formed in double, stored as fp32 (cos, sin)
+    std::vector<float2> rope((size_t)capacity * half);
+    for (int i = 0; i < half; ++i) {
+        const double inv = std::pow(m->rope_theta, -2.0 * i / (double)m->head_dim);
+        for (int u = 0; u < capacity; ++u) {
+            const double a = (double)u * inv;
+            rope[(size_t)u * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+        }
+    }
+    std::vector<uint32_t> zeros((size_t)batch * c->words, 0u);
+    e = cudaMemcpyAsync(c->d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->d_local, local_bits ? local_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c->d_sink, sink_bits ? sink_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_err, 0, 4 * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->d_sel, 0, wbytes, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_eloc, c->d_local, wbytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_esnk, c->d_sink, wbytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        kvr_status r = cuda_fail(e, "cache set-up");
+        free_cache(c);
+        return r;
+    }
+    *out = c;
+    return KVR_OK;
+}
+
+kvr_status kvr_destroy_cache(kvr_cache* c) {
+    if (!c) return KVR_OK;
+    cudaDeviceSynchronize();
+    free_cache(c);
+    return KVR_OK;
+}
+
+kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
+                      const int32_t* token_ids, const void* embed_table, int32_t vocab, const void* hidden_src,
+                      void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out, void* stream) {
+    if (!c || !counts) {
+        set_error("cache or counts is NULL");
+        return KVR_EINVAL;
+    }
+    const bool use_ids = token_ids || embed_table;
+    if (use_ids == (hidden_src != nullptr) || (use_ids && (!token_ids || !embed_table))) {
+        set_error("give exactly one row source: token_ids + embed_table, or hidden_src");
+        return KVR_EINVAL;
+    }
+    if (use_ids && vocab < 1) {
+        set_error("vocab must be >= 1 with an embedding table");
+        return KVR_EINVAL;
+    }
+    RowSource src;
+    src.token_ids = token_ids;
+    src.embed = embed_table;
+    src.vocab = vocab;
+    src.hidden_src = hidden_src;
+    return do_select(c, positions, counts, budget_percent, src, hidden_out, n_rows_out, n_intervals_out,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvr_status kvr_reselect(kvr_cache* c, const int32_t* positions, const int32_t* counts, const void* carry_rows,
+                        const void* fill_rows, void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out,
+                        void* stream) {
+    if (!c || !counts) {
+        set_error("cache or counts is NULL");
+        return KVR_EINVAL;
+    }
+    if (!fill_rows || !aligned16(fill_rows) || (c->sel.valid && c->sel.n_rows > 0 && !carry_rows)) {
+        set_error("fill_rows (and carry_rows when rows are selected) must be non-NULL and 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    if (carry_rows && carry_rows == hidden_out) {
+        set_error("hidden_out must not be the carried rows' buffer (rows move)");
+        return KVR_EINVAL;
+    }
+    RowSource src;
+    src.carry = carry_rows ? carry_rows : fill_rows;
+    src.fill = fill_rows;
+    return do_select(c, positions, counts, -1, src, hidden_out, n_rows_out, n_intervals_out,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvr_status kvr_refresh_interval_wise(kvr_cache* c, const int32_t* positions, const int32_t* counts,
+                                     int32_t budget_percent, const int32_t* token_ids, const void* embed_table,
+                                     int32_t vocab, const void* hidden_src, const kvr_layer_weights* w,
+                                     int32_t layer_begin, int32_t layer_end, void* hidden_out, void* workspace,
+                                     size_t ws_bytes, uint32_t flags, int32_t* n_intervals_out, void* stream) {
+    if (!c || !counts || (!positions && counts)) {
+        set_error("cache, positions or counts is NULL");
+        return KVR_EINVAL;
+    }
+    if (layer_begin < 0 || layer_end > c->m.n_layers || layer_begin > layer_end) {
+        set_error("layer range outside [0, n_layers]");
+        return KVR_ERANGE;
+    }
+    const int B = c->batch;
+    // validate the whole support once (packed selection of everything), which
+    // also gives the total rows; then walk sequence by sequence, interval by interval
+    int32_t n_rows = 0, n_iv = 0;
+    kvr_status st = kvr_select(c, positions, counts, budget_percent, token_ids, embed_table, vocab, hidden_src,
+                               hidden_out, &n_rows, &n_iv, stream);
+    if (st != KVR_OK) return st;
+    if (n_intervals_out) *n_intervals_out = n_iv;
+    std::vector<int32_t> sorted;
+    std::vector<std::pair<int, int>> ivs;   // (position begin, length) per interval, per sequence
+    int64_t off = 0;
+    int max_len = 0;
+    std::vector<std::vector<std::pair<int, int>>> per_seq(B);
+    for (int i = 0; i < B; ++i) {
+        sorted.assign(positions + off, positions + off + counts[i]);
+        std::sort(sorted.begin(), sorted.end());
+        for (size_t k = 0; k < sorted.size(); ++k) {
+            if (k == 0 || sorted[k] != sorted[k - 1] + 1) per_seq[i].push_back({sorted[k], 0});
+            per_seq[i].back().second += 1;
+            max_len = std::max(max_len, per_seq[i].back().second);
+        }
+        off += counts[i];
+    }
+    if (n_rows == 0) return KVR_OK;
+    if (!workspace || ws_bytes < kvr_workspace_bytes(c, max_len)) {
+        set_error("workspace too small: need kvr_workspace_bytes(c, longest interval) = " +
+                  std::to_string(kvr_workspace_bytes(c, max_len)) + " bytes");
+        return KVR_EINVAL;
+    }
+    if (!w && layer_end > layer_begin) {
+        set_error("weights array is NULL");
+        return KVR_EINVAL;
+    }
+    const size_t row_bytes = (size_t)c->m.d_model * dtype_size(c->m.dtype);
+    std::vector<int32_t> cnt(B, 0), pos;
+    int row0 = 0;
+    for (int i = 0; i < B; ++i) {
+        for (const auto& iv : per_seq[i]) {
+            pos.resize(iv.second);
+            for (int k = 0; k < iv.second; ++k) pos[k] = iv.first + k;
+            std::fill(cnt.begin(), cnt.end(), 0);
+            cnt[i] = iv.second;
+            void* rows_out = static_cast<uint8_t*>(hidden_out) + (size_t)row0 * row_bytes;
+            st = kvr_select(c, pos.data(), cnt.data(), -1, token_ids, embed_table, vocab, hidden_src, rows_out,
+                            nullptr, nullptr, stream);
+            if (st != KVR_OK) return st;
+            st = kvr_refresh(c, w, layer_begin, layer_end, rows_out, workspace, ws_bytes, flags, stream);
+            if (st != KVR_OK) return st;
+            row0 += iv.second;
+        }
+    }
+    return KVR_OK;
+}
+
+kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, int32_t row_begin,
+                          int32_t row_count, const void* a, const void* b, int32_t rank, float scale, int32_t dtype,
+                          void* stream) {
+    if (!w || !w_out || !a || !b || n_out < 1 || K < 1 || rank < 1 || row_begin < 0 || row_count < 0 ||
+        row_begin + row_count > n_out || (dtype != KVR_BF16 && dtype != KVR_F32)) {
+        set_error("lora merge: bad arguments");
+        return KVR_EINVAL;
+    }
+    KVR_CHECK_LAUNCH(launch_lora_merge(dtype, w, w_out, n_out, K, row_begin, row_count, a, b, rank, scale,
+                                       reinterpret_cast<cudaStream_t>(stream)),
+                     "lora merge");
     return KVR_OK;
 }
 

@@ -60,6 +60,7 @@ struct kvr_cache_impl {
     int32_t* d_seqinfo = nullptr;  // [batch][8]: count, row_off, iv_off, tile_off, n_tiles
     float2* d_rope = nullptr;      // [capacity][head_dim/2] (cos, sin)
     int32_t* d_err = nullptr;      // [4]
+    int32_t* d_map = nullptr;      // [batch][capacity] position -> row (carry selections)
     int32_t max_tiles = 0;
 
     // pinned staging for the position upload
@@ -111,6 +112,14 @@ cudaError_t launch_gather(int dtype, const int32_t* U, const int32_t* row_seq, i
 
 cudaError_t launch_commit(uint32_t* local, uint32_t* sink, const uint32_t* sel, int total_words, int sink_static,
                           cudaStream_t s);
+cudaError_t launch_map_rows(const int32_t* U, const int32_t* row_seq, int n_rows, int capacity, int32_t* map,
+                            cudaStream_t s);
+cudaError_t launch_gather_carry(int dtype, const int32_t* U, const int32_t* row_seq, int n_rows, int d, int capacity,
+                                const int32_t* map, const void* carry, const void* fill, void* out, cudaStream_t s);
+// w_out[i][k] = w[i][k] + scale * sum_j b[i - row_begin][j] * a[j][k] for rows in
+// [row_begin, row_begin + row_count); other rows copied when w_out != w
+cudaError_t launch_lora_merge(int dtype, const void* w, void* w_out, int n_out, int K, int row_begin, int row_count,
+                              const void* a, const void* b, int rank, float scale, cudaStream_t s);
 
 // RMSNorm: in is model dtype (in_f32 = 0) or fp32 (in_f32 = 1), out model dtype.
 cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w, void* out, int rows, int d,

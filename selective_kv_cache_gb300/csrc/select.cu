@@ -161,6 +161,31 @@ __global__ void gather_kernel(const int32_t* __restrict__ U, const int32_t* __re
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) o4[i] = s4[i];
 }
 
+// position -> row map of the current selection (rows of one sequence are
+// contiguous); entries of unselected positions stay -1
+__global__ void map_rows_kernel(const int32_t* __restrict__ U, const int32_t* __restrict__ row_seq, int n_rows,
+                                int capacity, int32_t* __restrict__ map) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < n_rows) map[(size_t)row_seq[r] * capacity + U[r]] = r;
+}
+
+// rows of a new selection: a position that was selected before keeps its
+// current row (carry), any other takes its per-position row (fill)
+template <typename T>
+__global__ void gather_carry_kernel(const int32_t* __restrict__ U, const int32_t* __restrict__ row_seq, int n_rows,
+                                    int d, int capacity, const int32_t* __restrict__ map, const T* __restrict__ carry,
+                                    const T* __restrict__ fill, T* __restrict__ out) {
+    const int r = blockIdx.x;
+    if (r >= n_rows) return;
+    const size_t pos = (size_t)row_seq[r] * capacity + U[r];
+    const int old = map[pos];
+    const T* row = old >= 0 ? carry + (size_t)old * d : fill + pos * d;
+    const int nvec = d * (int)sizeof(T) / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(row);
+    uint4* o4 = reinterpret_cast<uint4*>(out + (size_t)r * d);
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) o4[i] = s4[i];
+}
+
 __global__ void commit_kernel(uint32_t* local, uint32_t* sink, const uint32_t* sel, int n, int sink_static) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -188,6 +213,26 @@ cudaError_t launch_gather(int dtype, const int32_t* U, const int32_t* row_seq, i
         gather_kernel<float><<<n_rows, 128, 0, s>>>(U, row_seq, n_rows, d, capacity, token_ids,
                                                     (const float*)embed, (const float*)hidden_src, (float*)out,
                                                     err, vocab);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_map_rows(const int32_t* U, const int32_t* row_seq, int n_rows, int capacity, int32_t* map,
+                            cudaStream_t s) {
+    if (n_rows <= 0) return cudaSuccess;
+    map_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(U, row_seq, n_rows, capacity, map);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_carry(int dtype, const int32_t* U, const int32_t* row_seq, int n_rows, int d, int capacity,
+                                const int32_t* map, const void* carry, const void* fill, void* out, cudaStream_t s) {
+    if (n_rows <= 0) return cudaSuccess;
+    if (dtype == KVR_BF16)
+        gather_carry_kernel<__nv_bfloat16><<<n_rows, 128, 0, s>>>(U, row_seq, n_rows, d, capacity, map,
+                                                                  (const __nv_bfloat16*)carry,
+                                                                  (const __nv_bfloat16*)fill, (__nv_bfloat16*)out);
+    else
+        gather_carry_kernel<float><<<n_rows, 128, 0, s>>>(U, row_seq, n_rows, d, capacity, map, (const float*)carry,
+                                                          (const float*)fill, (float*)out);
     return cudaGetLastError();
 }
 

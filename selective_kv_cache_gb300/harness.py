@@ -11,6 +11,25 @@ from . import kvr
 from . import workloads as wl
 
 
+def merge_lora(layers, shape, stream=None):
+    """Fold each layer's LoRA (a_q/b_q on the Q rows, a_v/b_v on the V rows of
+    w_qkv) into a new w_qkv with kvr_lora_merge; returns new layer dicts."""
+    out = []
+    dt = kvr.KVR_BF16 if shape.dtype == "bf16" else kvr.KVR_F32
+    hq, hkv, dh, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.d_model
+    for L in layers:
+        M = dict(L)
+        if L.get("a_q") is not None:
+            wq = torch.empty_like(L["w_qkv"])
+            r = L["a_q"].shape[0]
+            kvr.kvr_lora_merge(L["w_qkv"], wq, shape.qkv_out, d, 0, hq * dh, L["a_q"], L["b_q"], r, 1.0, dt, stream)
+            kvr.kvr_lora_merge(wq, wq, shape.qkv_out, d, (hq + hkv) * dh, hkv * dh, L["a_v"], L["b_v"], r, 1.0, dt,
+                               stream)
+            M["w_qkv"] = wq
+        out.append(M)
+    return out
+
+
 class Setup:
     """One workload bound to a libkvr cache on the current CUDA device.
 
@@ -75,6 +94,57 @@ class Setup:
     def refresh(self, layer_begin=0, layer_end=None, flags=kvr.KVR_COMMIT_META, stream=None):
         L = self.shape.n_layers if layer_end is None else layer_end
         kvr.kvr_refresh(self.handle, self.warr, layer_begin, L, self.hidden, self.ws, self.ws_bytes, flags,
+                        stream=stream)
+
+    def refresh_interval_wise(self, layer_begin=0, layer_end=None, flags=kvr.KVR_COMMIT_META, stream=None):
+        """The interval-major comparator over the same selection: returns the
+        number of intervals.  Rows land in self.hidden in sorted order."""
+        L = self.shape.n_layers if layer_end is None else layer_end
+        longest = 1
+        for pos in self.positions:
+            u = np.sort(pos)
+            run = 1
+            for k in range(1, len(u)):
+                run = run + 1 if u[k] == u[k - 1] + 1 else 1
+                longest = max(longest, run)
+        n = int(np.asarray(self.counts).sum())
+        if n > self.hidden.shape[0]:
+            self.hidden = torch.empty((n, self.shape.d_model), dtype=self.shape.torch_dtype, device=self.device)
+        need = kvr.kvr_workspace_bytes(self.handle, max(longest, 1))
+        if self.ws is None or need > self.ws_bytes:
+            self.ws_bytes = need
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        return kvr.kvr_refresh_interval_wise(
+            self.handle, self.pos_host, self.counts, -1, token_ids=self.ids, embed_table=self.embed,
+            vocab=self.shape.vocab if self.embed is not None else 0, hidden_src=self.hidden_src,
+            weights_array=self.warr, layer_begin=layer_begin, layer_end=L, hidden_out=self.hidden,
+            workspace=self.ws, ws_bytes=self.ws_bytes, flags=flags, stream=stream)
+
+    def refresh_range(self, boundary, r0, r1, stream=None):
+        """Adapter-drift recovery: the selected rows through layers [0, r0),
+        the whole affected suffix through [r0, r1) (rows not selected enter from
+        `boundary` [batch, capacity, d], the stored hidden states at layer r0),
+        then the selected rows again through [r1, L) and the commit."""
+        w = self.w
+        L = self.shape.n_layers
+        full = [np.arange(w.suffix_start, w.n_tokens, dtype=np.int32) for _ in range(w.batch)]
+        full_pos = np.ascontiguousarray(np.concatenate(full))
+        full_cnt = np.array([len(f) for f in full], np.int32)
+        n_full = int(full_cnt.sum())
+        if getattr(self, "hidden_full", None) is None or self.hidden_full.shape[0] < n_full:
+            self.hidden_full = torch.empty((n_full, self.shape.d_model), dtype=self.shape.torch_dtype,
+                                           device=self.device)
+        need = kvr.kvr_workspace_bytes(self.handle, n_full)
+        if self.ws is None or need > self.ws_bytes:
+            self.ws_bytes = need
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.select(stream=stream)
+        kvr.kvr_refresh(self.handle, self.warr, 0, r0, self.hidden, self.ws, self.ws_bytes, 0, stream=stream)
+        kvr.kvr_reselect(self.handle, full_pos, full_cnt, self.hidden, boundary, self.hidden_full, stream=stream)
+        kvr.kvr_refresh(self.handle, self.warr, r0, r1, self.hidden_full, self.ws, self.ws_bytes, 0, stream=stream)
+        kvr.kvr_reselect(self.handle, self.pos_host, self.counts, self.hidden_full, boundary, self.hidden,
+                         stream=stream)
+        kvr.kvr_refresh(self.handle, self.warr, r1, L, self.hidden, self.ws, self.ws_bytes, kvr.KVR_COMMIT_META,
                         stream=stream)
 
     def sync(self, stream=None):

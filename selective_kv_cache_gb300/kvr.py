@@ -32,7 +32,7 @@ KVR_K_COUNT = len(KERNELS)
 EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace_bytes",
            "kvr_refresh_layer", "kvr_refresh", "kvr_attend", "kvr_sync_status", "kvr_last_error",
            "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read",
-           "kvr_refresh_layer_noalloc"]
+           "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge"]
 
 
 class kvr_model_desc(C.Structure):
@@ -63,6 +63,10 @@ lib.kvr_workspace_bytes.argtypes = [P, I32]
 lib.kvr_workspace_bytes.restype = C.c_size_t
 lib.kvr_refresh_layer.argtypes = [P, I32, C.POINTER(kvr_layer_weights), P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_refresh_layer_noalloc.argtypes = [P, I32, C.POINTER(kvr_layer_weights), P, C.c_uint32, P]
+lib.kvr_refresh_interval_wise.argtypes = [P, P, P, I32, P, P, I32, P, C.POINTER(kvr_layer_weights), I32, I32, P, P,
+                                          C.c_size_t, C.c_uint32, P, P]
+lib.kvr_reselect.argtypes = [P, P, P, P, P, P, P, P, P]
+lib.kvr_lora_merge.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, C.c_float, I32, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
@@ -167,6 +171,37 @@ def kvr_refresh(c: int, weights_array, layer_begin: int, layer_end: int, hidden_
                 flags: int = 0, stream=None):
     _check(lib.kvr_refresh(c, weights_array, layer_begin, layer_end, _ptr(hidden_inout), _ptr(workspace), ws_bytes,
                            flags, _stream(stream)), "kvr_refresh")
+
+
+def kvr_refresh_interval_wise(c: int, positions, counts, budget_percent: int = -1, token_ids=None, embed_table=None,
+                              vocab: int = 0, hidden_src=None, weights_array=None, layer_begin: int = 0,
+                              layer_end: int = 0, hidden_out=None, workspace=None, ws_bytes: int = 0,
+                              flags: int = KVR_COMMIT_META, stream=None) -> int:
+    """Returns the number of intervals."""
+    n_iv = I32()
+    pp = positions.ctypes.data if hasattr(positions, "ctypes") else _ptr(positions)
+    cp = counts.ctypes.data if hasattr(counts, "ctypes") else _ptr(counts)
+    _check(lib.kvr_refresh_interval_wise(c, pp, cp, budget_percent, _ptr(token_ids), _ptr(embed_table), vocab,
+                                         _ptr(hidden_src), weights_array, layer_begin, layer_end, _ptr(hidden_out),
+                                         _ptr(workspace), ws_bytes, flags, C.byref(n_iv), _stream(stream)),
+           "kvr_refresh_interval_wise")
+    return n_iv.value
+
+
+def kvr_reselect(c: int, positions, counts, carry_rows, fill_rows, hidden_out, stream=None):
+    n_rows = I32()
+    n_iv = I32()
+    pp = positions.ctypes.data if hasattr(positions, "ctypes") else _ptr(positions)
+    cp = counts.ctypes.data if hasattr(counts, "ctypes") else _ptr(counts)
+    _check(lib.kvr_reselect(c, pp, cp, _ptr(carry_rows), _ptr(fill_rows), _ptr(hidden_out), C.byref(n_rows),
+                            C.byref(n_iv), _stream(stream)), "kvr_reselect")
+    return n_rows.value, n_iv.value
+
+
+def kvr_lora_merge(w, w_out, n_out: int, K: int, row_begin: int, row_count: int, a, b, rank: int, scale: float,
+                   dtype: int, stream=None):
+    _check(lib.kvr_lora_merge(_ptr(w), _ptr(w_out), n_out, K, row_begin, row_count, _ptr(a), _ptr(b), rank, scale,
+                              dtype, _stream(stream)), "kvr_lora_merge")
 
 
 def kvr_attend(c: int, layer: int, q, out, workspace=None, ws_bytes: int = 0, stream=None):
