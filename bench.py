@@ -56,7 +56,7 @@ class Clocks:
     def __enter__(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
@@ -123,13 +123,14 @@ def algorithmic(shape, R, M_pairs_per_head, u_max):
     d, Hq, Hkv, dh, F = shape.d_model, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim
     qkv = (Hq + 2 * Hkv) * dh
 
-    def gemm(n_out, K):
-        return dict(flops=2.0 * R * n_out * K, bytes=2.0 * n_out * K + 2.0 * R * K + 4.0 * R * n_out)
+    def gemm(n_out, K, out_bytes=4.0):
+        return dict(flops=2.0 * R * n_out * K, bytes=2.0 * n_out * K + 2.0 * R * K + out_bytes * R * n_out)
 
     return {
         "gemm_qkv": gemm(qkv, d),
         "gemm_o": gemm(d, Hq * dh),
-        "gemm_gate_up": gemm(2 * F, d),
+        # SwiGLU is fused: the output is silu(g) * u in bf16, half as many features
+        "gemm_gate_up": gemm(2 * F, d, out_bytes=1.0),
         "gemm_down": gemm(d, F),
         "attention": dict(flops=4.0 * dh * Hq * M_pairs_per_head,
                           bytes=2.0 * 2 * Hkv * dh * (u_max + 1) + 2.0 * 2 * R * Hq * dh),
@@ -256,6 +257,11 @@ def run_ours(args):
     breakdown = {k: {"launches_per_step": n / args.steps, "us_per_step": round(v * 1e3 / args.steps, 1)}
                  for k, (n, v) in per_kernel.items()}
 
+    # ---- packed vs interval-wise on the fragmented workload (same model and cache)
+    cmp = None
+    if not args.no_compare and args.workload == "llama8b":
+        cmp = compare_schedules(s, args)
+
     # ---- CPU oracle baseline on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -281,12 +287,55 @@ def run_ours(args):
         "kernels": breakdown,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
+        "packed_vs_interval": cmp,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
     s.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def compare_schedules(s1, args):
+    """The fragmented workload (282 isolated positions of the same 5632-token
+    suffix, same model and cache): layer-major packed refresh against the
+    interval-major schedule, CUDA events around whole refreshes."""
+    import torch
+
+    from selective_kv_cache_gb300 import workloads as wl
+    from selective_kv_cache_gb300.harness import Setup
+
+    w = wl.WORKLOADS["llama8b_frag"]
+    s = Setup(w, weights=s1.layers, cache=(s1.K, s1.V))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def packed():
+        s.select(stream=stream)
+        s.refresh(stream=stream)
+
+    for _ in range(args.warmup):
+        packed()
+    t_packed = timed(packed, args.steps)
+    n_iv = s.refresh_interval_wise(stream=stream)   # warm-up
+    s.sync()
+    t_iv = timed(lambda: s.refresh_interval_wise(stream=stream), max(1, min(2, args.steps)))
+    s.sync()
+    s.close()
+    return {"workload": f"{w.name}: same model, N={w.n_tokens}, {w.n_select} isolated positions in "
+                        f"[{w.suffix_start},{w.n_tokens}) ({n_iv} intervals)",
+            "packed_ms": round(t_packed, 3), "interval_wise_ms": round(t_iv, 3),
+            "speedup": round(t_iv / t_packed, 2), "intervals": n_iv,
+            "packed_tokens_per_s": round(w.n_select / (t_packed / 1e3), 1)}
 
 
 def cpu_baseline(s, w, reference_line=False):
@@ -371,11 +420,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-compare", action="store_true", help="skip the packed vs interval-wise comparison")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
