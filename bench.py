@@ -262,6 +262,11 @@ def run_ours(args):
     if not args.no_compare and args.workload == "llama8b":
         cmp = compare_schedules(s, args)
 
+    # ---- Shift of the same edit (the step before the refresh), on its own cache
+    shift = None
+    if args.workload == "llama8b":
+        shift = measure_shift(w, hbm)
+
     # ---- CPU oracle baseline on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -288,12 +293,51 @@ def run_ours(args):
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
         "packed_vs_interval": cmp,
+        "shift": shift,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
     s.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_shift(w, hbm_peak, reps=10):
+    """Shift for the Llama-shaped edit: an 8192-token cache (32 layers, 8 K/V
+    heads x 128, bf16) loses the 512-token span at 2048, so 5632 rows per
+    (layer, head) move down with their keys re-rotated.  One fresh cache per
+    repetition (the shift changes the cache's length); CUDA events around the
+    kvr_shift call.  The cache (1.07 GB) is larger than L2."""
+    import torch
+
+    from selective_kv_cache_gb300 import kvr
+
+    m = w.model
+    cap, start, d = 8192, 2048, 512
+    shape = (1, m.n_layers, m.n_kv_heads, cap, m.head_dim)
+    K = torch.randn(shape, device="cuda").to(torch.bfloat16)
+    V = torch.randn(shape, device="cuda").to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 2):
+        h = kvr.kvr_create_cache(kvr.model_desc(m), 1, cap, K, V, cap, start)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kvr.kvr_shift(h, start, d, stream=stream)
+        e1.record(stream)
+        kvr.kvr_sync_status(h, stream)
+        kvr.kvr_destroy_cache(h)
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    moved = cap - start - d
+    nbytes = 2 * 2 * m.n_layers * m.n_kv_heads * moved * m.head_dim * 2   # K and V, read and write
+    us = sorted(times)[len(times) // 2] * 1e3
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"workload": f"delete [{start},{start + d}) of a {cap}-token Llama-3-8B-shaped cache "
+                        f"({m.n_layers} L x {m.n_kv_heads} K/V heads x {m.head_dim}, bf16)",
+            "us_median": round(us, 1), "bytes": int(nbytes), "achieved_gbs": round(gbs, 1), "peak_gbs": hbm_peak,
+            "frac": round(gbs / hbm_peak, 4), "reps": reps}
 
 
 def compare_schedules(s1, args):

@@ -279,6 +279,54 @@ kvr_status kvr_refresh_layer_noalloc(kvr_cache* c, int32_t layer, const kvr_laye
 kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out,
                       void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * kvr_shift -- Shift after a deletion ("Budgeted KV-Cache Repair for Evolving
+ * Contexts", Sec. 7.1, Eq. 2): positions [start, start + d) are removed from
+ * every sequence.  In every (sequence, layer, K/V head) the rows
+ * [start + d, n_tokens) move down to [start, n_tokens - d).  Keys are stored
+ * after the rotary map, so a key that moves from i to i - d becomes
+ * R_{i-d} R_i^{-1} k = R_{-d} k: one rotation by -d positions, the same for
+ * every row.  Values carry no position and move unchanged.  The local and
+ * sink bits move with their positions; the bits of [n_tokens - d, n_tokens)
+ * are cleared.  Cache rows [n_tokens - d, n_tokens) keep their old contents
+ * (they are now past the end and no attention reads them).
+ *   In place, on the cache's own K/V buffers, with one read and one write of
+ *   each moved row.  Afterwards n_tokens -= d and
+ *   suffix_start = min(suffix_start, start): every row from the deletion on
+ *   was computed with the deleted span visible.  The current selection is
+ *   dropped (kvr_select again before a refresh or kvr_attend).
+ *   EINVAL: start < 0, d < 0, start + d > n_tokens, or d == n_tokens.
+ *   d == 0 enqueues nothing.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_shift(kvr_cache* c, int32_t start, int32_t d, void* stream);
+
+/* kvr_splice flags */
+#define KVR_SPLICE_LOCAL 0x1u   /* mark the spliced positions type local */
+#define KVR_SPLICE_SINK 0x2u    /* mark the block's first min(4, n) positions as members of S' */
+
+/* ---------------------------------------------------------------------------
+ * kvr_splice -- place a block whose K/V were computed on their own at new
+ * global positions ("Models Take Notes at Prefill: KV Cache Can Be Editable
+ * and Composable", Sec. 5: the chunk's keys are re-rotated from their source
+ * positions to the target positions; values carry no position).  This builds
+ * a mixed cache out of independently prefilled blocks ("kv-cross-attention-
+ * reuse", Sec. 6: blocks B_1..B_m).
+ *   k_src, v_src  device [n_layers][n_kv_heads][n][head_dim], model dtype;
+ *                 row i holds the block's token i, its key rotated at
+ *                 position src_pos + i.  Must not overlap the cache.
+ *   Row i lands in cache row dst_pos + i of sequence `seq` in every layer and
+ *   head, its key rotated by dst_pos - src_pos.  Other rows are untouched.
+ *   flags: KVR_SPLICE_LOCAL sets the local bit of [dst_pos, dst_pos + n);
+ *   KVR_SPLICE_SINK sets the sink bit of the block's first min(4, n)
+ *   positions (the block's own attention sinks, "kv-cross-attention-reuse",
+ *   Sec. 6.4).  Bits are only ever set, never cleared, by this call.
+ *   EINVAL: NULL or non-16-byte-aligned sources, seq outside [0, batch),
+ *   n < 0, dst_pos < 0, src_pos < 0, or dst_pos + n > n_tokens.
+ *   n == 0 enqueues nothing.  The selection, if any, stays as it is.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_splice(kvr_cache* c, int32_t seq, int32_t dst_pos, int32_t n, const void* k_src,
+                      const void* v_src, int32_t src_pos, uint32_t flags, void* stream);
+
 /* Synchronise `stream` and report device-side failures recorded since the
  * last call (ETIMEOUT / EDEVICE), clearing them. */
 kvr_status kvr_sync_status(kvr_cache* c, void* stream);
@@ -304,6 +352,9 @@ kvr_status kvr_read_selection(kvr_cache* c, int32_t seq, int32_t* U, int32_t u_c
                               int32_t* plan, int32_t plan_cap, int32_t* n_tiles,
                               int32_t* rows_per_tile, int32_t* keys_per_tile);
 kvr_status kvr_read_meta(kvr_cache* c, uint32_t* local_bits, uint32_t* sink_bits);
+/* kvr_cache_info: the cache's current n_tokens and suffix_start (host state,
+ * no device work).  Either pointer may be NULL. */
+kvr_status kvr_cache_info(kvr_cache* c, int32_t* n_tokens, int32_t* suffix_start);
 
 /* ---------------------------------------------------------------------------
  * Per-kernel timing.  When enabled, every launch of a library kernel on the

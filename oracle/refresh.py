@@ -5,6 +5,8 @@ Sources (cited by page title and section):
   [KVX]  "kv-cross-attention-reuse" (mixed cache and operator F), Sec. 6
   [CRF]  "CacheReforge: Bounded Recovery for Stale KV Caches under Evolving
          Adapters"
+  [NOTES] "Models Take Notes at Prefill: KV Cache Can Be Editable and
+         Composable" (re-rotating a chunk's keys to new positions), Sec. 5
 
 Model block (the pages run dense Llama/Qwen decoders): pre-norm RMSNorm,
 Q/K/V projections (+bias for Qwen2.5 shapes), rotate-half RoPE at global
@@ -33,7 +35,7 @@ from .select import effective_masks, intervals, sorted_positions
 __all__ = [
     "Spec", "round_bf16", "round_store", "rms_norm", "rope", "silu",
     "attention", "layer_rows", "refresh_packed", "refresh_interval",
-    "refresh_range", "prefill", "shift", "attend", "lora_delta",
+    "refresh_range", "prefill", "shift", "reposition", "attend", "lora_delta",
 ]
 
 BF16_MAX = float.fromhex("0x1.fep127")
@@ -376,10 +378,22 @@ def shift(K, V, start, d, theta):
     lead = K.shape[:-2]
     Kn = np.concatenate([K[..., :start, :], np.zeros(lead + (n_move, K.shape[-1]))], axis=-2)
     Vn = np.concatenate([V[..., :start, :], V[..., start + d:, :]], axis=-2)
-    moved = K[..., start + d:, :].reshape(-1, n_move, K.shape[-1])
+    moved = K[..., start + d:, :].reshape(int(np.prod(lead)), n_move, K.shape[-1])
     rot = rope(moved, np.full(n_move, -d), theta)
     Kn[..., start:, :] = rot.reshape(lead + (n_move, K.shape[-1]))
     return Kn, Vn
+
+
+def reposition(K, V, src_pos, dst_pos, theta):
+    """Move a block computed on its own to new global positions ([NOTES]
+    Sec. 5): keys stored after the rotary map at src_pos + i are re-rotated
+    to dst_pos + i, i.e. rotated by dst_pos - src_pos; values carry no
+    position and are returned as they are.  K, V [..., n, d_h]."""
+    K = np.asarray(K, dtype=np.float64)
+    n = K.shape[-2]
+    flat = K.reshape(-1, n, K.shape[-1])
+    Kn = rope(flat, np.full(n, float(dst_pos) - float(src_pos)), theta).reshape(K.shape)
+    return Kn, np.asarray(V, dtype=np.float64).copy()
 
 
 def attend(q, K_l, V_l, positions, local, sink, alpha, beta):

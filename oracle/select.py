@@ -14,7 +14,7 @@ import numpy as np
 __all__ = [
     "budget", "validate_selection", "sorted_positions", "intervals",
     "bitmask_words", "effective_masks", "tile_plan", "pair_count",
-    "seam_set", "block_of",
+    "seam_set", "block_of", "shift_mask",
 ]
 
 
@@ -141,3 +141,16 @@ def seam_set(bounds, tau: int) -> np.ndarray:
     s_m, e_m = bounds[m - 1]
     sel |= set(range(max(s_m, e_m - tau), e_m))
     return np.array(sorted(sel), dtype=np.int64)
+
+
+def shift_mask(mask, start: int, d: int):
+    """Per-position flags after Shift deletes [start, start + d) ([BKR]
+    Sec. 7.1, Eq. 2): a flag stays with its token, so positions below start
+    keep theirs, position p >= start takes the flag of old position p + d,
+    and the last d positions, now past the end, read False."""
+    m = np.asarray(mask, dtype=bool)
+    out = np.zeros_like(m)
+    out[..., :start] = m[..., :start]
+    n_move = m.shape[-1] - start - d
+    out[..., start:start + n_move] = m[..., start + d:]
+    return out

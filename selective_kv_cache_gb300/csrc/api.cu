@@ -37,6 +37,17 @@ bool get_encode(std::string* why) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// (cos, sin) of delta * theta^(-2i/head_dim) for i < head_dim/2, the angles
+// formed in double as for the rotary table; a rotation by delta positions
+void rotation_table(const kvr_model_desc& m, double delta, float2* cs) {
+    const int half = m.head_dim / 2;
+    for (int i = 0; i < 64; ++i) cs[i] = make_float2(1.f, 0.f);
+    for (int i = 0; i < half; ++i) {
+        const double a = delta * std::pow(m.rope_theta, -2.0 * i / (double)m.head_dim);
+        cs[i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+}
 int dtype_size(int dtype) { return dtype == KVR_BF16 ? 2 : 4; }
 
 struct WsLayout {
@@ -828,6 +839,85 @@ kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, 
     KVR_CHECK_LAUNCH(launch_lora_merge(dtype, w, w_out, n_out, K, row_begin, row_count, a, b, rank, scale,
                                        reinterpret_cast<cudaStream_t>(stream)),
                      "lora merge");
+    return KVR_OK;
+}
+
+kvr_status kvr_shift(kvr_cache* c, int32_t start, int32_t d, void* stream) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (start < 0 || d < 0 || (int64_t)start + d > c->n_tokens || d == c->n_tokens) {
+        set_error("shift: need 0 <= start, 0 <= d, start + d <= n_tokens and d < n_tokens");
+        return KVR_EINVAL;
+    }
+    if (d == 0) return KVR_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const kvr_model_desc& m = c->m;
+    MoveLaunch a{};
+    a.k_src = c->k_base;
+    a.v_src = c->v_base;
+    a.k_dst = c->k_base;
+    a.v_dst = c->v_base;
+    a.src_slab_rows = a.dst_slab_rows = c->capacity;
+    a.dst_slab_off = 0;
+    a.src_row0 = start + d;
+    a.dst_row0 = start;
+    a.n_rows = c->n_tokens - start - d;
+    a.n_slabs = c->batch * m.n_layers * m.n_kv_heads;
+    rotation_table(m, -(double)d, a.cs);
+    KVR_CHECK_LAUNCH(launch_move_rows(m.dtype, m.head_dim, a, true, s), "shift rows");
+    KVR_CHECK_LAUNCH(launch_shift_bits(c->d_local, c->d_sink, c->batch, c->words, start, d, c->n_tokens, s),
+                     "shift metadata");
+    c->n_tokens -= d;
+    c->suffix_start = std::min(c->suffix_start, start);
+    c->sel = Selection{};
+    return KVR_OK;
+}
+
+kvr_status kvr_splice(kvr_cache* c, int32_t seq, int32_t dst_pos, int32_t n, const void* k_src,
+                      const void* v_src, int32_t src_pos, uint32_t flags, void* stream) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (seq < 0 || seq >= c->batch || n < 0 || dst_pos < 0 || src_pos < 0 || (int64_t)dst_pos + n > c->n_tokens) {
+        set_error("splice: need 0 <= seq < batch, n >= 0, dst_pos >= 0, src_pos >= 0, dst_pos + n <= n_tokens");
+        return KVR_EINVAL;
+    }
+    if (n == 0) return KVR_OK;
+    if (!k_src || !v_src || !aligned16(k_src) || !aligned16(v_src)) {
+        set_error("splice: K/V sources must be non-NULL and 16-byte aligned");
+        return KVR_EINVAL;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const kvr_model_desc& m = c->m;
+    MoveLaunch a{};
+    a.k_src = k_src;
+    a.v_src = v_src;
+    a.k_dst = c->k_base;
+    a.v_dst = c->v_base;
+    a.src_slab_rows = n;
+    a.dst_slab_rows = c->capacity;
+    a.dst_slab_off = (int64_t)seq * m.n_layers * m.n_kv_heads;
+    a.src_row0 = 0;
+    a.dst_row0 = dst_pos;
+    a.n_rows = n;
+    a.n_slabs = m.n_layers * m.n_kv_heads;
+    rotation_table(m, (double)dst_pos - (double)src_pos, a.cs);
+    KVR_CHECK_LAUNCH(launch_move_rows(m.dtype, m.head_dim, a, false, s), "splice rows");
+    const size_t off = (size_t)seq * c->words;
+    KVR_CHECK_LAUNCH(launch_set_bits(c->d_local + off, c->d_sink + off, dst_pos, n, flags, s), "splice metadata");
+    return KVR_OK;
+}
+
+kvr_status kvr_cache_info(kvr_cache* c, int32_t* n_tokens, int32_t* suffix_start) {
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (n_tokens) *n_tokens = c->n_tokens;
+    if (suffix_start) *suffix_start = c->suffix_start;
     return KVR_OK;
 }
 

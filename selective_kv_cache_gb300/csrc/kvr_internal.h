@@ -121,6 +121,29 @@ cudaError_t launch_gather_carry(int dtype, const int32_t* U, const int32_t* row_
 cudaError_t launch_lora_merge(int dtype, const void* w, void* w_out, int n_out, int K, int row_begin, int row_count,
                               const void* a, const void* b, int rank, float scale, cudaStream_t s);
 
+// Row move with key re-rotation (Shift / splice).  Slab = one (sequence,
+// layer, K/V head) run of rows; source slab i maps to destination slab
+// i + dst_slab_off.  Rows [src_row0, src_row0 + n_rows) of a source slab land
+// at dst_row0.. of its destination slab; keys are rotated by the angle table
+// cs[i] = (cos, sin) of delta * theta^(-2i/head_dim), values copied.
+struct MoveLaunch {
+    const void* k_src;
+    const void* v_src;
+    void* k_dst;
+    void* v_dst;
+    int64_t src_slab_rows;
+    int64_t dst_slab_rows;
+    int64_t dst_slab_off;
+    int32_t src_row0, dst_row0, n_rows, chunk, n_slabs;
+    float2 cs[64];
+};
+// in_place: source and destination are the same buffers, dst_row0 <= src_row0
+cudaError_t launch_move_rows(int dtype, int head_dim, const MoveLaunch& a, bool in_place, cudaStream_t s);
+cudaError_t launch_shift_bits(uint32_t* local, uint32_t* sink, int batch, int words, int start, int d, int n_old,
+                              cudaStream_t s);
+// local/sink point at the sequence's own words
+cudaError_t launch_set_bits(uint32_t* local, uint32_t* sink, int dst, int n, uint32_t flags, cudaStream_t s);
+
 // RMSNorm: in is model dtype (in_f32 = 0) or fp32 (in_f32 = 1), out model dtype.
 cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w, void* out, int rows, int d,
                            float eps, cudaStream_t s);

@@ -25,6 +25,8 @@ STATUS_NAMES = ["OK", "EINVAL", "ERANGE", "ENOMEM", "ECUDA", "ETIMEOUT", "EDEVIC
 KVR_F32, KVR_BF16 = 0, 1
 KVR_SINK_STATIC = 0x1
 KVR_COMMIT_META = 0x1
+KVR_SPLICE_LOCAL = 0x1
+KVR_SPLICE_SINK = 0x2
 KERNELS = ["select", "gather", "rmsnorm", "gemm_qkv", "epi_qkv", "attention", "gemm_o", "epi_o",
            "gemm_gate_up", "epi_gate_up", "gemm_down", "epi_down", "commit"]
 KVR_K_COUNT = len(KERNELS)
@@ -32,7 +34,8 @@ KVR_K_COUNT = len(KERNELS)
 EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace_bytes",
            "kvr_refresh_layer", "kvr_refresh", "kvr_attend", "kvr_sync_status", "kvr_last_error",
            "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read",
-           "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge"]
+           "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge",
+           "kvr_shift", "kvr_splice", "kvr_cache_info"]
 
 
 class kvr_model_desc(C.Structure):
@@ -67,6 +70,9 @@ lib.kvr_refresh_interval_wise.argtypes = [P, P, P, I32, P, P, I32, P, C.POINTER(
                                           C.c_size_t, C.c_uint32, P, P]
 lib.kvr_reselect.argtypes = [P, P, P, P, P, P, P, P, P]
 lib.kvr_lora_merge.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, C.c_float, I32, P]
+lib.kvr_shift.argtypes = [P, I32, I32, P]
+lib.kvr_splice.argtypes = [P, I32, I32, I32, P, P, I32, C.c_uint32, P]
+lib.kvr_cache_info.argtypes = [P, P, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
@@ -202,6 +208,24 @@ def kvr_lora_merge(w, w_out, n_out: int, K: int, row_begin: int, row_count: int,
                    dtype: int, stream=None):
     _check(lib.kvr_lora_merge(_ptr(w), _ptr(w_out), n_out, K, row_begin, row_count, _ptr(a), _ptr(b), rank, scale,
                               dtype, _stream(stream)), "kvr_lora_merge")
+
+
+def kvr_shift(c: int, start: int, d: int, stream=None):
+    _check(lib.kvr_shift(c, start, d, _stream(stream)), "kvr_shift")
+
+
+def kvr_splice(c: int, seq: int, dst_pos: int, n: int, k_src, v_src, src_pos: int = 0, flags: int = 0,
+               stream=None):
+    _check(lib.kvr_splice(c, seq, dst_pos, n, _ptr(k_src), _ptr(v_src), src_pos, flags, _stream(stream)),
+           "kvr_splice")
+
+
+def kvr_cache_info(c: int):
+    """(n_tokens, suffix_start) of the cache now."""
+    n = C.c_int32()
+    s = C.c_int32()
+    _check(lib.kvr_cache_info(c, C.byref(n), C.byref(s)), "kvr_cache_info")
+    return n.value, s.value
 
 
 def kvr_attend(c: int, layer: int, q, out, workspace=None, ws_bytes: int = 0, stream=None):

@@ -55,3 +55,6 @@ def test_host_validation_needs_no_gpu(lib):
     assert st == kvr.KVR_EUNSUPPORTED
     assert kvr.lib.kvr_select(None, None, None, -1, None, None, 0, None, None, None, None, None) == kvr.KVR_EINVAL
     assert kvr.kvr_workspace_bytes(None, 10) == 0
+    assert kvr.lib.kvr_shift(None, 0, 1, None) == kvr.KVR_EINVAL
+    assert kvr.lib.kvr_splice(None, 0, 0, 1, None, None, 0, 0, None) == kvr.KVR_EINVAL
+    assert kvr.lib.kvr_cache_info(None, None, None) == kvr.KVR_EINVAL

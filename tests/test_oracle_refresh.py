@@ -326,6 +326,10 @@ def test_shift_eq2():
     want = oracle.rope(raw[..., start + d:, :].reshape(-1, N - start - d, dh),
                        np.arange(start, N - d), theta).reshape(Kn[..., start:, :].shape)
     np.testing.assert_allclose(Kn[..., start:, :], want, atol=1e-10)
+    # a deletion that reaches the end moves nothing and only shortens the cache
+    Kt, Vt = oracle.shift(K, V, N - d, d, theta)
+    np.testing.assert_array_equal(Kt, K[..., :N - d, :])
+    np.testing.assert_array_equal(Vt, V[..., :N - d, :])
 
 
 def test_refresh_range_equals_layerwise_definition():
@@ -352,3 +356,27 @@ def test_refresh_range_equals_layerwise_definition():
     np.testing.assert_array_equal(K2[0][:, others], Ks[0][:, others])
     np.testing.assert_array_equal(K2[2][:, others], Ks[2][:, others])
     assert np.abs(K2[1][:, others] - Ks[1][:, others]).max() > 1e-3
+
+
+def test_reposition_notes_sec5():
+    """Repositioning (Models Take Notes at Prefill, Sec. 5): a block whose keys
+    were rotated at src.. and then moved to dst.. equals the same pre-rotation
+    keys rotated at dst.. directly; values are untouched; moves compose, and a
+    move by zero is the identity."""
+    rng = np.random.default_rng(53)
+    n, dh, theta = 9, 16, 1e4
+    raw = rng.standard_normal((2, 3, n, dh))
+    V = rng.standard_normal((2, 3, n, dh))
+    at = lambda p0: oracle.rope(raw.reshape(-1, n, dh), np.arange(p0, p0 + n), theta).reshape(raw.shape)
+    K5 = at(5)
+    Kd, Vd = oracle.reposition(K5, V, 5, 1000, theta)
+    np.testing.assert_allclose(Kd, at(1000), atol=1e-10)
+    np.testing.assert_array_equal(Vd, V)
+    K2, _ = oracle.reposition(*oracle.reposition(K5, V, 5, 40, theta), 40, 1000, theta)
+    np.testing.assert_allclose(K2, Kd, atol=1e-10)
+    np.testing.assert_allclose(oracle.reposition(K5, V, 7, 7, theta)[0], K5, atol=0)
+    # moving down by d is what Shift does to the moved suffix
+    K = at(0)
+    Ks, _ = oracle.shift(K, V, 2, 3, theta)
+    np.testing.assert_allclose(Ks[..., 2:, :], oracle.reposition(K[..., 5:, :], V[..., 5:, :], 5, 2, theta)[0],
+                               atol=1e-12)

@@ -173,3 +173,22 @@ def test_seam_set_brute_force_and_count():
     T = oracle.seam_set(bounds, 64)
     assert T.size == 896
     assert oracle.intervals(T).shape[0] == 8
+
+
+def test_shift_mask_worked_example_and_brute_force():
+    """Flags move with their tokens under Shift (Budgeted KV-Cache Repair,
+    Sec. 7.1, Eq. 2).  Worked by hand: flags at 1, 3, 5, 8, 9 of ten
+    positions; deleting [2, 5) drops 3 and moves 5 -> 2, 8 -> 5, 9 -> 6."""
+    m = np.isin(np.arange(10), [1, 3, 5, 8, 9])
+    np.testing.assert_array_equal(np.flatnonzero(oracle.shift_mask(m, 2, 3)), [1, 2, 5, 6])
+    rng = np.random.default_rng(71)
+    for _ in range(50):
+        N = int(rng.integers(1, 200))
+        start = int(rng.integers(0, N))
+        d = int(rng.integers(0, N - start + 1))
+        m = rng.random((2, N)) < 0.4
+        want = np.zeros_like(m)
+        for b in range(2):
+            kept = [m[b, p] for p in range(N) if not (start <= p < start + d)]
+            want[b, :len(kept)] = kept
+        np.testing.assert_array_equal(oracle.shift_mask(m, start, d), want)
