@@ -47,6 +47,13 @@ constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
 
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -246,8 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        // base-2 logit of key k: x_k = (s_k + bias_k) * sl2, the bias in raw
+        // score units (alpha*sqrt(d_h) for local keys, beta*sqrt(d_h) for S'),
+        // -inf past the row's causal limit
         const float sl2 = 1.4426950408889634f / sqrtf(128.0f);
-        const float al2 = a.alpha * 1.4426950408889634f, bl2 = a.beta * 1.4426950408889634f;
+        const float ar = a.alpha * sqrtf(128.0f), br = a.beta * sqrtf(128.0f);
         const bool biased = a.alpha != 0.f || a.beta != 0.f;
         const uint32_t* loc = a.loc + (size_t)seq * a.words;
         const uint32_t* snk = a.snk + (size_t)seq * a.words;
@@ -267,30 +277,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&s_free[sb]);
 
             const int key0 = (jb + j) * 128;
-            uint32_t lw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
+            const bool masked = jb + j >= n_full;
             if (biased) {
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int wd = (key0 >> 5) + t;
-                    if (wd < a.words) {
-                        lw[t] = loc[wd];
-                        sw[t] = snk[wd];
+                    const uint32_t lw = wd < a.words ? loc[wd] : 0u;
+                    const uint32_t sw = wd < a.words ? snk[wd] : 0u;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        float b = ((lw >> k) & 1u) ? ar : 0.f;
+                        b += ((sw >> k) & 1u) ? br : 0.f;
+                        s[32 * t + k] += b;
                     }
                 }
             }
-            const bool masked = jb + j >= n_full;
-            float mt = -INFINITY;
+            if (masked) {
+                const int lim = g - key0;   // keys k > lim are in the row's future
 #pragma unroll
-            for (int k = 0; k < 128; ++k) {
-                float x = s[k] * sl2;
-                if (biased) {
-                    x += ((lw[k >> 5] >> (k & 31)) & 1u) ? al2 : 0.f;
-                    x += ((sw[k >> 5] >> (k & 31)) & 1u) ? bl2 : 0.f;
-                }
-                if (masked && key0 + k > g) x = -INFINITY;
-                s[k] = x;
-                mt = fmaxf(mt, x);
+                for (int k = 0; k < 128; ++k)
+                    if (k > lim) s[k] = -INFINITY;
             }
+            // row max over 8 independent chains of 3-input maxima
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mx[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+                for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
+            }
+            const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
             // the previous PV must finish before P is overwritten or O rescaled
             if (j > 0) {
                 if (!warp_wait(o_done, (uint32_t)(j - 1) & 1u)) {
@@ -313,21 +329,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (raise) l_run *= f;
             }
             if (raise) m_run = mt;
-            float ls0 = 0.f, ls1 = 0.f;
+            // p = 2^(x - m): one packed FMA per two keys, then ex2; l sums the
+            // probabilities exactly as the PV product sees them (bf16)
+            const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    pk[t] = pack_bf16(ex2(s[c * 8 + 2 * t] - m_run), ex2(s[c * 8 + 2 * t + 1] - m_run));
-                    // l sums the probabilities exactly as the PV product sees them (bf16)
-                    ls0 += __uint_as_float(pk[t] << 16);
-                    ls1 += __uint_as_float(pk[t] & 0xffff0000u);
+                    const float2 x = __ffma2_rn(make_float2(s[c * 8 + 2 * t], s[c * 8 + 2 * t + 1]), sc, nm);
+                    pk[t] = pack_bf16(ex2(x.x), ex2(x.y));
+                    acc[t] = __fadd2_rn(acc[t], make_float2(__uint_as_float(pk[t] << 16),
+                                                            __uint_as_float(pk[t] & 0xffff0000u)));
                 }
                 st_shared_v4(tile_chunk(sbase + kOffP, m, c), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             }
-            const float ls = ls0 + ls1;
-            l_run += ls;
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a03 = __fadd2_rn(a01, a23);
+            l_run += a03.x + a03.y;
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
