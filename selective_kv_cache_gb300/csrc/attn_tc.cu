@@ -37,14 +37,15 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
-constexpr int kKStages = 3;                     // K runs ahead of V: S needs K first
-constexpr int kVStages = 2;
+constexpr int kKStages = 3;                     // K runs one tile ahead of V: S needs K first
+constexpr int kVStages = 3;
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffP = kTile;
-constexpr uint32_t kOffK = 2 * kTile;
+constexpr uint32_t kOffK = kTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kTmemO = 256;                 // TMEM columns: S[0] 0-127, S[1] 128-255, O 256-383,
+constexpr uint32_t kTmemP = 384;                 // P[0] 384-447, P[1] 448-511 (bf16 pairs)
 constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
 
 // max of three (one instruction on sm_100 and later)
@@ -89,16 +90,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* k_full = bars + 0;     // [3]
-    uint64_t* k_empty = bars + 3;    // [3]
-    uint64_t* v_full = bars + 6;     // [2]
-    uint64_t* v_empty = bars + 8;    // [2]
-    uint64_t* s_full = bars + 10;    // [2]
-    uint64_t* s_free = bars + 12;    // [2]
-    uint64_t* p_full = bars + 14;
-    uint64_t* o_done = bars + 15;
-    uint64_t* mma_done = bars + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+    uint64_t* k_full = bars + 0;                          // [kKStages]
+    uint64_t* k_empty = k_full + kKStages;                // [kKStages]
+    uint64_t* v_full = k_empty + kKStages;                // [kVStages]
+    uint64_t* v_empty = v_full + kVStages;                // [kVStages]
+    uint64_t* s_full = v_empty + kVStages;                // [2]
+    uint64_t* s_free = s_full + 2;                        // [2]
+    uint64_t* p_full = s_free + 2;                        // [2], per P buffer
+    uint64_t* o_done = p_full + 2;                        // [2], PV of tile j commits o_done[j & 1]
+    uint64_t* mma_done = o_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
     const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
@@ -126,14 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -233,19 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int st = j % kVStages;
-                if (!mbar_wait(p_full, (uint32_t)j & 1u) || !mbar_wait(&v_full[st], (uint32_t)(j / kVStages) & 1u)) {
+                if (!mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u) ||
+                    !mbar_wait(&v_full[st], (uint32_t)(j / kVStages) & 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t pa = sbase + kOffP, va = sbase + kOffV + st * kTile;
+                const uint32_t pt = tmem + kTmemP + (uint32_t)(j & 1) * 64u, va = sbase + kOffV + st * kTile;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16(tmem + 256u, sdesc_sw128(pa + off, 16, 1024),
-                             sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
+                    mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)kk * 8u, sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024),
+                                idesc_o, (j > 0 || kk > 0));
                 }
-                mma_commit(o_done);
+                mma_commit(&o_done[j & 1]);
                 mma_commit(&v_empty[st]);
             }
             mma_commit(mma_done);
@@ -307,55 +310,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
             }
             const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-            // the previous PV must finish before P is overwritten or O rescaled
-            if (j > 0) {
-                if (!warp_wait(o_done, (uint32_t)(j - 1) & 1u)) {
+            // O is rescaled only after the previous PV has finished; P[j & 1] is
+            // rewritten only after the PV two tiles back (which read it) has
+            const bool raise = mt > m_run + kRescale;
+            const bool rescale = __any_sync(0xffffffffu, raise && j > 0);
+            if (rescale) {
+                if (!warp_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
             }
-            const bool raise = mt > m_run + kRescale;
-            if (__any_sync(0xffffffffu, raise && j > 0)) {
+            if (j >= 2) {
+                if (!warp_wait(&o_done[j & 1], (uint32_t)((j - 2) >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (rescale) {
                 const float f = raise ? ex2(m_run - mt) : 1.f;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
-                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                    tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) o[t] *= f;
-                    tmem_st16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                    tmem_st16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
                 }
                 if (raise) l_run *= f;
             }
             if (raise) m_run = mt;
             // p = 2^(x - m): one packed FMA per two keys, then ex2; l sums the
             // probabilities exactly as the PV product sees them (bf16)
+            // P goes to tensor memory as the PV product's A operand: column c of
+            // the row holds keys 2c, 2c+1 as packed bf16
             const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
+            const uint32_t ptm = tmem + lane_base + kTmemP + (uint32_t)(j & 1) * 64u;
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint32_t pk[4];
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 x = __ffma2_rn(make_float2(s[c * 8 + 2 * t], s[c * 8 + 2 * t + 1]), sc, nm);
+                for (int t = 0; t < 16; ++t) {
+                    const int k = 32 * c + 2 * t;
+                    const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), sc, nm);
                     pk[t] = pack_bf16(ex2(x.x), ex2(x.y));
-                    acc[t] = __fadd2_rn(acc[t], make_float2(__uint_as_float(pk[t] << 16),
-                                                            __uint_as_float(pk[t] & 0xffff0000u)));
+                    acc[t & 3] = __fadd2_rn(acc[t & 3], make_float2(__uint_as_float(pk[t] << 16),
+                                                                    __uint_as_float(pk[t] & 0xffff0000u)));
                 }
-                st_shared_v4(tile_chunk(sbase + kOffP, m, c), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                tmem_st16_async(ptm + 16u * (uint32_t)c, pk);
             }
+            tmem_wait_st();
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a03 = __fadd2_rn(a01, a23);
             l_run += a03.x + a03.y;
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[j & 1]);
         }
         if (ok && n_total > 0) {
-            if (!warp_wait(o_done, (uint32_t)(n_total - 1) & 1u)) {
+            if (!warp_wait(&o_done[(n_total - 1) & 1], (uint32_t)((n_total - 1) >> 1) & 1u)) {
                 ok = false;
             } else if (n_split == 1) {
                 tc_fence_after();
@@ -364,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
-                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                    tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
                     if (row_valid) {
                         uint4 v0, v1;
                         v0.x = pack_bf16(o[0] * inv, o[1] * inv);
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
-                    tmem_ld16(tmem + lane_base + 256u + (uint32_t)c * 16u, o);
+                    tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
 #pragma unroll
                     for (int t = 0; t < 4; ++t)
                         reinterpret_cast<float4*>(po + c * 16)[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
