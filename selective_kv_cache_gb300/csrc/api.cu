@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -396,6 +397,23 @@ kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_by
 
 void set_error(const std::string& msg) { g_err = msg; }
 
+namespace {
+thread_local bool t_pdl_armed = false;
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("KVR_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+}  // namespace
+void pdl_begin_call() { t_pdl_armed = false; }
+bool pdl_take() {
+    const bool r = t_pdl_armed && pdl_enabled();
+    t_pdl_armed = true;
+    return r;
+}
+
 kvr_status cuda_fail(cudaError_t e, const char* what) {
     set_error(std::string(what) + ": " + cudaGetErrorString(e));
     return KVR_ECUDA;
@@ -717,6 +735,7 @@ kvr_status kvr_destroy_cache(kvr_cache* c) {
 kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
                       const int32_t* token_ids, const void* embed_table, int32_t vocab, const void* hidden_src,
                       void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c || !counts) {
         set_error("cache or counts is NULL");
         return KVR_EINVAL;
@@ -742,6 +761,7 @@ kvr_status kvr_select(kvr_cache* c, const int32_t* positions, const int32_t* cou
 kvr_status kvr_reselect(kvr_cache* c, const int32_t* positions, const int32_t* counts, const void* carry_rows,
                         const void* fill_rows, void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out,
                         void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c || !counts) {
         set_error("cache or counts is NULL");
         return KVR_EINVAL;
@@ -766,6 +786,7 @@ kvr_status kvr_refresh_interval_wise(kvr_cache* c, const int32_t* positions, con
                                      int32_t vocab, const void* hidden_src, const kvr_layer_weights* w,
                                      int32_t layer_begin, int32_t layer_end, void* hidden_out, void* workspace,
                                      size_t ws_bytes, uint32_t flags, int32_t* n_intervals_out, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c || !counts || (!positions && counts)) {
         set_error("cache, positions or counts is NULL");
         return KVR_EINVAL;
@@ -831,6 +852,7 @@ kvr_status kvr_refresh_interval_wise(kvr_cache* c, const int32_t* positions, con
 kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, int32_t row_begin,
                           int32_t row_count, const void* a, const void* b, int32_t rank, float scale, int32_t dtype,
                           void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!w || !w_out || !a || !b || n_out < 1 || K < 1 || rank < 1 || row_begin < 0 || row_count < 0 ||
         row_begin + row_count > n_out || (dtype != KVR_BF16 && dtype != KVR_F32)) {
         set_error("lora merge: bad arguments");
@@ -843,6 +865,7 @@ kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, 
 }
 
 kvr_status kvr_shift(kvr_cache* c, int32_t start, int32_t d, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c) {
         set_error("cache is NULL");
         return KVR_EINVAL;
@@ -877,6 +900,7 @@ kvr_status kvr_shift(kvr_cache* c, int32_t start, int32_t d, void* stream) {
 
 kvr_status kvr_splice(kvr_cache* c, int32_t seq, int32_t dst_pos, int32_t n, const void* k_src,
                       const void* v_src, int32_t src_pos, uint32_t flags, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c) {
         set_error("cache is NULL");
         return KVR_EINVAL;
@@ -939,6 +963,7 @@ size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
 
 kvr_status kvr_refresh_layer(kvr_cache* c, int32_t layer, const kvr_layer_weights* w, void* hidden_inout,
                              void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     WsLayout L;
     kvr_status st = check_refresh_args(c, hidden_inout, workspace, ws_bytes, &L);
     if (st != KVR_OK) return st;
@@ -958,6 +983,7 @@ kvr_status kvr_refresh_layer(kvr_cache* c, int32_t layer, const kvr_layer_weight
 
 kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_begin, int32_t layer_end,
                        void* hidden_inout, void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     WsLayout L;
     kvr_status st = check_refresh_args(c, hidden_inout, workspace, ws_bytes, &L);
     if (st != KVR_OK) return st;
@@ -985,6 +1011,7 @@ kvr_status kvr_refresh(kvr_cache* c, const kvr_layer_weights* w, int32_t layer_b
 
 kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, void* workspace, size_t ws_bytes,
                       void* stream) {
+    pdl_begin_call();   // no overlap with work enqueued before this call
     if (!c) {
         set_error("cache is NULL");
         return KVR_EINVAL;

@@ -28,6 +28,8 @@ __device__ __forceinline__ void stf(float* p, float v) { *p = v; }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnLaunch a) {
     extern __shared__ float sm[];
+    pdl_trigger();
+    pdl_wait();
     const int dh = a.head_dim, G = a.n_q_heads / a.n_kv_heads;
     const int tile = blockIdx.x, kvh = blockIdx.y;
     const int* plan = a.plan + 8 * tile;
@@ -147,8 +149,8 @@ cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_simt_kernel<float><<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    KVR_LAUNCH(attn_simt_kernel<float>, grid, dim3(kThreads), smem, s, a);
+    return cudaSuccess;
 }
 
 }  // namespace kvr

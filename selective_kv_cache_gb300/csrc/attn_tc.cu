@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_total = min(plan[5], jb + a.chunk) - jb;   // tiles handled here
     if (n_split > 1 && n_total <= 0) {
         // nothing to read: an empty partial for the merge, and no set-up at all
+        pdl_trigger();
+        pdl_wait();
         if (threadIdx.x < 128) {
             const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
             a.part_ml[(slot * 128 + threadIdx.x) * 2] = -INFINITY;
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
 
+    pdl_wait();   // Q rows and the cache rows written by the previous kernel
     // rows of this thread (softmax warps): m = 32 * (warp % 4) + lane
     const int m = 32 * (warp & 3) + lane;
     const int p = m / G, gi = m % G;
@@ -169,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // dependents may start only once this CTA holds its tensor memory
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -431,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge the split partials of one (query tile, K/V head): one warp per MMA
 // row, 4 output dimensions per lane.  Splits that saw no key are skipped.
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnLaunch a, int n_tiles, int n_split) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int rows_total = n_tiles * a.n_kv_heads * 128;
     if (warp >= rows_total) return;
@@ -501,12 +508,12 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         attr = true;
     }
     dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, b);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || n_split == 1) return e;
+    KVR_LAUNCH(attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, b);
+    if (n_split == 1) return cudaSuccess;
     const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
-    attn_combine_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(b, a.n_tiles, n_split);
-    return cudaGetLastError();
+    KVR_LAUNCH(attn_combine_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, s, b, a.n_tiles,
+               n_split);
+    return cudaSuccess;
 }
 
 }  // namespace kvr

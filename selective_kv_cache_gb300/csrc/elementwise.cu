@@ -68,6 +68,8 @@ __device__ __forceinline__ void sum_parts8(const float* part, size_t split_strid
 template <typename T, typename Tin>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const Tin* __restrict__ in, const T* __restrict__ w,
                                                       T* __restrict__ out, int d, float eps) {
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     const Tin* x = in + (size_t)r * d;
     float ss = 0.f;
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const Tin* __restrict__ in
 // one thread per (row, head, 8-pair chunk of the first half of head_dim)
 template <typename T>
 __global__ void epi_qkv_kernel(QkvEpi a) {
+    pdl_trigger();
+    pdl_wait();
     const int dh = a.head_dim, half = dh / 2, chunks = half / 8;
     const int heads = a.n_q_heads + 2 * a.n_kv_heads;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -153,6 +157,8 @@ __global__ void epi_qkv_kernel(QkvEpi a) {
 template <typename T>
 __global__ void epi_residual_kernel(const float* __restrict__ part, int splits, int R, int d, const T* __restrict__ x,
                                     float* __restrict__ h) {
+    pdl_trigger();
+    pdl_wait();
     const long long i8 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i8 >= (long long)R * d) return;
     float v[8], xv[8];
@@ -165,6 +171,8 @@ __global__ void epi_residual_kernel(const float* __restrict__ part, int splits, 
 
 template <typename T>
 __global__ void epi_swiglu_kernel(const float* __restrict__ part, int splits, int R, int F, T* __restrict__ act) {
+    pdl_trigger();
+    pdl_wait();
     const long long i8 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i8 >= (long long)R * F) return;
     const int r = (int)(i8 / F), f = (int)(i8 % F);
@@ -180,6 +188,8 @@ __global__ void epi_swiglu_kernel(const float* __restrict__ part, int splits, in
 template <typename T>
 __global__ void epi_down_kernel(const float* __restrict__ part, int splits, int R, int d, const float* __restrict__ h,
                                 T* __restrict__ x) {
+    pdl_trigger();
+    pdl_wait();
     const long long i8 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i8 >= (long long)R * d) return;
     float v[8], hv[8];
@@ -217,6 +227,8 @@ __global__ void __launch_bounds__(kRowThreads) epi_residual_norm_kernel(const fl
                                                                         int R, int d, const T* __restrict__ x,
                                                                         float* __restrict__ h, const T* __restrict__ w,
                                                                         T* __restrict__ hn, float eps) {
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     float v[kRowChunks][8];
     float ss = 0.f;
@@ -256,6 +268,8 @@ __global__ void __launch_bounds__(kRowThreads) epi_down_norm_kernel(const float*
                                                                     int d, const float* __restrict__ h,
                                                                     T* __restrict__ x, const T* __restrict__ w_next,
                                                                     T* __restrict__ xn, float eps) {
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     float v[kRowChunks][8];
     float ss = 0.f;
@@ -297,13 +311,13 @@ cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w,
     if (rows <= 0) return cudaSuccess;
     if (dtype == KVR_BF16) {
         if (in_f32)
-            rmsnorm_kernel<__nv_bfloat16, float><<<rows, 256, 0, s>>>((const float*)in, (const __nv_bfloat16*)w,
+            KVR_LAUNCH(rmsnorm_kernel<__nv_bfloat16, float>, dim3(rows), dim3(256), 0, s, (const float*)in, (const __nv_bfloat16*)w,
                                                                       (__nv_bfloat16*)out, d, eps);
         else
-            rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, s>>>(
+            KVR_LAUNCH(rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s,
                 (const __nv_bfloat16*)in, (const __nv_bfloat16*)w, (__nv_bfloat16*)out, d, eps);
     } else {
-        rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>((const float*)in, (const float*)w, (float*)out, d, eps);
+        KVR_LAUNCH(rmsnorm_kernel<float, float>, dim3(rows), dim3(256), 0, s, (const float*)in, (const float*)w, (float*)out, d, eps);
     }
     return cudaGetLastError();
 }
@@ -312,9 +326,9 @@ cudaError_t launch_epi_qkv(int dtype, const QkvEpi& a, cudaStream_t s) {
     const long long total = (long long)a.R * (a.n_q_heads + 2 * a.n_kv_heads) * (a.head_dim / 16);
     if (total <= 0) return cudaSuccess;
     if (dtype == KVR_BF16)
-        epi_qkv_kernel<__nv_bfloat16><<<blocks_for(total, 256), 256, 0, s>>>(a);
+        KVR_LAUNCH(epi_qkv_kernel<__nv_bfloat16>, dim3(blocks_for(total, 256)), dim3(256), 0, s, a);
     else
-        epi_qkv_kernel<float><<<blocks_for(total, 256), 256, 0, s>>>(a);
+        KVR_LAUNCH(epi_qkv_kernel<float>, dim3(blocks_for(total, 256)), dim3(256), 0, s, a);
     return cudaGetLastError();
 }
 
@@ -323,10 +337,10 @@ cudaError_t launch_epi_residual_f32(int dtype, const float* part, int splits, in
     const long long n = (long long)R * d / 8;
     if (n <= 0) return cudaSuccess;
     if (dtype == KVR_BF16)
-        epi_residual_kernel<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, d,
+        KVR_LAUNCH(epi_residual_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d,
                                                                               (const __nv_bfloat16*)x, h_out);
     else
-        epi_residual_kernel<float><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, d, (const float*)x, h_out);
+        KVR_LAUNCH(epi_residual_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d, (const float*)x, h_out);
     return cudaGetLastError();
 }
 
@@ -334,10 +348,10 @@ cudaError_t launch_epi_swiglu(int dtype, const float* part, int splits, int R, i
     const long long n = (long long)R * F / 8;
     if (n <= 0) return cudaSuccess;
     if (dtype == KVR_BF16)
-        epi_swiglu_kernel<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, F,
+        KVR_LAUNCH(epi_swiglu_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, F,
                                                                             (__nv_bfloat16*)act_out);
     else
-        epi_swiglu_kernel<float><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, F, (float*)act_out);
+        KVR_LAUNCH(epi_swiglu_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, F, (float*)act_out);
     return cudaGetLastError();
 }
 
@@ -346,10 +360,10 @@ cudaError_t launch_epi_down(int dtype, const float* part, int splits, int R, int
     const long long n = (long long)R * d / 8;
     if (n <= 0) return cudaSuccess;
     if (dtype == KVR_BF16)
-        epi_down_kernel<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, d, h,
+        KVR_LAUNCH(epi_down_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d, h,
                                                                           (__nv_bfloat16*)x_out);
     else
-        epi_down_kernel<float><<<blocks_for(n, 256), 256, 0, s>>>(part, splits, R, d, h, (float*)x_out);
+        KVR_LAUNCH(epi_down_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d, h, (float*)x_out);
     return cudaGetLastError();
 }
 
@@ -358,10 +372,10 @@ cudaError_t launch_epi_residual_norm(int dtype, const float* part, int splits, i
     if (R <= 0) return cudaSuccess;
     if (d > kRowThreads * kRowChunks * 8) return cudaErrorInvalidValue;
     if (dtype == KVR_BF16)
-        epi_residual_norm_kernel<__nv_bfloat16><<<R, kRowThreads, 0, s>>>(
+        KVR_LAUNCH(epi_residual_norm_kernel<__nv_bfloat16>, dim3(R), dim3(kRowThreads), 0, s,
             part, splits, R, d, (const __nv_bfloat16*)x, h, (const __nv_bfloat16*)w, (__nv_bfloat16*)hn, eps);
     else
-        epi_residual_norm_kernel<float><<<R, kRowThreads, 0, s>>>(part, splits, R, d, (const float*)x, h,
+        KVR_LAUNCH(epi_residual_norm_kernel<float>, dim3(R), dim3(kRowThreads), 0, s, part, splits, R, d, (const float*)x, h,
                                                                   (const float*)w, (float*)hn, eps);
     return cudaGetLastError();
 }
@@ -371,10 +385,10 @@ cudaError_t launch_epi_down_norm(int dtype, const float* part, int splits, int R
     if (R <= 0) return cudaSuccess;
     if (d > kRowThreads * kRowChunks * 8) return cudaErrorInvalidValue;
     if (dtype == KVR_BF16)
-        epi_down_norm_kernel<__nv_bfloat16><<<R, kRowThreads, 0, s>>>(
+        KVR_LAUNCH(epi_down_norm_kernel<__nv_bfloat16>, dim3(R), dim3(kRowThreads), 0, s,
             part, splits, R, d, h, (__nv_bfloat16*)x, (const __nv_bfloat16*)w_next, (__nv_bfloat16*)xn, eps);
     else
-        epi_down_norm_kernel<float><<<R, kRowThreads, 0, s>>>(part, splits, R, d, h, (float*)x,
+        KVR_LAUNCH(epi_down_norm_kernel<float>, dim3(R), dim3(kRowThreads), 0, s, part, splits, R, d, h, (float*)x,
                                                               (const float*)w_next, (float*)xn, eps);
     return cudaGetLastError();
 }

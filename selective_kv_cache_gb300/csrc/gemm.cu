@@ -114,32 +114,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // dependents may start only once this CTA holds its tensor memory, so a
+    // waiting dependent can never keep it from allocating
+    pdl_trigger();
+    if (warp >= 2) pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            auto load_a = [&](int s, int kb, int m_t) {
+                for (int a = 0; a < atoms; ++a) {
+                    const int kx = (kb * atoms + a) * kBK;
+                    uint8_t* da = sA + (size_t)s * stA + a * kTileABytes;
+                    if (g.swiglu_F) {   // gate rows f0..f0+63, then up rows F+f0..
+                        tma_load_2d(da, &tmA, &full[s], kx, m_t * 64);
+                        tma_load_2d(da + kTileABytes / 2, &tmA, &full[s], kx, g.swiglu_F + m_t * 64);
+                    } else {
+                        tma_load_2d(da, &tmA, &full[s], kx, m_t * 128);
+                    }
+                }
+            };
+            // The weights are written by no kernel of the call: the weight tiles
+            // of the first ring stages go out before the wait for the previous
+            // kernel, whose outputs (the activation rows) are read after it.
+            int pre = 0;
+            for (int item = blockIdx.x; item < g.items && pre < stages; item += gridDim.x) {
+                int m_t, n_t, split, kb0, kb1;
+                item_coords(g, item, m_t, n_t, split, kb0, kb1);
+                for (int kb = kb0; kb < kb1 && pre < stages; ++kb, ++pre) {
+                    mbar_arrive_expect_tx(&full[pre], (uint32_t)(stA + stB));
+                    load_a(pre, kb, m_t);
+                }
+            }
+            pdl_wait();
             int it = 0;
             for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
                 int m_t, n_t, split, kb0, kb1;
                 item_coords(g, item, m_t, n_t, split, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % stages;
-                    if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(stA + stB));
-                    for (int a = 0; a < atoms; ++a) {
-                        const int kx = (kb * atoms + a) * kBK;
-                        uint8_t* da = sA + (size_t)s * stA + a * kTileABytes;
-                        if (g.swiglu_F) {   // gate rows f0..f0+63, then up rows F+f0..
-                            tma_load_2d(da, &tmA, &full[s], kx, m_t * 64);
-                            tma_load_2d(da + kTileABytes / 2, &tmA, &full[s], kx, g.swiglu_F + m_t * 64);
-                        } else {
-                            tma_load_2d(da, &tmA, &full[s], kx, m_t * 128);
+                    if (it >= pre) {
+                        if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
                         }
-                        tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], kx, n_t * BN);
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(stA + stB));
+                        load_a(s, kb, m_t);
                     }
+                    for (int a = 0; a < atoms; ++a)
+                        tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], (kb * atoms + a) * kBK, n_t * BN);
                 }
             }
             if (!ok) {  // let every copy still in flight land before the CTA exits
@@ -266,6 +289,8 @@ __global__ void __launch_bounds__(256) gemm_f32_simt_kernel(const float* __restr
                                                             int splits) {
     __shared__ float xs[16][64 + 4];
     __shared__ float ws[16][64 + 4];
+    pdl_trigger();
+    pdl_wait();
     const int f0 = blockIdx.x * 64, r0 = blockIdx.y * 64, split = blockIdx.z;
     const int k0 = (int)((long long)split * (K / 16) / splits) * 16;
     const int k1 = (int)((long long)(split + 1) * (K / 16) / splits) * 16;
@@ -365,9 +390,9 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     if (p.R <= 0) return cudaSuccess;
     if (dtype == KVR_F32) {
         dim3 grid(p.m_tiles, p.n_tiles, p.splits);
-        gemm_f32_simt_kernel<<<grid, 256, 0, s>>>((const float*)w, (const float*)x, part, p.n_out, p.K, p.R,
-                                                   p.splits);
-        return cudaGetLastError();
+        KVR_LAUNCH(gemm_f32_simt_kernel, grid, dim3(256), 0, s, (const float*)w, (const float*)x, part, p.n_out, p.K,
+                   p.R, p.splits);
+        return cudaSuccess;
     }
     CUtensorMap ta, tb;
     if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, p.swiglu_F ? 64 : 128,
@@ -407,8 +432,8 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         attr_set = true;
     }
     const unsigned grid = (unsigned)std::min(g.items, kNumSMs);
-    gemm_bf16_tc_kernel<<<grid, kGemmThreads, smem, s>>>(ta, tb, g);
-    return cudaGetLastError();
+    KVR_LAUNCH(gemm_bf16_tc_kernel, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+    return cudaSuccess;
 }
 
 }  // namespace kvr

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/kvr.h"
@@ -215,6 +216,50 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
 // kAttnMaxSplitCTAs CTAs' worth.
 constexpr int kAttnMaxSplitCTAs = 4 * kNumSMs;
 size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_heads);
+
+// ---------------------------------------------------------------- dependent launch
+// Kernels of one library call run back to back on one stream.  Each kernel
+// signals at entry that the next one may be scheduled, and the next one does
+// its set-up (barriers, tensor memory, descriptor prefetch, and for the
+// projections the first weight tiles, which no kernel writes) before
+// griddepcontrol.wait, which returns once the previous grid has completed and
+// its writes are visible.  Every access to data another kernel of the call
+// produces or consumes comes after that wait.  The first kernel of each call
+// is launched with plain stream order, so nothing overlaps work the caller
+// enqueued before the call.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
+// Host side: whether the next launch may overlap the previous kernel of the
+// same call (false for a call's first launch; set by pdl_begin_call()).
+void pdl_begin_call();
+bool pdl_take();   // returns the current permission and grants it to later launches
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (pdl_take()) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#define KVR_LAUNCH(...)                                     \
+    do {                                                    \
+        cudaError_t e_ = ::kvr::launch_kernel(__VA_ARGS__); \
+        if (e_ != cudaSuccess) return e_;                   \
+    } while (0)
 
 }  // namespace kvr
 
