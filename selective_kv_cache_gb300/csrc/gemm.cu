@@ -39,6 +39,11 @@ struct GemmDev {
     __nv_bfloat16* act;
 };
 
+// one lane polls, the whole warp follows with the result
+__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
+
 // all four epilogue warps (128 threads) on named barrier 2; returns the AND of pred
 __device__ __forceinline__ bool epi_bar_and(bool pred) {
     uint32_t r;
@@ -172,43 +177,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, BN, 0, 0);
-            int it = 0, local = 0;
-            for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x, ++local) {
-                int m_t, n_t, split, kb0, kb1;
-                item_coords(g, item, m_t, n_t, split, kb0, kb1);
-                const int ab = local & 1;
-                if (!mbar_wait(&acc_empty[ab], ((uint32_t)(local >> 1) & 1u) ^ 1u)) {
+        // The whole warp walks the loop (every value warp-uniform); one elected
+        // lane issues.  Descriptors are formed once and advanced by adding the
+        // byte offset >> 4 to the start-address field.
+        const uint32_t idesc = idesc_bf16(128, BN, 0, 0);
+        const uint64_t descA = sdesc_sw128(smem_u32(sA), 16, 1024);
+        const uint64_t descB = sdesc_sw128(smem_u32(sB), 16, 1024);
+        int it = 0, local = 0;
+        for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x, ++local) {
+            int m_t, n_t, split, kb0, kb1;
+            item_coords(g, item, m_t, n_t, split, kb0, kb1);
+            const int ab = local & 1;
+            if (!warp_wait_all(&acc_empty[ab], ((uint32_t)(local >> 1) & 1u) ^ 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)ab * acc_stride;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % stages;
+                if (!warp_wait_all(&full[s], (uint32_t)(it / stages) & 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)ab * acc_stride;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = it % stages;
-                    if (!mbar_wait(&full[s], (uint32_t)(it / stages) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int a = 0; a < atoms; ++a) {
-                        const uint32_t a0 = smem_u32(sA + (size_t)s * stA + a * kTileABytes);
-                        const uint32_t b0 = smem_u32(sB + (size_t)s * stB + a * tileB);
+                for (int a = 0; a < atoms; ++a) {
+                    const uint64_t da = descA + (uint64_t)(((uint32_t)s * stA + (uint32_t)a * kTileABytes) >> 4);
+                    const uint64_t db = descB + (uint64_t)(((uint32_t)s * stB + (uint32_t)a * tileB) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            mma_bf16(d, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
-                                     idesc, (kb > kb0 || a > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(&empty[s]);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_elect(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || a > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (!ok) break;
-                mma_commit(&acc_full[ab]);
+                mma_commit_elect(&empty[s]);
             }
-            mma_commit(mma_done);
-            mbar_wait(mma_done, 0);
+            if (!ok) break;
+            mma_commit_elect(&acc_full[ab]);
         }
+        mma_commit_elect(mma_done);
+        warp_wait_all(mma_done, 0);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
