@@ -327,6 +327,71 @@ kvr_status kvr_shift(kvr_cache* c, int32_t start, int32_t d, void* stream);
 kvr_status kvr_splice(kvr_cache* c, int32_t seq, int32_t dst_pos, int32_t n, const void* k_src,
                       const void* v_src, int32_t src_pos, uint32_t flags, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Layer-range policy of "CacheReforge: Bounded Recovery for Stale KV Caches
+ * under Evolving Adapters" (Methodology: Layerwise Risk; Runtime risk and
+ * range selection; Cache and anchor updates).  The adapter is one flat
+ * parameter vector theta (n_params elements in device memory, the caller
+ * packs its LoRA matrices into it).  Every cached layer keeps its own anchor,
+ * the theta that produced its K/V, and a version number.
+ * ------------------------------------------------------------------------- */
+typedef struct kvr_policy kvr_policy;
+
+/* updated module, for the restart layer r_KV(m, s) */
+enum { KVR_MOD_Q = 0, KVR_MOD_K, KVR_MOD_V, KVR_MOD_O, KVR_MOD_MLP };
+
+/* r_KV(m, s) (CacheReforge, supplementary Eq. S4): the first cache layer an
+ * update of module m at layer s can change: s for K or V, min(s + 1, N) for
+ * Q, O or the MLP; N (= n_layers) means no cached layer changes.
+ * Returns -1 for an unknown module or s outside [0, n_layers). */
+int32_t kvr_restart_layer(int32_t module, int32_t s, int32_t n_layers);
+
+/* Layer sensitivities from a calibration split (CacheReforge, Eqs. 6-7), on
+ * the host.  Condition i has restart layer restart[i], first safe window
+ * window[i] (layers recomputed from restart[i]; 0 = direct reuse) and adapter
+ * distance drift[i].  Layer l is labelled for i when
+ * restart[i] <= l < restart[i] + window[i]; with D_l the labelled distances
+ * (n_l of them, ascending), delta_l = max(D_l[floor(0.05 n_l)], 1e-12) and
+ * s_l = 1 / delta_l, or 0 when D_l is empty.  s_out: host [n_layers].
+ * EINVAL on NULL arrays, n_layers < 1, n_cond < 0, a negative window or
+ * drift, or a restart outside [0, n_layers). */
+kvr_status kvr_policy_sensitivity(int32_t n_layers, int32_t n_cond, const int32_t* restart,
+                                  const int32_t* window, const double* drift, double* s_out);
+
+/* Create a policy for n_layers cached layers.  theta0: device [n_params] in
+ * `dtype` (KVR_F32 or KVR_BF16), the adapter that produced every layer's
+ * cache (version 0); it is copied into each layer's anchor, which the policy
+ * owns (n_layers * n_params elements of device memory).  sensitivity: host
+ * [n_layers], s_l >= 0, copied.  Synchronous on `stream`. */
+kvr_status kvr_policy_create(int32_t n_layers, int64_t n_params, int32_t dtype, const void* theta0,
+                             const double* sensitivity, void* stream, kvr_policy** out);
+kvr_status kvr_policy_destroy(kvr_policy* p);
+
+/* Runtime risk and range (CacheReforge, Eqs. 8-9), synchronous:
+ *   d_l = ||theta_t - anchor_l||_2 on the GPU (differences and squares in
+ *   double, a fixed reduction order, so the result is deterministic);
+ *   q_l = s_l * d_l; layer l triggers when q_l >= 1;
+ *   b_t = 1 + max{l : q_l >= 1}.
+ * The update is to module `module` at layer `update_layer` (the executable
+ * restart r = update_layer).  The recovery range is [r, b_t).  It is empty
+ * (range_out = {r, r}) when no layer triggers or when b_t <= r_KV(module,
+ * update_layer): such a range replaces no affected K/V, which is reuse.
+ *   theta_t: device [n_params], the policy's dtype.  drift_out, risk_out:
+ *   host [n_layers], nullable.  range_out: host int32[2].
+ * EINVAL on NULL theta_t/range_out or a bad module/layer. */
+kvr_status kvr_policy_plan(kvr_policy* p, const void* theta_t, int32_t module, int32_t update_layer,
+                           double* drift_out, double* risk_out, int32_t* range_out, void* stream);
+
+/* Cache and anchor updates (CacheReforge): after layers [begin, end) were
+ * recomputed under theta_t, their anchors become theta_t and their version
+ * `version`; other layers keep their older anchors.  Enqueued on `stream`
+ * (device copies); an empty range does nothing. */
+kvr_status kvr_policy_commit(kvr_policy* p, const void* theta_t, int32_t begin, int32_t end, int64_t version,
+                             void* stream);
+
+/* Per-layer versions (host [n_layers]); synchronous. */
+kvr_status kvr_policy_versions(kvr_policy* p, int64_t* versions);
+
 /* Synchronise `stream` and report device-side failures recorded since the
  * last call (ETIMEOUT / EDEVICE), clearing them. */
 kvr_status kvr_sync_status(kvr_cache* c, void* stream);

@@ -30,6 +30,18 @@ def merge_lora(layers, shape, stream=None):
     return out
 
 
+def pack_adapter(layers):
+    """The adapter as one flat parameter vector theta: every layer's a_q, b_q,
+    a_v, b_v flattened and concatenated in layer order (the layout the
+    layer-range policy takes)."""
+    parts = []
+    for L in layers:
+        for k in ("a_q", "b_q", "a_v", "b_v"):
+            if L.get(k) is not None:
+                parts.append(L[k].reshape(-1))
+    return torch.cat(parts)
+
+
 class Setup:
     """One workload bound to a libkvr cache on the current CUDA device.
 

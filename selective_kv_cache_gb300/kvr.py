@@ -27,6 +27,7 @@ KVR_SINK_STATIC = 0x1
 KVR_COMMIT_META = 0x1
 KVR_SPLICE_LOCAL = 0x1
 KVR_SPLICE_SINK = 0x2
+KVR_MOD_Q, KVR_MOD_K, KVR_MOD_V, KVR_MOD_O, KVR_MOD_MLP = range(5)
 KERNELS = ["select", "gather", "rmsnorm", "gemm_qkv", "epi_qkv", "attention", "gemm_o", "epi_o",
            "gemm_gate_up", "epi_gate_up", "gemm_down", "epi_down", "commit"]
 KVR_K_COUNT = len(KERNELS)
@@ -35,7 +36,8 @@ EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace
            "kvr_refresh_layer", "kvr_refresh", "kvr_attend", "kvr_sync_status", "kvr_last_error",
            "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read",
            "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge",
-           "kvr_shift", "kvr_splice", "kvr_cache_info"]
+           "kvr_shift", "kvr_splice", "kvr_cache_info", "kvr_restart_layer", "kvr_policy_sensitivity",
+           "kvr_policy_create", "kvr_policy_destroy", "kvr_policy_plan", "kvr_policy_commit", "kvr_policy_versions"]
 
 
 class kvr_model_desc(C.Structure):
@@ -73,16 +75,24 @@ lib.kvr_lora_merge.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, C.c_float, I
 lib.kvr_shift.argtypes = [P, I32, I32, P]
 lib.kvr_splice.argtypes = [P, I32, I32, I32, P, P, I32, C.c_uint32, P]
 lib.kvr_cache_info.argtypes = [P, P, P]
+lib.kvr_restart_layer.argtypes = [I32, I32, I32]
+lib.kvr_policy_sensitivity.argtypes = [I32, I32, P, P, P, P]
+lib.kvr_policy_create.argtypes = [I32, C.c_int64, I32, P, P, P, C.POINTER(P)]
+lib.kvr_policy_destroy.argtypes = [P]
+lib.kvr_policy_plan.argtypes = [P, P, I32, I32, P, P, P, P]
+lib.kvr_policy_commit.argtypes = [P, P, I32, I32, C.c_int64, P]
+lib.kvr_policy_versions.argtypes = [P, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
 lib.kvr_last_error.restype = C.c_char_p
+lib.kvr_restart_layer.restype = C.c_int32
 lib.kvr_read_selection.argtypes = [P, I32, P, I32, P, I32, P, P, P, P, I32, P, P, P]
 lib.kvr_read_meta.argtypes = [P, P, P]
 lib.kvr_profile_enable.argtypes = [P, I32]
 lib.kvr_profile_read.argtypes = [P, P, P, I32]
 for _f in EXPORTS:
-    if _f not in ("kvr_workspace_bytes", "kvr_last_error"):
+    if _f not in ("kvr_workspace_bytes", "kvr_last_error", "kvr_restart_layer"):
         getattr(lib, _f).restype = C.c_int
 
 
@@ -275,3 +285,55 @@ def kvr_profile_read(c: int):
     n = (C.c_int64 * KVR_K_COUNT)()
     _check(lib.kvr_profile_read(c, ms, n, KVR_K_COUNT), "kvr_profile_read")
     return {KERNELS[i]: (int(n[i]), float(ms[i])) for i in range(KVR_K_COUNT)}
+
+# ---------------------------------------------------------------- layer-range policy
+def kvr_restart_layer(module: int, s: int, n_layers: int) -> int:
+    return int(lib.kvr_restart_layer(module, s, n_layers))
+
+
+def kvr_policy_sensitivity(n_layers: int, restart, window, drift):
+    import numpy as np
+    r = np.ascontiguousarray(restart, dtype=np.int32)
+    w = np.ascontiguousarray(window, dtype=np.int32)
+    d = np.ascontiguousarray(drift, dtype=np.float64)
+    out = np.zeros(n_layers, np.float64)
+    _check(lib.kvr_policy_sensitivity(n_layers, len(r), r.ctypes.data, w.ctypes.data, d.ctypes.data,
+                                      out.ctypes.data), "kvr_policy_sensitivity")
+    return out
+
+
+def kvr_policy_create(n_layers: int, theta0, sensitivity, stream=None) -> int:
+    """theta0: flat device tensor (bf16 or fp32); sensitivity: n_layers floats."""
+    import numpy as np
+    s = np.ascontiguousarray(sensitivity, dtype=np.float64)
+    out = P()
+    dt = KVR_BF16 if theta0.dtype == torch.bfloat16 else KVR_F32
+    _check(lib.kvr_policy_create(n_layers, theta0.numel(), dt, _ptr(theta0), s.ctypes.data, _stream(stream),
+                                 C.byref(out)), "kvr_policy_create")
+    return out.value
+
+
+def kvr_policy_destroy(p: int):
+    _check(lib.kvr_policy_destroy(p), "kvr_policy_destroy")
+
+
+def kvr_policy_plan(p: int, n_layers: int, theta_t, module: int, update_layer: int, stream=None):
+    """Returns (drift [n_layers], risk [n_layers], (begin, end))."""
+    import numpy as np
+    d = np.zeros(n_layers, np.float64)
+    q = np.zeros(n_layers, np.float64)
+    rng = np.zeros(2, np.int32)
+    _check(lib.kvr_policy_plan(p, _ptr(theta_t), module, update_layer, d.ctypes.data, q.ctypes.data,
+                               rng.ctypes.data, _stream(stream)), "kvr_policy_plan")
+    return d, q, (int(rng[0]), int(rng[1]))
+
+
+def kvr_policy_commit(p: int, theta_t, begin: int, end: int, version: int, stream=None):
+    _check(lib.kvr_policy_commit(p, _ptr(theta_t), begin, end, version, _stream(stream)), "kvr_policy_commit")
+
+
+def kvr_policy_versions(p: int, n_layers: int):
+    import numpy as np
+    v = np.zeros(n_layers, np.int64)
+    _check(lib.kvr_policy_versions(p, v.ctypes.data), "kvr_policy_versions")
+    return v

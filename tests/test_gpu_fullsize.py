@@ -20,7 +20,7 @@ from selective_kv_cache_gb300 import workloads as wl
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 kvr = pytest.importorskip("selective_kv_cache_gb300.kvr")
-from selective_kv_cache_gb300.harness import Setup, merge_lora  # noqa: E402
+from selective_kv_cache_gb300.harness import Setup, merge_lora, pack_adapter  # noqa: E402
 from helpers import TOL, LazyWeights, assert_close, f64, oracle_spec  # noqa: E402
 
 
@@ -106,11 +106,28 @@ def test_block_seam_full_size(sink_static):
 
 
 def test_adapter_drift_full_size():
-    """Batch 4 x 32768, rank-16 LoRA on Q and V merged on the GPU, layers
-    10-14 over the whole 24576-token affected suffix from stored boundary
-    states, 492 isolated positions per sequence in the other layers."""
+    """Batch 4 x 32768, rank-16 LoRA on Q and V merged on the GPU; the
+    layer-range policy picks layers 10-14, which run over the whole
+    24576-token affected suffix from stored boundary states; 492 isolated
+    positions per sequence in the other layers."""
     w = wl.WORKLOADS["qwen1p5b_drift"]
+    m = w.model
     layers = wl.make_layer_weights(w, "cuda", lora="new")
+    # the recovery range comes from the layer-range policy (CacheReforge, Eqs.
+    # 8-9): anchors at the old adapter, synthetic sensitivities calibrated on
+    # windows [10, 15) at distances 0.8-1.0 x the observed drift
+    old = wl.make_layer_weights(w, "cuda", lora="old")
+    theta0, theta1 = pack_adapter(old), pack_adapter(layers)
+    del old
+    d_obs = float((theta1.float() - theta0.float()).norm())
+    cal = np.random.default_rng(3)
+    s_l = kvr.kvr_policy_sensitivity(m.n_layers, [10] * 40, [5] * 40, d_obs * cal.uniform(0.8, 1.0, 40))
+    pol = kvr.kvr_policy_create(m.n_layers, theta0, s_l)
+    _, q, (r0, r1) = kvr.kvr_policy_plan(pol, m.n_layers, theta1, kvr.KVR_MOD_V, 10)
+    assert (r0, r1) == w.range_layers and np.all(q[10:15] >= 1.0) and np.all(q[15:] == 0.0)
+    kvr.kvr_policy_commit(pol, theta1, r0, r1, 1)
+    assert kvr.kvr_policy_plan(pol, m.n_layers, theta1, kvr.KVR_MOD_V, 10)[2] == (10, 10)   # now current: reuse
+    kvr.kvr_policy_destroy(pol)
     merged = merge_lora(layers, w.model)
     for L in layers:        # the base projections are no longer needed on the device
         L["w_qkv"] = None
@@ -121,7 +138,6 @@ def test_adapter_drift_full_size():
     boundary = torch.empty((w.batch, w.capacity, w.model.d_model), device="cuda", dtype=torch.float32)
     boundary.normal_(0.0, 1.0, generator=g)
     boundary = boundary.to(torch.bfloat16)
-    r0, r1 = w.range_layers
     s.refresh_range(boundary, r0, r1)
     # the oracle runs the merged projection as it is (the merge itself is pinned
     # by the LoRA test); the adapter terms are already inside w_qkv

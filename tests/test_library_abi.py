@@ -58,3 +58,25 @@ def test_host_validation_needs_no_gpu(lib):
     assert kvr.lib.kvr_shift(None, 0, 1, None) == kvr.KVR_EINVAL
     assert kvr.lib.kvr_splice(None, 0, 0, 1, None, None, 0, 0, None) == kvr.KVR_EINVAL
     assert kvr.lib.kvr_cache_info(None, None, None) == kvr.KVR_EINVAL
+
+
+def test_policy_host_logic_needs_no_gpu(lib):
+    """Eq. S4 and the calibration of Eqs. 6-7 run on the host: the library's
+    answers equal the oracle's on random calibration splits."""
+    import numpy as np
+    import oracle.policy as OP
+    from selective_kv_cache_gb300 import kvr
+    for m in range(5):
+        for s_ in (0, 5, 27):
+            assert kvr.kvr_restart_layer(m, s_, 28) == OP.restart_layer(m, s_, 28)
+    assert kvr.kvr_restart_layer(7, 0, 28) == -1 and kvr.kvr_restart_layer(0, 28, 28) == -1
+    rng = np.random.default_rng(8)
+    for _ in range(20):
+        L, n = int(rng.integers(1, 30)), int(rng.integers(0, 60))
+        r = rng.integers(0, L, n)
+        h = rng.integers(0, 10, n)
+        d = rng.random(n) * 3
+        np.testing.assert_array_equal(kvr.kvr_policy_sensitivity(L, r, h, d), OP.sensitivity(L, r, h, d))
+    with pytest.raises(kvr.KvrError):
+        kvr.kvr_policy_sensitivity(3, [5], [1], [0.1])
+    assert kvr.lib.kvr_policy_plan(None, None, 0, 0, None, None, None, None) == kvr.KVR_EINVAL
