@@ -262,10 +262,12 @@ def run_ours(args):
     if not args.no_compare and args.workload == "llama8b":
         cmp = compare_schedules(s, args)
 
-    # ---- Shift of the same edit (the step before the refresh), on its own cache
-    shift = None
+    # ---- Shift of the same edit (the step before the refresh), on its own cache,
+    # and the Semantic-Unit Refresh selection that picks positions for it
+    shift = sur = None
     if args.workload == "llama8b":
         shift = measure_shift(w, hbm)
+        sur = measure_sur(s)
 
     # ---- CPU oracle baseline on a bounded sample (rank 0 only)
     cpu = None
@@ -294,6 +296,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "packed_vs_interval": cmp,
         "shift": shift,
+        "sur_select": sur,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -338,6 +341,48 @@ def measure_shift(w, hbm_peak, reps=10):
                         f"({m.n_layers} L x {m.n_kv_heads} K/V heads x {m.head_dim}, bf16)",
             "us_median": round(us, 1), "bytes": int(nbytes), "achieved_gbs": round(gbs, 1), "peak_gbs": hbm_peak,
             "frac": round(gbs / hbm_peak, 4), "reps": reps}
+
+
+def measure_sur(s, reps=10):
+    """Semantic-Unit Refresh selection for the same edit: the 5632-token
+    retained suffix of the timed workload, a 64-token query, units of 8-128
+    tokens, the 5 % budget; CUDA events around kvr_sur_select.  The scoring
+    contraction is fp32 FFMA (the pages score in fp32): its peak is
+    152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz = 80.5 TFLOP/s."""
+    import numpy as np
+    import torch
+
+    from selective_kv_cache_gb300 import kvr, workloads as wl
+
+    w = s.w
+    S = w.n_tokens - w.suffix_start
+    Q = 64
+    sids = s.ids[0, w.suffix_start:w.n_tokens].contiguous()
+    qids = torch.from_numpy(wl.make_query_ids(w.model.vocab, Q, 21, sids.cpu().numpy(), overlap=4)).cuda()
+    bounds = torch.from_numpy(wl.make_unit_bounds(S, 22)).cuda()
+    ws = torch.empty(kvr.kvr_sur_workspace_bytes(S, Q, w.model.d_model, bounds.numel() - 1), dtype=torch.uint8,
+                     device="cuda")
+    pos = torch.empty(S, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B = kvr.kvr_sur_select(s.embed, sids, qids, bounds, 5, w.suffix_start, ws, pos, stream=stream)
+        e1.record(stream)
+        kvr.kvr_sur_status(ws, stream)
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    us = float(np.median(times)) * 1e3
+    flops = 2.0 * S * Q * w.model.d_model
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    ach = flops / (us * 1e-6) / 1e12
+    return {"workload": f"{S}-token suffix, {Q}-token query, {bounds.numel() - 1} units of 8-128 tokens, "
+                        f"{w.model.vocab} x {w.model.d_model} bf16 embeddings, 5 % budget ({B} positions)",
+            "us_median": round(us, 1), "bound": "fp32 FFMA", "achieved_tflops": round(ach, 2),
+            "peak_tflops": round(peak, 1), "peak_source": "derived: 152 SMs x 128 lanes x 2 x 2.07 GHz",
+            "frac": round(ach / peak, 4)}
 
 
 def compare_schedules(s1, args):

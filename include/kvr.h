@@ -328,6 +328,51 @@ kvr_status kvr_splice(kvr_cache* c, int32_t seq, int32_t dst_pos, int32_t n, con
                       const void* v_src, int32_t src_pos, uint32_t flags, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvr_sur_select -- Semantic-Unit Refresh selection ("Budgeted KV-Cache
+ * Repair for Evolving Contexts", Sec. 3.2 and Sec. 7.3, Eqs. 1/7 and 8).
+ *   Token scores: r_i = max_j cos(E[s_i], E[q_j]) + 0.25 * 1[s_i in q], in
+ *   fp32 (a zero-norm embedding row scores cosine 0; a token that occurs in
+ *   the query meets its own embedding, cosine exactly 1, and scores exactly
+ *   1.25, so the tie rule below is not decided by rounding).
+ *   Unit score: the mean of the unit's four largest token scores (all of
+ *   them when it has fewer than four).  Units are ranked by score, earlier
+ *   start first on ties, and admitted whole in that order while they fit the
+ *   allowance B = min(S, ceil(S * b / 100)) (Eq. 3).  The first unit that
+ *   does not fit the remaining w positions contributes the width-w window
+ *   that maximises the sum of the forward envelope
+ *   u_t = max(exp(r_t - r_max), exp(-1/16) u_{t-1}), u_0 = 0 (t runs over the
+ *   unit's tokens in order, r_max is the unit's largest score; the earliest
+ *   window wins ties), and selection stops.  The envelope and the window
+ *   sums are formed in double.
+ *   embed       device [vocab][d] (dtype KVR_F32 or KVR_BF16).
+ *   suffix_ids  device int32 [S]: token ids of the retained suffix, whose
+ *               first token sits at global position suffix_start.
+ *   query_ids   device int32 [Q], Q >= 1.
+ *   unit_bounds device int32 [n_units + 1]: 0 = b_0 < b_1 < ... < b_n = S;
+ *               unit k is suffix tokens [b_k, b_{k+1}).  Segmenting text into
+ *               units happens before this call.
+ *   workspace   device, >= kvr_sur_workspace_bytes(S, Q, d, n_units),
+ *               256-byte aligned.
+ *   positions_out device int32 [B]: the selected global positions,
+ *               ascending (ready for kvr_select).  n_out (host) receives B.
+ *   scores_out  device float [S] or NULL: the token scores r_i.
+ * EINVAL on NULL arguments, budget_percent outside [0, 100] or a small
+ * workspace; ERANGE when n_units > min(S, 65536).  Ids outside the
+ * vocabulary and empty units are caught on the device and reported by
+ * kvr_sur_status.  Enqueues only; synchronise the stream before reading.
+ * ------------------------------------------------------------------------- */
+size_t kvr_sur_workspace_bytes(int32_t S, int32_t Q, int32_t d, int32_t n_units);
+kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t dtype, const int32_t* suffix_ids,
+                          int32_t S, int32_t suffix_start, const int32_t* query_ids, int32_t Q,
+                          const int32_t* unit_bounds, int32_t n_units, int32_t budget_percent, void* workspace,
+                          size_t ws_bytes, int32_t* positions_out, int32_t* n_out, float* scores_out,
+                          void* stream);
+/* Synchronise `stream` and report a device-side failure of the last
+ * kvr_sur_select that used `workspace` (an id outside the vocabulary or a
+ * malformed partition: EDEVICE), clearing it. */
+kvr_status kvr_sur_status(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Layer-range policy of "CacheReforge: Bounded Recovery for Stale KV Caches
  * under Evolving Adapters" (Methodology: Layerwise Risk; Runtime risk and
  * range selection; Cache and anchor updates).  The adapter is one flat

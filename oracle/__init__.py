@@ -14,3 +14,4 @@ with rounding to the model's storage dtype only where a tensor is stored
 from .refresh import *  # noqa: F401,F403
 from .select import *   # noqa: F401,F403
 from . import policy  # noqa: F401  (CacheReforge layer-range policy: oracle.policy.*)
+from . import sur  # noqa: F401  (Semantic-Unit Refresh selection: oracle.sur.*)

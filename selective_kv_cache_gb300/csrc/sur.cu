@@ -1,0 +1,456 @@
+// sur.cu -- Semantic-Unit Refresh selection ("Budgeted KV-Cache Repair for
+// Evolving Contexts", Sec. 3.2 and Sec. 7.3: Eqs. 1/7 for token relevance,
+// ranked admission of whole units, Eq. 8 for the window of the unit that
+// does not fit).
+//
+//   sur_qnorm_kernel    one CTA per query token: E[q_j] / ||E[q_j]|| in fp32
+//   sur_score_kernel    64 suffix tokens per CTA against all queries: an fp32
+//                       tiled dot product (16 outputs per thread), the row
+//                       max over queries, 1/||E[s_i]||, and the 0.25 bonus
+//                       for a token that occurs in the query (whose cosine
+//                       with its own embedding is exactly 1)
+//   sur_unit_kernel     one warp per unit: mean of the four largest scores
+//   sur_rank_kernel     one thread per unit: its rank by (score desc, start asc)
+//   sur_admit_kernel    one CTA: admission in rank order by a block scan of
+//                       unit sizes, the forward-envelope window of the first
+//                       unit that does not fit, and compaction of the selected
+//                       tokens into ascending global positions
+// The scoring contraction is fp32 as the pages state (the tensor cores have
+// no fp32 MMA), so it runs on the FFMA pipe; everything after it is a few
+// passes over S floats.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "kvr_internal.h"
+
+namespace kvr {
+namespace {
+
+constexpr int kTokTile = 64;    // suffix tokens per CTA
+constexpr int kQryTile = 64;    // queries per inner tile
+constexpr int kKTile = 32;      // embedding dims per smem step
+constexpr int kAdmitThreads = 1024;
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+struct SurWs {
+    int32_t* err;        // [4]
+    float* qn;           // [Q][d] normalised query rows
+    float* scores;       // [S]
+    float* unit_score;   // [n_units]
+    int32_t* order;      // [n_units] unit of each rank
+    uint32_t* sel;       // [ceil(S/32)]
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) sur_qnorm_kernel(const T* __restrict__ E, int vocab, int d,
+                                                        const int32_t* __restrict__ qids, float* __restrict__ qn,
+                                                        int32_t* err) {
+    __shared__ float red[256];
+    const int j = blockIdx.x;
+    const int id = qids[j];
+    float* out = qn + (size_t)j * d;
+    if (id < 0 || id >= vocab) {
+        if (threadIdx.x == 0) atomicOr(err, DEV_ERR_INDEX);
+        for (int k = threadIdx.x; k < d; k += blockDim.x) out[k] = 0.f;
+        return;
+    }
+    const T* row = E + (size_t)id * d;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float v = ldf(row + k);
+        ss = fmaf(v, v, ss);
+    }
+    red[threadIdx.x] = ss;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    const float nrm = sqrtf(red[0]);
+    const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) out[k] = ldf(row + k) * inv;
+}
+
+// scores[i] = max_j <E[s_i], qn_j> / ||E[s_i]|| + 0.25 * [s_i in q]
+template <typename T>
+__global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E, int vocab, int d,
+                                                        const int32_t* __restrict__ sids, int S,
+                                                        const int32_t* __restrict__ qids, int Q,
+                                                        const float* __restrict__ qn, float* __restrict__ scores,
+                                                        int32_t* err) {
+    __shared__ float ts[kKTile][kTokTile + 4];   // token chunk, k-major
+    __shared__ float qs[kKTile][kQryTile + 4];   // query chunk, k-major
+    __shared__ float rowmax[kTokTile];
+    __shared__ float rownorm[kTokTile];
+    __shared__ int rowid[kTokTile];
+    const int i0 = blockIdx.x * kTokTile;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads, 4 x 4 outputs each
+    if (threadIdx.x < kTokTile) {
+        const int i = i0 + threadIdx.x;
+        int id = i < S ? sids[i] : -1;
+        if (i < S && (id < 0 || id >= vocab)) {
+            atomicOr(err, DEV_ERR_INDEX);
+            id = -1;
+        }
+        rowid[threadIdx.x] = id;
+        rowmax[threadIdx.x] = -INFINITY;
+        rownorm[threadIdx.x] = 0.f;
+    }
+    __syncthreads();
+    float nrm_part[4] = {0.f, 0.f, 0.f, 0.f};   // token sums of squares (first query tile only)
+    for (int j0 = 0; j0 < Q; j0 += kQryTile) {
+        float acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+        for (int k0 = 0; k0 < d; k0 += kKTile) {
+            // 64 tokens x 32 dims and 64 queries x 32 dims: 8 loads each per thread
+            for (int e = threadIdx.x; e < kTokTile * kKTile; e += 256) {
+                const int r = e / kKTile, k = e % kKTile;
+                const int id = rowid[r];
+                ts[k][r] = (id >= 0 && k0 + k < d) ? ldf(E + (size_t)id * d + k0 + k) : 0.f;
+                const int j = j0 + r;
+                qs[k][r] = (j < Q && k0 + k < d) ? qn[(size_t)j * d + k0 + k] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int k = 0; k < kKTile; ++k) {
+                float tv[4], qv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) tv[a] = ts[k][ty * 4 + a];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) qv[b] = qs[k][tx * 4 + b];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tv[a], qv[b], acc[a][b]);
+                if (j0 == 0 && tx == 0) {
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) nrm_part[a] = fmaf(tv[a], tv[a], nrm_part[a]);
+                }
+            }
+            __syncthreads();
+        }
+        // row max over this query tile: 16 threads (tx) share each row
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (j0 + tx * 4 + b < Q) m = fmaxf(m, acc[a][b]);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (tx == 0) rowmax[ty * 4 + a] = fmaxf(rowmax[ty * 4 + a], m);
+        }
+        if (j0 == 0 && tx == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) rownorm[ty * 4 + a] = sqrtf(nrm_part[a]);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x < kTokTile) {
+        const int i = i0 + threadIdx.x;
+        if (i < S) {
+            const int id = rowid[threadIdx.x];
+            const float nrm = rownorm[threadIdx.x];
+            bool in_q = false;
+            for (int j = 0; j < Q && !in_q; ++j) in_q = qids[j] == id;
+            // a token of the query meets its own embedding: cosine exactly 1
+            // (the largest possible), so its score is exactly 1 + 0.25
+            scores[i] = in_q ? 1.25f : (nrm > 0.f ? rowmax[threadIdx.x] / nrm : 0.f);
+        }
+    }
+}
+
+// mean of the four largest scores of each unit (all of them below four)
+__global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int n_units,
+                                float* __restrict__ unit_score, int32_t* err) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= n_units) return;
+    const int b = bounds[warp], e = bounds[warp + 1];
+    if (b >= e) {
+        if (lane == 0) atomicOr(err, DEV_ERR_INDEX);
+        if (lane == 0) unit_score[warp] = -INFINITY;
+        return;
+    }
+    // each lane keeps its own top four, then four rounds of warp max take the unit's
+    float t[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int i = b + lane; i < e; i += 32) {
+        float v = scores[i];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (v > t[k]) {
+                const float x = t[k];
+                t[k] = v;
+                v = x;
+            }
+        }
+    }
+    float sum = 0.f;
+    const int n = min(4, e - b);
+    int head = 0;
+    for (int k = 0; k < n; ++k) {
+        float m = head < 4 ? t[head] : -INFINITY;
+        int who = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
+            if (m2 > m || (m2 == m && w2 < who)) {
+                m = m2;
+                who = w2;
+            }
+        }
+        sum += m;
+        if (lane == who) ++head;
+    }
+    if (lane == 0) unit_score[warp] = sum / (float)n;
+}
+
+// rank of unit u: units with a higher score, or the same score and an earlier start
+__global__ void sur_rank_kernel(const float* __restrict__ unit_score, int n_units, int32_t* __restrict__ order) {
+    __shared__ float sc[1024];
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    const float mine = u < n_units ? unit_score[u] : 0.f;
+    int rank = 0;
+    for (int base = 0; base < n_units; base += 1024) {
+        const int v = base + threadIdx.x;
+        sc[threadIdx.x] = v < n_units ? unit_score[v] : 0.f;
+        __syncthreads();
+        const int lim = min(1024, n_units - base);
+        if (u < n_units)
+            for (int k = 0; k < lim; ++k) {
+                const float x = sc[k];
+                rank += (x > mine || (x == mine && base + k < u)) ? 1 : 0;
+            }
+        __syncthreads();
+    }
+    if (u < n_units) order[rank] = u;
+}
+
+__device__ int block_scan_incl(int v, int* total) {
+    __shared__ int ws[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) ws[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = ws[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        ws[lane] = w;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? ws[warp - 1] : 0);
+    *total = ws[31];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* __restrict__ scores,
+                                                                  const int32_t* __restrict__ bounds, int n_units,
+                                                                  const int32_t* __restrict__ order, int S, int B,
+                                                                  int suffix_start, uint32_t* __restrict__ sel,
+                                                                  int32_t* __restrict__ positions) {
+    __shared__ int s_partial, s_w, s_stop;
+    const int W = (S + 31) / 32;
+    for (int w = threadIdx.x; w < W; w += blockDim.x) sel[w] = 0u;
+    if (threadIdx.x == 0) {
+        s_partial = -1;
+        s_w = 0;
+        s_stop = 0;
+    }
+    __syncthreads();
+    // admission in rank order: unit of rank k is whole when its running end fits B
+    int carry = 0;
+    for (int base = 0; base < n_units; base += blockDim.x) {
+        const int k = base + threadIdx.x;
+        const int u = k < n_units ? order[k] : -1;
+        const int len = u >= 0 ? bounds[u + 1] - bounds[u] : 0;
+        int total;
+        const int end = carry + block_scan_incl(len, &total);
+        const int start = end - len;
+        if (u >= 0 && start < B) {
+            if (end <= B) {
+                for (int i = bounds[u]; i < bounds[u + 1]; ++i) atomicOr(&sel[i >> 5], 1u << (i & 31));
+            } else {
+                s_partial = u;   // the first unit that does not fit (unique: starts below B, ends above)
+                s_w = B - start;
+            }
+        }
+        carry += total;
+        __syncthreads();
+        if (carry >= B) break;
+    }
+    __syncthreads();
+    // forward-envelope window of the partial unit (Eq. 8): one thread, double.
+    // With P(t) the sum of u over [b, t], the window [a, a + w) sums to
+    // P(a + w - 1) - P(a - 1); a second envelope cursor, w tokens behind the
+    // first, supplies P(a - 1).  Strictly greater sums replace the best, so
+    // the earliest maximiser wins.
+    if (threadIdx.x == 0 && s_partial >= 0) {
+        const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w;
+        double rmax = -INFINITY;
+        for (int i = b; i < e; ++i) rmax = fmax(rmax, (double)scores[i]);
+        const double decay = exp(-1.0 / 16.0);
+        double u = 0.0, p = 0.0, u_lag = 0.0, p_lag = 0.0, best = -INFINITY;
+        int best_a = b;
+        for (int t = b; t < e; ++t) {
+            u = fmax(exp((double)scores[t] - rmax), decay * u);
+            p += u;
+            const int a = t - w + 1;
+            if (a < b) continue;
+            if (a > b) {
+                u_lag = fmax(exp((double)scores[a - 1] - rmax), decay * u_lag);
+                p_lag += u_lag;
+            }
+            const double win = p - p_lag;
+            if (win > best) {
+                best = win;
+                best_a = a;
+            }
+        }
+        for (int i = best_a; i < best_a + w; ++i) sel[i >> 5] |= 1u << (i & 31);
+    }
+    __syncthreads();
+    // compaction: ascending positions from the bit mask
+    int pcarry = 0;
+    for (int base = 0; base < W; base += blockDim.x) {
+        const int w = base + threadIdx.x;
+        uint32_t word = w < W ? sel[w] : 0u;
+        int total;
+        const int incl = block_scan_incl(__popc(word), &total);
+        int k = pcarry + incl - __popc(word);
+        while (word) {
+            const int bit = __ffs(word) - 1;
+            if (k < B) positions[k] = suffix_start + w * 32 + bit;
+            ++k;
+            word &= word - 1u;
+        }
+        pcarry += total;
+    }
+}
+
+}  // namespace
+
+size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) {
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    size_t off = 0;
+    const size_t o_err = off;
+    off += al(16);
+    const size_t o_qn = off;
+    off += al((size_t)Q * d * sizeof(float));
+    const size_t o_sc = off;
+    off += al((size_t)S * sizeof(float));
+    const size_t o_us = off;
+    off += al((size_t)n_units * sizeof(float));
+    const size_t o_or = off;
+    off += al((size_t)n_units * sizeof(int32_t));
+    const size_t o_sel = off;
+    off += al((size_t)((S + 31) / 32) * sizeof(uint32_t));
+    if (L && base) {
+        L->err = (int32_t*)(base + o_err);
+        L->qn = (float*)(base + o_qn);
+        L->scores = (float*)(base + o_sc);
+        L->unit_score = (float*)(base + o_us);
+        L->order = (int32_t*)(base + o_or);
+        L->sel = (uint32_t*)(base + o_sel);
+    }
+    return off;
+}
+
+}  // namespace kvr
+
+using namespace kvr;
+
+extern "C" {
+
+size_t kvr_sur_workspace_bytes(int32_t S, int32_t Q, int32_t d, int32_t n_units) {
+    if (S < 1 || Q < 1 || d < 1 || n_units < 1) return 0;
+    return sur_ws_layout(S, Q, d, n_units, nullptr, nullptr);
+}
+
+kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t dtype, const int32_t* suffix_ids,
+                          int32_t S, int32_t suffix_start, const int32_t* query_ids, int32_t Q,
+                          const int32_t* unit_bounds, int32_t n_units, int32_t budget_percent, void* workspace,
+                          size_t ws_bytes, int32_t* positions_out, int32_t* n_out, float* scores_out,
+                          void* stream) {
+    if (!embed || !suffix_ids || !query_ids || !unit_bounds || !workspace || !positions_out || !n_out) {
+        set_error("sur: NULL argument");
+        return KVR_EINVAL;
+    }
+    if (vocab < 1 || d < 1 || S < 1 || Q < 1 || n_units < 1 || suffix_start < 0 || budget_percent < 0 ||
+        budget_percent > 100 || (dtype != KVR_F32 && dtype != KVR_BF16)) {
+        set_error("sur: need vocab, d, S, Q, n_units >= 1, suffix_start >= 0, budget in [0, 100], dtype F32/BF16");
+        return KVR_EINVAL;
+    }
+    if (n_units > 65536 || n_units > S) {
+        set_error("sur: n_units must be <= min(S, 65536)");
+        return KVR_ERANGE;
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) {
+        set_error("sur: workspace must be 256-byte aligned");
+        return KVR_EINVAL;
+    }
+    SurWs L;
+    const size_t need = sur_ws_layout(S, Q, d, n_units, &L, (uint8_t*)workspace);
+    if (ws_bytes < need) {
+        set_error("sur: workspace too small: need " + std::to_string(need) + " bytes");
+        return KVR_EINVAL;
+    }
+    const int B = (int)std::min<int64_t>(S, ((int64_t)S * budget_percent + 99) / 100);   // Eq. 3
+    *n_out = B;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float* scores = scores_out ? scores_out : L.scores;
+    cudaError_t e = cudaMemsetAsync(L.err, 0, 16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sur");
+    if (dtype == KVR_BF16) {
+        sur_qnorm_kernel<__nv_bfloat16><<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, L.qn,
+                                                          L.err);
+        sur_score_kernel<__nv_bfloat16><<<(S + kTokTile - 1) / kTokTile, 256, 0, s>>>(
+            (const __nv_bfloat16*)embed, vocab, d, suffix_ids, S, query_ids, Q, L.qn, scores, L.err);
+    } else {
+        sur_qnorm_kernel<float><<<Q, 256, 0, s>>>((const float*)embed, vocab, d, query_ids, L.qn, L.err);
+        sur_score_kernel<float><<<(S + kTokTile - 1) / kTokTile, 256, 0, s>>>(
+            (const float*)embed, vocab, d, suffix_ids, S, query_ids, Q, L.qn, scores, L.err);
+    }
+    sur_unit_kernel<<<(n_units * 32 + 255) / 256, 256, 0, s>>>(scores, unit_bounds, n_units, L.unit_score, L.err);
+    sur_rank_kernel<<<(n_units + 1023) / 1024, 1024, 0, s>>>(L.unit_score, n_units, L.order);
+    if (B > 0)
+        sur_admit_kernel<<<1, kAdmitThreads, 0, s>>>(scores, unit_bounds, n_units, L.order, S, B, suffix_start,
+                                                     L.sel, positions_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "sur launch");
+    return KVR_OK;
+}
+
+kvr_status kvr_sur_status(void* workspace, void* stream) {
+    if (!workspace) {
+        set_error("sur status: NULL workspace");
+        return KVR_EINVAL;
+    }
+    int32_t h[4] = {0, 0, 0, 0};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(h, workspace, 16, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, 16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sur status");
+    if (h[0]) {
+        set_error("sur: an id outside the vocabulary or an empty unit");
+        return KVR_EDEVICE;
+    }
+    return KVR_OK;
+}
+
+}  // extern "C"

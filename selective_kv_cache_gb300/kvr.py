@@ -37,7 +37,8 @@ EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace
            "kvr_read_selection", "kvr_read_meta", "kvr_profile_enable", "kvr_profile_read",
            "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge",
            "kvr_shift", "kvr_splice", "kvr_cache_info", "kvr_restart_layer", "kvr_policy_sensitivity",
-           "kvr_policy_create", "kvr_policy_destroy", "kvr_policy_plan", "kvr_policy_commit", "kvr_policy_versions"]
+           "kvr_policy_create", "kvr_policy_destroy", "kvr_policy_plan", "kvr_policy_commit", "kvr_policy_versions",
+           "kvr_sur_workspace_bytes", "kvr_sur_select", "kvr_sur_status"]
 
 
 class kvr_model_desc(C.Structure):
@@ -82,6 +83,10 @@ lib.kvr_policy_destroy.argtypes = [P]
 lib.kvr_policy_plan.argtypes = [P, P, I32, I32, P, P, P, P]
 lib.kvr_policy_commit.argtypes = [P, P, I32, I32, C.c_int64, P]
 lib.kvr_policy_versions.argtypes = [P, P]
+lib.kvr_sur_workspace_bytes.argtypes = [I32, I32, I32, I32]
+lib.kvr_sur_workspace_bytes.restype = C.c_size_t
+lib.kvr_sur_select.argtypes = [P, I32, I32, I32, P, I32, I32, P, I32, P, I32, I32, P, C.c_size_t, P, P, P, P]
+lib.kvr_sur_status.argtypes = [P, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
@@ -92,7 +97,7 @@ lib.kvr_read_meta.argtypes = [P, P, P]
 lib.kvr_profile_enable.argtypes = [P, I32]
 lib.kvr_profile_read.argtypes = [P, P, P, I32]
 for _f in EXPORTS:
-    if _f not in ("kvr_workspace_bytes", "kvr_last_error", "kvr_restart_layer"):
+    if _f not in ("kvr_workspace_bytes", "kvr_last_error", "kvr_restart_layer", "kvr_sur_workspace_bytes"):
         getattr(lib, _f).restype = C.c_int
 
 
@@ -337,3 +342,26 @@ def kvr_policy_versions(p: int, n_layers: int):
     v = np.zeros(n_layers, np.int64)
     _check(lib.kvr_policy_versions(p, v.ctypes.data), "kvr_policy_versions")
     return v
+
+
+# ---------------------------------------------------------------- Semantic-Unit Refresh selection
+def kvr_sur_workspace_bytes(S: int, Q: int, d: int, n_units: int) -> int:
+    return int(lib.kvr_sur_workspace_bytes(S, Q, d, n_units))
+
+
+def kvr_sur_select(embed, suffix_ids, query_ids, unit_bounds, budget_percent: int, suffix_start: int, workspace,
+                   positions_out, scores_out=None, stream=None) -> int:
+    """Device tensors: embed [vocab, d], suffix_ids [S], query_ids [Q],
+    unit_bounds [n_units + 1] (int32), workspace (uint8), positions_out int32
+    (room for the allowance).  Returns B, the number of positions written."""
+    n = I32()
+    dt = KVR_BF16 if embed.dtype == torch.bfloat16 else KVR_F32
+    _check(lib.kvr_sur_select(_ptr(embed), embed.shape[0], embed.shape[1], dt, _ptr(suffix_ids), suffix_ids.numel(),
+                              suffix_start, _ptr(query_ids), query_ids.numel(), _ptr(unit_bounds),
+                              unit_bounds.numel() - 1, budget_percent, _ptr(workspace), workspace.numel(),
+                              _ptr(positions_out), C.byref(n), _ptr(scores_out), _stream(stream)), "kvr_sur_select")
+    return n.value
+
+
+def kvr_sur_status(workspace, stream=None):
+    _check(lib.kvr_sur_status(_ptr(workspace), _stream(stream)), "kvr_sur_status")

@@ -270,6 +270,29 @@ def make_positions(w: Workload):
     return seqs
 
 
+def make_unit_bounds(S: int, seed: int, lo: int = 8, hi: int = 128):
+    """A synthetic partition of an S-token suffix into semantic units of lo..hi
+    tokens (text segmentation stands outside the method's hot path): int32
+    offsets 0 = b_0 < ... < b_n = S.  The last unit takes the remainder and
+    may be shorter than lo."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    b = [0]
+    while b[-1] < S:
+        b.append(min(S, b[-1] + int(rng.integers(lo, hi + 1))))
+    return np.array(b, dtype=np.int32)
+
+
+def make_query_ids(vocab: int, Q: int, seed: int, suffix_ids=None, overlap: int = 4):
+    """Q query token ids, uniform over the vocabulary; `overlap` of them are
+    copied from the suffix so that the identical-token bonus occurs."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.integers(0, vocab, size=Q).astype(np.int32)
+    if suffix_ids is not None and overlap > 0:
+        sid = np.asarray(suffix_ids)
+        q[:overlap] = sid[rng.integers(0, sid.size, size=overlap)]
+    return q
+
+
 def block_bounds(w: Workload, n_blocks=8):
     """Half-open block spans [s_i, e_i) of an equal-block layout."""
     size = w.n_tokens // n_blocks
