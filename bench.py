@@ -269,6 +269,11 @@ def run_ours(args):
         shift = measure_shift(w, hbm)
         sur = measure_sur(s)
 
+    # ---- the pages' matched-work benchmark at their shape (Qwen3-8B-like)
+    mw = None
+    if args.workload == "llama8b" and not args.no_matched:
+        mw = matched_work()
+
     # ---- CPU oracle baseline on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -297,6 +302,7 @@ def run_ours(args):
         "packed_vs_interval": cmp,
         "shift": shift,
         "sur_select": sur,
+        "matched_work": mw,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -383,6 +389,74 @@ def measure_sur(s, reps=10):
             "us_median": round(us, 1), "bound": "fp32 FFMA", "achieved_tflops": round(ach, 2),
             "peak_tflops": round(peak, 1), "peak_source": "derived: 152 SMs x 128 lanes x 2 x 2.07 GHz",
             "frac": round(ach / peak, 4)}
+
+
+# Table 18 of "Budgeted KV-Cache Repair for Evolving Contexts" (Sec. 13.3):
+# Qwen3-8B on one H100, B = 64, medians in ms.  Context only (other hardware).
+PAGES_TABLE18_H100 = {(2048, 1): (31.465, 32.389), (2048, 4): (121.456, 32.470), (2048, 16): (485.378, 32.775),
+                      (8192, 1): (32.571, 33.372), (8192, 4): (120.679, 32.235), (8192, 16): (494.826, 33.375)}
+
+
+def matched_work():
+    """The pages' matched-work benchmark at their shape (Sec. 13.3, Table 18):
+    a Qwen3-8B-shaped stack (36 layers, 4096, 32/8 heads x 128, FFN 12288),
+    a random-token prompt of N + 8 tokens that loses 8 tokens at 64 (Shift,
+    untimed), B = 64 refreshed positions in R = 1, 4, 16 intervals with the
+    same M(U).  Timed like the pages: synchronised wall time per refresh,
+    host planning and upload included, medians of 20 after 10 warm-ups for the
+    packed refresh; the interval-wise comparator (the pages' direct
+    sequential control) takes 10 after 3."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    from selective_kv_cache_gb300 import kvr, workloads as wl
+    from selective_kv_cache_gb300.harness import Setup
+
+    w0 = wl.WORKLOADS["qwen3_matched"]
+    layers = wl.make_layer_weights(w0, "cuda")
+    embed = wl.make_embeddings(w0, "cuda")
+
+    def wall(fn, warm, reps):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return float(np.median(ts))
+
+    rows = []
+    for N in (2048, 8192):
+        w = dataclasses.replace(w0, capacity=N + 8, n_tokens=N + 8, suffix_start=64)
+        for R in (1, 4, 16):
+            pos = wl.matched_positions(N, 64, R)
+            s = Setup(w, weights=layers, positions=[pos], embed=embed)
+            kvr.kvr_shift(s.handle, 64, 8)            # the edit: 8 tokens deleted at 64
+            assert kvr.kvr_cache_info(s.handle) == (N, 64)
+            m_u = int(np.sum(pos.astype(np.int64) + 1))
+
+            def packed():
+                s.select()
+                s.refresh()
+
+            t_p = wall(packed, 10, 20)
+            t_i = wall(lambda: s.refresh_interval_wise(), 3, 10)
+            s.sync()
+            s.close()
+            seq_h100, custom_h100 = PAGES_TABLE18_H100[(N, R)]
+            rows.append({"N": N, "R": R, "B": 64, "M_U": m_u, "packed_ms": round(t_p, 3),
+                         "interval_wise_ms": round(t_i, 3), "speedup": round(t_i / t_p, 2),
+                         "pages_h100_direct_seq_ms": seq_h100, "pages_h100_custom_ms": custom_h100})
+    del layers, embed
+    torch.cuda.empty_cache()
+    return {"workload": "Qwen3-8B-shaped stack (36 L, d 4096, 32/8 heads x 128, FFN 12288, bf16, no QK norm), "
+                        "B = 64, 8 tokens deleted at 64, synchronised wall time with host planning",
+            "rows": rows}
 
 
 def compare_schedules(s1, args):
@@ -515,6 +589,7 @@ def main():
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the packed vs interval-wise comparison")
+    ap.add_argument("--no-matched", action="store_true", help="skip the matched-work benchmark (Qwen3-8B shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

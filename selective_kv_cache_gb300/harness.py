@@ -50,7 +50,7 @@ class Setup:
     selection (list of int arrays, one per sequence)."""
 
     def __init__(self, w: wl.Workload, cache="random", positions=None, weights=None, flags=0,
-                 local=None, sink=None, device="cuda"):
+                 local=None, sink=None, device="cuda", embed=None):
         self.w = w
         self.shape = w.model
         self.device = device
@@ -73,7 +73,7 @@ class Setup:
             w.alpha, w.beta, flags)
         self.words = (w.capacity + 31) // 32
         if w.uses_embeddings:
-            self.embed = wl.make_embeddings(w, device)
+            self.embed = embed if embed is not None else wl.make_embeddings(w, device)
             self.ids = wl.make_token_ids(w, device)
             self.hidden_src = None
         else:

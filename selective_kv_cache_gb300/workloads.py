@@ -77,6 +77,7 @@ class Workload:
     range_layers: tuple = ()   # (r0, r1): layers recomputed over the whole suffix
     lora_rank: int = 0
     uses_embeddings: bool = True
+    n_intervals: int = 0       # "matched" selection: the interval count R
 
     def seed(self, stream: int) -> int:
         return BASE_SEED + 100 * self.index + stream
@@ -85,6 +86,10 @@ class Workload:
 TINY = ModelShape(1, 256, 4, 4, 64, 1024, 10000.0, 1e-5, "f32", False)
 LLAMA8B = ModelShape(32, 4096, 32, 8, 128, 14336, 500000.0, 1e-5, "bf16", False)
 QWEN7B = ModelShape(28, 3584, 28, 4, 128, 18944, 1000000.0, 1e-6, "bf16", True)
+# Qwen3-8B geometry (36 layers, hidden 4096, 32 query / 8 K/V heads x 128, FFN
+# 12288, vocabulary 151936): the model of the pages' matched-work benchmark
+# ("Budgeted KV-Cache Repair for Evolving Contexts", Sec. 13.3).
+QWEN3_8B = ModelShape(36, 4096, 32, 8, 128, 12288, 1000000.0, 1e-6, "bf16", False, vocab=151936)
 QWEN1P5B = ModelShape(28, 1536, 12, 2, 128, 8960, 1000000.0, 1e-6, "bf16", True)
 
 WORKLOADS = {
@@ -100,6 +105,11 @@ WORKLOADS = {
                             alpha=-2.0, beta=-4.0, selection="seams"),
     "qwen1p5b_drift": Workload("qwen1p5b_drift", 4, QWEN1P5B, 4, 32768, 32768, 8192, 492,
                                selection="isolated", range_layers=(10, 15), lora_rank=16),
+    # the pages' matched-work benchmark: 8200-token prompt, 8 tokens deleted at
+    # 64 (Shift), 64 positions in 16 intervals about the centre of the 8192
+    # remaining (the bench runs N in {2048, 8192} and R in {1, 4, 16})
+    "qwen3_matched": Workload("qwen3_matched", 9, QWEN3_8B, 1, 8200, 8192, 64, 64, selection="matched",
+                              n_intervals=16),
     # the Llama-3-8B-shaped refresh cut to 2 layers: a small case (about 1.2 GB
     # on the device) for kernel profiles of the same launch configuration
     "llama8b_2l": Workload("llama8b_2l", 1, dataclasses.replace(LLAMA8B, n_layers=2), 1, 8192, 7680, 2048, 282,
@@ -260,6 +270,8 @@ def make_positions(w: Workload):
             pos = (rng.choice(hi - lo, size=w.n_select, replace=False) + lo).tolist()
         elif w.selection == "seams":
             pos = seam_positions(w)
+        elif w.selection == "matched":
+            pos = matched_positions(w.n_tokens, w.n_select, w.n_intervals).tolist()
         elif w.selection == "all":
             pos = list(range(lo, hi))
         else:
@@ -291,6 +303,25 @@ def make_query_ids(vocab: int, Q: int, seed: int, suffix_ids=None, overlap: int 
         sid = np.asarray(suffix_ids)
         q[:overlap] = sid[rng.integers(0, sid.size, size=overlap)]
     return q
+
+
+def matched_positions(N: int, B: int, R: int, spacing: int = 64):
+    """The matched-work geometry of the pages' execution benchmark ("Budgeted
+    KV-Cache Repair for Evolving Contexts", Sec. 13.3, Table 18): B positions
+    as R intervals of B/R tokens placed symmetrically about the centre
+    (N - 1)/2, so M(U) = sum(u + 1) = B (N + 1) / 2 is the same for every R
+    (65,568 at N = 2048 and 262,176 at N = 8192 with B = 64, the values the
+    pages state).  Interval k spans [a_k, a_k + B/R) with mean
+    (N - 1)/2 + (k - (R - 1)/2) * spacing; an even spacing keeps every a_k
+    an integer."""
+    L = B // R
+    assert L * R == B and spacing >= L and spacing % 2 == 0
+    c = (N - 1) / 2.0
+    starts = [c - (L - 1) / 2.0 + (k - (R - 1) / 2.0) * spacing for k in range(R)]
+    assert all(float(x).is_integer() for x in starts)
+    pos = np.concatenate([np.arange(int(a), int(a) + L) for a in starts])
+    assert pos.min() >= 0 and pos.max() < N
+    return pos.astype(np.int32)
 
 
 def block_bounds(w: Workload, n_blocks=8):
