@@ -139,11 +139,11 @@ def algorithmic(shape, R, M_pairs_per_head, u_max):
 
 def source_files(kernel_class):
     if kernel_class.startswith("gemm"):
-        return ["gemm.cu", "ptx.cuh"]
+        return ["gemm.cu", "kvr_internal.h", "ptx.cuh"]
     if kernel_class == "attention":
         return sorted(f for f in os.listdir(os.path.join(ROOT, "selective_kv_cache_gb300", "csrc"))
-                      if f.startswith("attn") or f == "ptx.cuh")
-    return ["elementwise.cu"]
+                      if f.startswith("attn") or f in ("ptx.cuh", "kvr_internal.h"))
+    return ["elementwise.cu", "kvr_internal.h"]
 
 
 def run_ours(args):
