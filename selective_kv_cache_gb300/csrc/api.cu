@@ -454,6 +454,23 @@ bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t
     return true;
 }
 
+bool make_tmap_4d_bf16(CUtensorMap* out, const void* base, const uint64_t dims_in[4], const uint64_t strides_bytes[3],
+                       const uint32_t box_in[4], std::string* why) {
+    if (!get_encode(why)) return false;
+    cuuint64_t dims[4] = {dims_in[0], dims_in[1], dims_in[2], dims_in[3]};
+    cuuint64_t strides[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled (4-d) failed with " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
 kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,
                      const RowSource& src, void* hidden_out, int32_t* n_rows_out, int32_t* n_intervals_out,
                      cudaStream_t s) {

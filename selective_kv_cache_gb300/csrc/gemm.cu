@@ -34,7 +34,10 @@ struct GemmDev {
     int32_t* err;
     int n_out, K, R, BN, m_tiles, n_tiles, splits, stages, tmem_cols, items, atoms;
     // fused SwiGLU (swiglu_F > 0, one K split): a tile holds 64 gate rows and the
-    // 64 matching up rows; the epilogue writes act[r][f] = silu(g) * u in bf16
+    // 64 matching up rows, interleaved in blocks of 16 (rows 32j..32j+15 gate
+    // f0+16j.., rows 32j+16..32j+31 the matching up), so every 32-lane TMEM
+    // quarter holds both halves of 16 features; the epilogue writes
+    // act[r][f] = silu(g) * u in bf16
     int swiglu_F;
     __nv_bfloat16* act;
 };
@@ -44,20 +47,6 @@ __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
 }
 
-// all four epilogue warps (128 threads) on named barrier 2; returns the AND of pred
-__device__ __forceinline__ bool epi_bar_and(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 2, 128, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // work item -> (feature tile, row tile, K range); row tiles of one feature tile
 // are consecutive items, so CTAs that run at the same time share weight tiles in L2
@@ -90,7 +79,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* acc_empty = acc_full + 2;    // [2]
     uint64_t* mma_done = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-    float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);   // [64][16] up values
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t acc_stride = (uint32_t)g.tmem_cols / 2u;
 
@@ -131,9 +119,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int a = 0; a < atoms; ++a) {
                     const int kx = (kb * atoms + a) * kBK;
                     uint8_t* da = sA + (size_t)s * stA + a * kTileABytes;
-                    if (g.swiglu_F) {   // gate rows f0..f0+63, then up rows F+f0..
-                        tma_load_2d(da, &tmA, &full[s], kx, m_t * 64);
-                        tma_load_2d(da + kTileABytes / 2, &tmA, &full[s], kx, g.swiglu_F + m_t * 64);
+                    if (g.swiglu_F) {   // one 4-d box: 16-row blocks g0 u0 g1 u1 g2 u2 g3 u3
+                        tma_load_4d(da, &tmA, &full[s], kx, 0, 0, m_t * 4);
                     } else {
                         tma_load_2d(da, &tmA, &full[s], kx, m_t * 128);
                     }
@@ -228,7 +215,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int got = 0;
             if (lane == 0) got = mbar_wait(&acc_full[ab], (uint32_t)(local >> 1) & 1u) ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
-            if (g.swiglu_F) got = epi_bar_and(got != 0);   // the four warps decide together
             if (!got) {
                 ok = false;
                 break;
@@ -250,28 +236,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                // lanes 0-63 (warps of quarters 0, 1) hold gate, lanes 64-127 the matching up
-                const int f = m_t * 64 + (q & 1) * 32 + lane;
-                float* row = xch + ((q & 1) * 32 + lane) * 16;
+                // this warp's lanes 0-15 hold gate of features f0+16q.., lanes 16-31
+                // the matching up.  For a column pair (2p, 2p+1) the gate lane takes
+                // column 2p and the up lane column 2p+1; one exchange across the
+                // half-warps hands each the other half of its pair.
+                const bool up_lane = lane >= 16;
+                const int f = m_t * 64 + q * 16 + (lane & 15);
+                __nv_bfloat16* act = g.act + f;
                 for (int c = 0; c < BN; c += 16) {
                     float v[16];
                     tmem_ld16(src + (uint32_t)c, v);
-                    if (q >= 2) {
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            reinterpret_cast<float4*>(row)[t] = make_float4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+                    for (int p = 0; p < 8; ++p) {
+                        const float a = v[2 * p], b = v[2 * p + 1];
+                        const float r = __shfl_xor_sync(0xffffffffu, up_lane ? a : b, 16);
+                        const float gv = up_lane ? r : a, uv = up_lane ? b : r;
+                        const int tok = tok0 + c + 2 * p + (up_lane ? 1 : 0);
+                        const float y = gv / (1.0f + __expf(-gv)) * uv;
+                        if (tok < g.R) act[(size_t)tok * g.swiglu_F] = __float2bfloat16_rn(y);
                     }
-                    epi_bar();
-                    if (q < 2) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int tok = tok0 + c + j;
-                            const float gv = v[j];
-                            const float a = gv / (1.0f + __expf(-gv)) * row[j];
-                            if (tok < g.R) g.act[(size_t)tok * g.swiglu_F + f] = __float2bfloat16_rn(a);
-                        }
-                    }
-                    epi_bar();
                 }
             }
             tc_fence_before();
@@ -365,7 +348,7 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
     p.atoms = (K % (2 * kBK) == 0) ? 2 : 1;
     const int KB = K / (kBK * p.atoms);
     const int tileB = p.BN * 128;
-    p.stages = std::min(8, (kSmemBudget - 1024 - 1024 - 4096) / (p.atoms * (kTileABytes + tileB)));
+    p.stages = std::min(8, (kSmemBudget - 1024 - 1024) / (p.atoms * (kTileABytes + tileB)));
     p.swiglu_F = 0;
     // K splits from a cost model fitted to measurements on GB300: one item
     // streams its (128 + BN) x (K / S) operand tiles at ~100 GB/s per SM, the
@@ -401,9 +384,16 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         return cudaSuccess;
     }
     CUtensorMap ta, tb;
-    if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, p.swiglu_F ? 64 : 128,
-                           why))
+    if (p.swiglu_F) {
+        // the [2F, K] gate/up matrix as (K, 16 rows, {gate, up}, F/16 blocks):
+        // a {64, 16, 2, 4} box lands as gate and up 16-row blocks in turn
+        const uint64_t dims[4] = {(uint64_t)p.K, 16, 2, (uint64_t)p.swiglu_F / 16};
+        const uint64_t strides[3] = {(uint64_t)p.K * 2, (uint64_t)p.swiglu_F * p.K * 2, (uint64_t)16 * p.K * 2};
+        const uint32_t box[4] = {(uint32_t)kBK, 16, 2, 4};
+        if (!make_tmap_4d_bf16(&ta, w, dims, strides, box, why)) return cudaErrorInvalidValue;
+    } else if (!make_tmap_2d_bf16(&ta, w, (uint64_t)p.K, (uint64_t)p.n_out, (uint64_t)p.K * 2, kBK, 128, why)) {
         return cudaErrorInvalidValue;
+    }
     if (!make_tmap_2d_bf16(&tb, x, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.K * 2, kBK, (uint32_t)p.BN, why))
         return cudaErrorInvalidValue;
     GemmDev g;
@@ -428,8 +418,8 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     int cols = 32;
     while (cols < 2 * p.BN) cols <<= 1;   // two accumulators
     g.tmem_cols = cols;
-    // pipeline ring, barriers (1 KB) and the SwiGLU exchange area (4 KB)
-    const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + 1024 + 64 * 16 * 4;
+    // alignment slack, pipeline ring, barriers (1 KB)
+    const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -88,6 +88,9 @@ bool make_tmap_2d_bf16(CUtensorMap* out, const void* base, uint64_t inner, uint6
 bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                        std::string* why);
+// 4-d: dims[0] innermost (elements), strides of dims 1-3 in bytes
+bool make_tmap_4d_bf16(CUtensorMap* out, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                       const uint32_t box[4], std::string* why);
 
 // ---------------------------------------------------------------- launchers
 struct SelectLaunch {
