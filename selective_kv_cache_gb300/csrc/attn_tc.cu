@@ -448,24 +448,46 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnLaunch a, int n_t
     const int p = m / G, gi = m % G;
     const int* plan = a.plan + 8 * tile;
     if (m >= (128 / G) * G || p >= plan[1]) return;
-    float mx = -INFINITY;
-    for (int s = 0; s < n_split; ++s) {
-        const size_t slot = ((size_t)s * n_tiles + tile) * a.n_kv_heads + h;
-        mx = fmaxf(mx, a.part_ml[(slot * 128 + m) * 2]);
-    }
+    // splits in groups of 8: all loads of a group are independent (one L2
+    // round trip), folded into a running (max, sum, o) in split order
+    constexpr int kGroup = 8;
+    float mx = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float l = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-        const size_t slot = ((size_t)s * n_tiles + tile) * a.n_kv_heads + h;
-        const float ms = a.part_ml[(slot * 128 + m) * 2];
-        if (ms == -INFINITY) continue;
-        const float w = ex2(ms - mx);
-        l += w * a.part_ml[(slot * 128 + m) * 2 + 1];
-        const float4 o = reinterpret_cast<const float4*>(a.part_o + (slot * 128 + m) * 128)[lane];
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+    for (int s0 = 0; s0 < n_split; s0 += kGroup) {
+        float ms[kGroup], ls[kGroup];
+        float4 os[kGroup];
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            ms[k] = -INFINITY;
+            if (s0 + k < n_split) {
+                const size_t slot = ((size_t)(s0 + k) * n_tiles + tile) * a.n_kv_heads + h;
+                const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[slot * 128 + m];
+                ms[k] = ml.x;
+                ls[k] = ml.y;
+                os[k] = reinterpret_cast<const float4*>(a.part_o + (slot * 128 + m) * 128)[lane];
+            }
+        }
+        float gm = mx;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) gm = fmaxf(gm, ms[k]);
+        if (gm == -INFINITY) continue;
+        const float r = ex2(mx - gm);   // rescale of what is accumulated so far (0 before the first split)
+        l *= r;
+        acc.x *= r;
+        acc.y *= r;
+        acc.z *= r;
+        acc.w *= r;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            if (ms[k] == -INFINITY) continue;
+            const float w = ex2(ms[k] - gm);
+            l += w * ls[k];
+            acc.x += w * os[k].x;
+            acc.y += w * os[k].y;
+            acc.z += w * os[k].z;
+            acc.w += w * os[k].w;
+        }
+        mx = gm;
     }
     const float inv = 1.0f / l;
     __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan[0] + p) * a.n_q_heads + h * G + gi) * 128;
