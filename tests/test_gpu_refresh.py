@@ -98,6 +98,25 @@ def test_bf16_small_against_oracle(selection, alpha, beta, sink_static):
     print(selection, alpha, beta, "worst scaled errors", worst)
 
 
+@pytest.mark.parametrize("alpha,beta", [(0.0, 0.0), (-2.0, -4.0)])
+def test_bf16_many_heads(alpha, beta):
+    """64 query / 8 K/V heads (80 head tiles of the QKV projection, 8 query
+    heads per K/V head); two layers, q/k/v bias, a ragged row tile."""
+    w = small_bf16(n_layers=2, d=512, hq=64, hkv=8, F=1024, n_select=150, selection="isolated", alpha=alpha,
+                   beta=beta)
+    layers = wl.make_layer_weights(w, "cuda")
+    rng = np.random.default_rng(13)
+    local = rng.random((1, w.capacity)) < 0.5
+    sink = rng.random((1, w.capacity)) < 0.2
+    s = Setup(w, weights=layers, local=local, sink=sink)
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = f64(s.embed)
+    ids = s.ids.cpu().numpy()
+    worst = run_and_compare(s, LazyWeights(layers), Ks0, Vs0, [emb[ids[0]]], TOL["bf16"])
+    s.close()
+    print("many-head worst", worst)
+
+
 def test_bf16_batch_of_sequences():
     """Independent sequences sharing weights (seq-major rows, per-sequence
     caches and plans)."""
