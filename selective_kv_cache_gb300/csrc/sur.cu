@@ -42,6 +42,7 @@ struct SurWs {
     float* unit_score;   // [n_units]
     int32_t* order;      // [n_units] unit of each rank
     uint32_t* sel;       // [ceil(S/32)]
+    double* cum;         // [S] prefix sums of the envelope of the partial unit
 };
 
 template <typename T>
@@ -74,20 +75,43 @@ __global__ void __launch_bounds__(256) sur_qnorm_kernel(const T* __restrict__ E,
     for (int k = threadIdx.x; k < d; k += blockDim.x) out[k] = ldf(row + k) * inv;
 }
 
+// 8 consecutive embedding values as fp32 (one 16-byte load for bf16)
+__device__ __forceinline__ void ld8f(const __nv_bfloat16* p, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void ld8f(const float* p, float* v) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 // scores[i] = max_j <E[s_i], qn_j> / ||E[s_i]|| + 0.25 * [s_i in q]
+// 64 tokens x 64 queries per CTA and step, 32 dimensions per step: thread
+// (ty, tx) owns tokens 4ty.. and queries 4tx.., 16 products from two float4
+// shared reads per dimension; each thread fetches one token row and one query
+// row segment of 8 dimensions per step, the next step's while this one runs.
+// Needs d % 8 == 0.
 template <typename T>
 __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E, int vocab, int d,
                                                         const int32_t* __restrict__ sids, int S,
                                                         const int32_t* __restrict__ qids, int Q,
                                                         const float* __restrict__ qn, float* __restrict__ scores,
                                                         int32_t* err) {
-    __shared__ float ts[kKTile][kTokTile + 4];   // token chunk, k-major
-    __shared__ float qs[kKTile][kQryTile + 4];   // query chunk, k-major
+    constexpr int kPad = 4;
+    __shared__ __align__(16) float ts[kKTile][kTokTile + kPad];   // token chunk, k-major
+    __shared__ __align__(16) float qs[kKTile][kQryTile + kPad];   // query chunk, k-major
     __shared__ float rowmax[kTokTile];
     __shared__ float rownorm[kTokTile];
     __shared__ int rowid[kTokTile];
     const int i0 = blockIdx.x * kTokTile;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads, 4 x 4 outputs each
+    const int lr = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;   // the row and 8 dims this thread fetches
     if (threadIdx.x < kTokTile) {
         const int i = i0 + threadIdx.x;
         int id = i < S ? sids[i] : -1;
@@ -97,45 +121,49 @@ __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E,
         }
         rowid[threadIdx.x] = id;
         rowmax[threadIdx.x] = -INFINITY;
-        rownorm[threadIdx.x] = 0.f;
     }
     __syncthreads();
-    float nrm_part[4] = {0.f, 0.f, 0.f, 0.f};   // token sums of squares (first query tile only)
+    const int my_id = rowid[lr];
+    float nrm = 0.f;   // sum of squares of this thread's token segment (first query tile)
     for (int j0 = 0; j0 < Q; j0 += kQryTile) {
         float acc[4][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+        const int qj = j0 + lr;
+        float tnext[8], qnext[8];
+        auto fetch = [&](int k0) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) tnext[t] = qnext[t] = 0.f;
+            if (k0 + lk < d) {
+                if (my_id >= 0) ld8f(E + (size_t)my_id * d + k0 + lk, tnext);
+                if (qj < Q) ld8f(qn + (size_t)qj * d + k0 + lk, qnext);
+            }
+        };
+        fetch(0);
         for (int k0 = 0; k0 < d; k0 += kKTile) {
-            // 64 tokens x 32 dims and 64 queries x 32 dims: 8 loads each per thread
-            for (int e = threadIdx.x; e < kTokTile * kKTile; e += 256) {
-                const int r = e / kKTile, k = e % kKTile;
-                const int id = rowid[r];
-                ts[k][r] = (id >= 0 && k0 + k < d) ? ldf(E + (size_t)id * d + k0 + k) : 0.f;
-                const int j = j0 + r;
-                qs[k][r] = (j < Q && k0 + k < d) ? qn[(size_t)j * d + k0 + k] : 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                ts[lk + t][lr] = tnext[t];
+                qs[lk + t][lr] = qnext[t];
+                if (j0 == 0) nrm = fmaf(tnext[t], tnext[t], nrm);
             }
             __syncthreads();
+            if (k0 + kKTile < d) fetch(k0 + kKTile);
 #pragma unroll 8
             for (int k = 0; k < kKTile; ++k) {
-                float tv[4], qv[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) tv[a] = ts[k][ty * 4 + a];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) qv[b] = qs[k][tx * 4 + b];
+                const float4 tv = *reinterpret_cast<const float4*>(&ts[k][ty * 4]);
+                const float4 qv = *reinterpret_cast<const float4*>(&qs[k][tx * 4]);
+                const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, q4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tv[a], qv[b], acc[a][b]);
-                if (j0 == 0 && tx == 0) {
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) nrm_part[a] = fmaf(tv[a], tv[a], nrm_part[a]);
-                }
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(t4[a], q4[b], acc[a][b]);
             }
             __syncthreads();
         }
-        // row max over this query tile: 16 threads (tx) share each row
+        // row max over this query tile: the 16 threads of a row group (tx) share each row
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             float m = -INFINITY;
@@ -146,9 +174,11 @@ __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E,
             for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (tx == 0) rowmax[ty * 4 + a] = fmaxf(rowmax[ty * 4 + a], m);
         }
-        if (j0 == 0 && tx == 0) {
-#pragma unroll
-            for (int a = 0; a < 4; ++a) rownorm[ty * 4 + a] = sqrtf(nrm_part[a]);
+        if (j0 == 0) {
+            // the four threads of a token row hold its four 8-dim segments of every step
+            nrm += __shfl_xor_sync(0xffffffffu, nrm, 1);
+            nrm += __shfl_xor_sync(0xffffffffu, nrm, 2);
+            if ((threadIdx.x & 3) == 0) rownorm[lr] = sqrtf(nrm);
         }
         __syncthreads();
     }
@@ -156,12 +186,12 @@ __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E,
         const int i = i0 + threadIdx.x;
         if (i < S) {
             const int id = rowid[threadIdx.x];
-            const float nrm = rownorm[threadIdx.x];
+            const float nr = rownorm[threadIdx.x];
             bool in_q = false;
             for (int j = 0; j < Q && !in_q; ++j) in_q = qids[j] == id;
             // a token of the query meets its own embedding: cosine exactly 1
             // (the largest possible), so its score is exactly 1 + 0.25
-            scores[i] = in_q ? 1.25f : (nrm > 0.f ? rowmax[threadIdx.x] / nrm : 0.f);
+            scores[i] = in_q ? 1.25f : (nr > 0.f ? rowmax[threadIdx.x] / nr : 0.f);
         }
     }
 }
@@ -262,14 +292,14 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
                                                                   const int32_t* __restrict__ bounds, int n_units,
                                                                   const int32_t* __restrict__ order, int S, int B,
                                                                   int suffix_start, uint32_t* __restrict__ sel,
+                                                                  double* __restrict__ cum,
                                                                   int32_t* __restrict__ positions) {
-    __shared__ int s_partial, s_w, s_stop;
+    __shared__ int s_partial, s_w;
     const int W = (S + 31) / 32;
     for (int w = threadIdx.x; w < W; w += blockDim.x) sel[w] = 0u;
     if (threadIdx.x == 0) {
         s_partial = -1;
         s_w = 0;
-        s_stop = 0;
     }
     __syncthreads();
     // admission in rank order: unit of rank k is whole when its running end fits B
@@ -294,34 +324,116 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
         if (carry >= B) break;
     }
     __syncthreads();
-    // forward-envelope window of the partial unit (Eq. 8): one thread, double.
-    // With P(t) the sum of u over [b, t], the window [a, a + w) sums to
-    // P(a + w - 1) - P(a - 1); a second envelope cursor, w tokens behind the
-    // first, supplies P(a - 1).  Strictly greater sums replace the best, so
-    // the earliest maximiser wins.
-    if (threadIdx.x == 0 && s_partial >= 0) {
-        const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w;
-        double rmax = -INFINITY;
-        for (int i = b; i < e; ++i) rmax = fmax(rmax, (double)scores[i]);
-        const double decay = exp(-1.0 / 16.0);
-        double u = 0.0, p = 0.0, u_lag = 0.0, p_lag = 0.0, best = -INFINITY;
-        int best_a = b;
-        for (int t = b; t < e; ++t) {
-            u = fmax(exp((double)scores[t] - rmax), decay * u);
-            p += u;
-            const int a = t - w + 1;
-            if (a < b) continue;
-            if (a > b) {
-                u_lag = fmax(exp((double)scores[a - 1] - rmax), decay * u_lag);
-                p_lag += u_lag;
+    // forward-envelope window of the partial unit (Eq. 8), in double.
+    // Unrolling u_t = max(exp(rho_t), g u_{t-1}) with rho = r - r_max and
+    // g = exp(-1/16) gives u_t = exp(max_{s<=t}(rho_s + s/16) - t/16): a block
+    // prefix max, one exponential per token, then a prefix sum C, and the
+    // window [a, a + w) sums to C[a + w - 1] - C[a - 1].  The largest sum wins,
+    // the earliest start on ties.
+    if (s_partial >= 0) {
+        __shared__ double red[32];
+        __shared__ int redi[32];
+        const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w, len = e - b;
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+        // r_max of the unit
+        double rm = -INFINITY;
+        for (int t = threadIdx.x; t < len; t += blockDim.x) rm = fmax(rm, (double)scores[b + t]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rm = fmax(rm, __shfl_xor_sync(0xffffffffu, rm, o));
+        if (lane == 0) red[wid] = rm;
+        __syncthreads();
+        if (wid == 0) {
+            double v = lane < nw ? red[lane] : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[0] = v;
+        }
+        __syncthreads();
+        const double rmax = red[0];
+        __syncthreads();
+        // prefix max of rho_s + s/16 and prefix sum of u, chunk by chunk
+        double pm_carry = -INFINITY, cs_carry = 0.0;
+        for (int base = 0; base < len; base += blockDim.x) {
+            const int t = base + threadIdx.x;
+            double a = t < len ? ((double)scores[b + t] - rmax) + (double)t / 16.0 : -INFINITY;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, a, o);
+                if (lane >= o) a = fmax(a, y);
             }
-            const double win = p - p_lag;
-            if (win > best) {
-                best = win;
-                best_a = a;
+            if (lane == 31) red[wid] = a;
+            __syncthreads();
+            if (wid == 0) {
+                double v = lane < nw ? red[lane] : -INFINITY;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v = fmax(v, y);
+                }
+                red[lane] = v;
+            }
+            __syncthreads();
+            const double pm = fmax(pm_carry, fmax(a, wid > 0 ? red[wid - 1] : -INFINITY));
+            const double chunk_max = red[nw - 1];
+            __syncthreads();
+            double u = t < len ? exp(pm - (double)t / 16.0) : 0.0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, u, o);
+                if (lane >= o) u += y;
+            }
+            if (lane == 31) red[wid] = u;
+            __syncthreads();
+            if (wid == 0) {
+                double v = lane < nw ? red[lane] : 0.0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += y;
+                }
+                red[lane] = v;
+            }
+            __syncthreads();
+            const double c = cs_carry + u + (wid > 0 ? red[wid - 1] : 0.0);
+            if (t < len) cum[t] = c;
+            cs_carry += red[nw - 1];
+            pm_carry = fmax(pm_carry, chunk_max);
+            __syncthreads();
+        }
+        // best window start
+        double best = -INFINITY;
+        int best_a = 0;
+        for (int a0 = threadIdx.x; a0 + w <= len; a0 += blockDim.x) {
+            const double sum = cum[a0 + w - 1] - (a0 > 0 ? cum[a0 - 1] : 0.0);
+            if (sum > best) {   // a0 ascends per thread: the first maximiser stays
+                best = sum;
+                best_a = a0;
             }
         }
-        for (int i = best_a; i < best_a + w; ++i) sel[i >> 5] |= 1u << (i & 31);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oa = __shfl_xor_sync(0xffffffffu, best_a, o);
+            if (ob > best || (ob == best && oa < best_a)) {
+                best = ob;
+                best_a = oa;
+            }
+        }
+        if (lane == 0) {
+            red[wid] = best;
+            redi[wid] = best_a;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double bb = red[0];
+            int ba = redi[0];
+            for (int k = 1; k < nw; ++k)
+                if (red[k] > bb || (red[k] == bb && redi[k] < ba)) {
+                    bb = red[k];
+                    ba = redi[k];
+                }
+            for (int i = b + ba; i < b + ba + w; ++i) sel[i >> 5] |= 1u << (i & 31);
+        }
     }
     __syncthreads();
     // compaction: ascending positions from the bit mask
@@ -359,6 +471,8 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) 
     off += al((size_t)n_units * sizeof(int32_t));
     const size_t o_sel = off;
     off += al((size_t)((S + 31) / 32) * sizeof(uint32_t));
+    const size_t o_cum = off;
+    off += al((size_t)S * sizeof(double));
     if (L && base) {
         L->err = (int32_t*)(base + o_err);
         L->qn = (float*)(base + o_qn);
@@ -366,6 +480,7 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) 
         L->unit_score = (float*)(base + o_us);
         L->order = (int32_t*)(base + o_or);
         L->sel = (uint32_t*)(base + o_sel);
+        L->cum = (double*)(base + o_cum);
     }
     return off;
 }
@@ -390,9 +505,10 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
         set_error("sur: NULL argument");
         return KVR_EINVAL;
     }
-    if (vocab < 1 || d < 1 || S < 1 || Q < 1 || n_units < 1 || suffix_start < 0 || budget_percent < 0 ||
+    if (vocab < 1 || d < 8 || d % 8 || S < 1 || Q < 1 || n_units < 1 || suffix_start < 0 || budget_percent < 0 ||
         budget_percent > 100 || (dtype != KVR_F32 && dtype != KVR_BF16)) {
-        set_error("sur: need vocab, d, S, Q, n_units >= 1, suffix_start >= 0, budget in [0, 100], dtype F32/BF16");
+        set_error("sur: need vocab, S, Q, n_units >= 1, d a multiple of 8, suffix_start >= 0, budget in [0, 100], "
+                  "dtype F32/BF16");
         return KVR_EINVAL;
     }
     if (n_units > 65536 || n_units > S) {
@@ -429,7 +545,7 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
     sur_rank_kernel<<<(n_units + 1023) / 1024, 1024, 0, s>>>(L.unit_score, n_units, L.order);
     if (B > 0)
         sur_admit_kernel<<<1, kAdmitThreads, 0, s>>>(scores, unit_bounds, n_units, L.order, S, B, suffix_start,
-                                                     L.sel, positions_out);
+                                                     L.sel, L.cum, positions_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sur launch");
     return KVR_OK;
