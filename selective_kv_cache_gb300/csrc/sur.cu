@@ -15,9 +15,12 @@
 //                       unit sizes, the forward-envelope window of the first
 //                       unit that does not fit, and compaction of the selected
 //                       tokens into ascending global positions
-// The scoring contraction is fp32 as the pages state (the tensor cores have
-// no fp32 MMA), so it runs on the FFMA pipe; everything after it is a few
-// passes over S floats.
+// The scoring contraction is fp32 as the pages state.  For bf16 embeddings it
+// runs on the tensor cores (sur_qsplit_kernel, sur_gather_kernel, the tcgen05
+// projection kernel, sur_finish_kernel): the normalised query splits exactly
+// into three bf16 terms and bf16 products are exact in fp32, so the dot
+// products are fp32 up to summation order.  fp32 embeddings take the FFMA
+// kernel.  Everything after it is a few passes over S floats.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -43,6 +46,11 @@ struct SurWs {
     int32_t* order;      // [n_units] unit of each rank
     uint32_t* sel;       // [ceil(S/32)]
     double* cum;         // [S] prefix sums of the envelope of the partial unit
+    // bf16 embeddings: the scoring contraction on the tensor cores
+    __nv_bfloat16* eg;   // [S_pad][d] gathered suffix embedding rows (zero rows past S)
+    __nv_bfloat16* qp;   // [3Q][d] normalised query rows as hi, mid and lo bf16 terms
+    float* enorm;        // [S] ||E[s_i]||
+    float* part;         // GEMM partials [splits][3Q][S_pad]
 };
 
 template <typename T>
@@ -196,6 +204,116 @@ __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E,
     }
 }
 
+// ---- tensor-core scoring (bf16 embeddings).  An fp32 value splits exactly
+// into three bf16 terms (8 significand bits each), and bf16 products are exact
+// in fp32, so <E[s], hi + mid + lo> accumulated in fp32 is the fp32 dot product
+// up to the order of the sums.
+
+// one CTA per query token: q = E[q_j] / ||E[q_j]|| in fp32, written as the rows
+// j (hi), Q + j (mid), 2Q + j (lo) of qp
+__global__ void __launch_bounds__(256) sur_qsplit_kernel(const __nv_bfloat16* __restrict__ E, int vocab, int d,
+                                                         const int32_t* __restrict__ qids, int Q,
+                                                         __nv_bfloat16* __restrict__ qp, int32_t* err) {
+    __shared__ float red[256];
+    const int j = blockIdx.x;
+    const int id = qids[j];
+    const bool ok = id >= 0 && id < vocab;
+    if (!ok && threadIdx.x == 0) atomicOr(err, DEV_ERR_INDEX);
+    const __nv_bfloat16* row = E + (size_t)(ok ? id : 0) * d;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float v = ok ? __bfloat162float(row[k]) : 0.f;
+        ss = fmaf(v, v, ss);
+    }
+    red[threadIdx.x] = ss;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    const float nrm = sqrtf(red[0]);
+    const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float x = ok ? __bfloat162float(row[k]) * inv : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const float r1 = x - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        qp[(size_t)j * d + k] = hi;
+        qp[(size_t)(Q + j) * d + k] = mid;
+        qp[(size_t)(2 * Q + j) * d + k] = lo;
+    }
+}
+
+// one warp per suffix token: its embedding row into eg (16-byte copies) and
+// its fp32 norm; rows S..S_pad-1 are zero
+__global__ void __launch_bounds__(256) sur_gather_kernel(const __nv_bfloat16* __restrict__ E, int vocab, int d,
+                                                         const int32_t* __restrict__ sids, int S, int S_pad,
+                                                         __nv_bfloat16* __restrict__ eg, float* __restrict__ enorm,
+                                                         int32_t* err) {
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (i >= S_pad) return;
+    uint4* dst = reinterpret_cast<uint4*>(eg + (size_t)i * d);
+    const int nv = d / 8;
+    int id = i < S ? sids[i] : -1;
+    if (i < S && (id < 0 || id >= vocab)) {
+        if (lane == 0) atomicOr(err, DEV_ERR_INDEX);
+        id = -1;
+    }
+    float ss = 0.f;
+    const uint4* src = reinterpret_cast<const uint4*>(E + (size_t)(id >= 0 ? id : 0) * d);
+    for (int v = lane; v < nv; v += 32) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (id >= 0) u = src[v];
+        dst[v] = u;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(h[t]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0 && i < S) enorm[i] = sqrtf(ss);
+}
+
+// scores from the GEMM partials: 32 suffix tokens per CTA, 8 threads per token
+// split the queries; consecutive threads take consecutive tokens (coalesced)
+__global__ void __launch_bounds__(256) sur_finish_kernel(const float* __restrict__ part, int splits, int S, int S_pad,
+                                                         int Q, const float* __restrict__ enorm,
+                                                         const int32_t* __restrict__ sids,
+                                                         const int32_t* __restrict__ qids, float* __restrict__ scores) {
+    __shared__ float red[8][32];
+    const int fl = threadIdx.x & 31, jg = threadIdx.x >> 5;
+    const int f = blockIdx.x * 32 + fl;
+    const size_t split_stride = (size_t)3 * Q * S_pad;
+    float best = -INFINITY;
+    if (f < S) {
+        for (int j = jg; j < Q; j += 8) {
+            float dot = 0.f;
+            for (int s = 0; s < splits; ++s) {
+                const float* p = part + s * split_stride + f;
+                dot += (p[(size_t)j * S_pad] + p[(size_t)(Q + j) * S_pad]) + p[(size_t)(2 * Q + j) * S_pad];
+            }
+            best = fmaxf(best, dot);
+        }
+    }
+    red[jg][fl] = best;
+    __syncthreads();
+    if (jg == 0 && f < S) {
+#pragma unroll
+        for (int g = 1; g < 8; ++g) best = fmaxf(best, red[g][fl]);
+        const int id = sids[f];
+        bool in_q = false;
+        for (int j = 0; j < Q && !in_q; ++j) in_q = qids[j] == id;
+        const float nr = enorm[f];
+        // a token of the query meets its own embedding: cosine exactly 1
+        scores[f] = in_q ? 1.25f : (nr > 0.f ? best / nr : 0.f);
+    }
+}
+
 // mean of the four largest scores of each unit (all of them below four)
 __global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int n_units,
                                 float* __restrict__ unit_score, int32_t* err) {
@@ -312,8 +430,13 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
         const int end = carry + block_scan_incl(len, &total);
         const int start = end - len;
         if (u >= 0 && start < B) {
-            if (end <= B) {
-                for (int i = bounds[u]; i < bounds[u + 1]; ++i) atomicOr(&sel[i >> 5], 1u << (i & 31));
+            if (end <= B) {   // the whole unit: whole-word masks, at most ceil(len/32) + 1 atomics
+                const int b0 = bounds[u], e0 = bounds[u + 1];
+                for (int w = b0 >> 5; w <= (e0 - 1) >> 5; ++w) {
+                    const int lo = max(b0 - 32 * w, 0), hi = min(e0 - 32 * w, 32);
+                    const uint32_t mask = (hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+                    atomicOr(&sel[w], mask);
+                }
             } else {
                 s_partial = u;   // the first unit that does not fit (unique: starts below B, ends above)
                 s_w = B - start;
@@ -456,7 +579,7 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
 
 }  // namespace
 
-size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) {
+size_t sur_ws_layout(int S, int Q, int d, int n_units, bool tc, SurWs* L, uint8_t* base) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     size_t off = 0;
     const size_t o_err = off;
@@ -473,6 +596,19 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) 
     off += al((size_t)((S + 31) / 32) * sizeof(uint32_t));
     const size_t o_cum = off;
     off += al((size_t)S * sizeof(double));
+    size_t o_eg = 0, o_qp = 0, o_en = 0, o_part = 0;
+    if (tc) {
+        const int S_pad = (S + 127) / 128 * 128;
+        const GemmPlan gp = plan_gemm(KVR_BF16, S_pad, d, 3 * Q);
+        o_eg = off;
+        off += al((size_t)S_pad * d * 2);
+        o_qp = off;
+        off += al((size_t)3 * Q * d * 2);
+        o_en = off;
+        off += al((size_t)S * sizeof(float));
+        o_part = off;
+        off += al(gemm_partial_bytes(gp));
+    }
     if (L && base) {
         L->err = (int32_t*)(base + o_err);
         L->qn = (float*)(base + o_qn);
@@ -481,6 +617,10 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, SurWs* L, uint8_t* base) 
         L->order = (int32_t*)(base + o_or);
         L->sel = (uint32_t*)(base + o_sel);
         L->cum = (double*)(base + o_cum);
+        L->eg = tc ? (__nv_bfloat16*)(base + o_eg) : nullptr;
+        L->qp = tc ? (__nv_bfloat16*)(base + o_qp) : nullptr;
+        L->enorm = tc ? (float*)(base + o_en) : nullptr;
+        L->part = tc ? (float*)(base + o_part) : nullptr;
     }
     return off;
 }
@@ -493,7 +633,7 @@ extern "C" {
 
 size_t kvr_sur_workspace_bytes(int32_t S, int32_t Q, int32_t d, int32_t n_units) {
     if (S < 1 || Q < 1 || d < 1 || n_units < 1) return 0;
-    return sur_ws_layout(S, Q, d, n_units, nullptr, nullptr);
+    return sur_ws_layout(S, Q, d, n_units, d % 64 == 0, nullptr, nullptr);
 }
 
 kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t dtype, const int32_t* suffix_ids,
@@ -520,7 +660,8 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
         return KVR_EINVAL;
     }
     SurWs L;
-    const size_t need = sur_ws_layout(S, Q, d, n_units, &L, (uint8_t*)workspace);
+    const bool tc = dtype == KVR_BF16 && d % 64 == 0;   // the scoring contraction on the tensor cores
+    const size_t need = sur_ws_layout(S, Q, d, n_units, tc, &L, (uint8_t*)workspace);
     if (ws_bytes < need) {
         set_error("sur: workspace too small: need " + std::to_string(need) + " bytes");
         return KVR_EINVAL;
@@ -531,7 +672,19 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
     float* scores = scores_out ? scores_out : L.scores;
     cudaError_t e = cudaMemsetAsync(L.err, 0, 16, s);
     if (e != cudaSuccess) return cuda_fail(e, "sur");
-    if (dtype == KVR_BF16) {
+    if (tc) {
+        pdl_begin_call();   // the projection kernel must not overlap the gather that feeds it
+        const int S_pad = (S + 127) / 128 * 128;
+        sur_qsplit_kernel<<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, Q, L.qp, L.err);
+        sur_gather_kernel<<<(unsigned)(((size_t)S_pad * 32 + 255) / 256), 256, 0, s>>>(
+            (const __nv_bfloat16*)embed, vocab, d, suffix_ids, S, S_pad, L.eg, L.enorm, L.err);
+        const GemmPlan gp = plan_gemm(KVR_BF16, S_pad, d, 3 * Q);
+        std::string why;
+        e = launch_gemm(KVR_BF16, gp, L.eg, L.qp, L.part, L.err, s, &why);
+        if (e != cudaSuccess) return cuda_fail(e, ("sur scoring " + why).c_str());
+        sur_finish_kernel<<<(S + 31) / 32, 256, 0, s>>>(L.part, gp.splits, S, S_pad, Q, L.enorm, suffix_ids,
+                                                        query_ids, scores);
+    } else if (dtype == KVR_BF16) {
         sur_qnorm_kernel<__nv_bfloat16><<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, L.qn,
                                                           L.err);
         sur_score_kernel<__nv_bfloat16><<<(S + kTokTile - 1) / kTokTile, 256, 0, s>>>(
