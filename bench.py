@@ -146,6 +146,21 @@ def source_files(kernel_class):
     return ["elementwise.cu", "kvr_internal.h"]
 
 
+def job_throughput(local_time, units_per_rank, world, device=None):
+    """Whole-job throughput of N independent replicas: the slowest rank's
+    time (max over ranks) bounds the job, and every rank processed
+    units_per_rank units.  Works on any process-group backend (NCCL on GPUs,
+    gloo on CPU); returns (max time, units per second)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(local_time)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max = float(t.item())
+    return t_max, units_per_rank * world / t_max
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -192,12 +207,9 @@ def run_ours(args):
     barrier()
     ms = ev0.elapsed_time(ev1)
     s.sync()
-    t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
     rows = s.n_rows
-    value = rows * args.steps * world / (ms_total / 1e3)
+    sec_total, value = job_throughput(ms / 1e3, rows * args.steps, world, device="cuda")
+    ms_total = sec_total * 1e3
 
     # ---- per-kernel breakdown: the same K steps again with CUDA events around every launch
     kvr.kvr_profile_read(s.handle)
@@ -223,10 +235,7 @@ def run_ours(args):
         out_host.copy_(s.hidden, non_blocking=True)
         stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    t = torch.tensor([e2e_s], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = rows * args.steps * world / float(t.item())
+    _, e2e_value = job_throughput(e2e_s, rows * args.steps, world, device="cuda")
 
     # ---- roofline of the dominant kernel
     hbm, tf_burst, tf_sust, src = peaks()
