@@ -463,7 +463,7 @@ def matched_work():
                          "pages_h100_direct_seq_ms": seq_h100, "pages_h100_custom_ms": custom_h100})
     del layers, embed
     torch.cuda.empty_cache()
-    return {"workload": "Qwen3-8B-shaped stack (36 L, d 4096, 32/8 heads x 128, FFN 12288, bf16, no QK norm), "
+    return {"workload": "Qwen3-8B-shaped stack (36 L, d 4096, 32/8 heads x 128, FFN 12288, bf16, Q/K RMSNorm), "
                         "B = 64, 8 tokens deleted at 64, synchronised wall time with host planning",
             "rows": rows}
 

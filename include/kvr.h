@@ -78,6 +78,9 @@ typedef struct {
     float   rms_eps;
     int32_t dtype;          /* kvr_dtype of weights, cache and hidden rows */
     int32_t has_qkv_bias;   /* Qwen2.5 shapes carry q/k/v biases */
+    int32_t has_qk_norm;    /* Qwen3 shapes: RMSNorm of every Q and K head (over head_dim,
+                               eps = rms_eps) before RoPE; the recompute of "Budgeted
+                               KV-Cache Repair", Sec. 13.2, runs the model's own block */
 } kvr_model_desc;
 
 /* One layer's weights: caller-owned device pointers in the model dtype,
@@ -91,6 +94,8 @@ typedef struct {
     const void* w_down;     /* [d, F] */
     const void* norm1;      /* [d] RMSNorm weight before attention */
     const void* norm2;      /* [d] RMSNorm weight before the MLP */
+    const void* q_norm;     /* [head_dim] per-head RMSNorm weight of Q, or NULL without has_qk_norm */
+    const void* k_norm;     /* [head_dim] per-head RMSNorm weight of K, or NULL without has_qk_norm */
 } kvr_layer_weights;
 
 typedef struct kvr_cache kvr_cache;   /* opaque */

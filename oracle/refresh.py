@@ -9,8 +9,8 @@ Sources (cited by page title and section):
          Composable" (re-rotating a chunk's keys to new positions), Sec. 5
 
 Model block (the pages run dense Llama/Qwen decoders): pre-norm RMSNorm,
-Q/K/V projections (+bias for Qwen2.5 shapes), rotate-half RoPE at global
-positions, grouped-query softmax attention with scale 1/sqrt(d_h), output
+Q/K/V projections (+bias for Qwen2.5 shapes; per-head RMSNorm of Q and K
+for Qwen3 shapes), rotate-half RoPE at global positions, grouped-query softmax attention with scale 1/sqrt(d_h), output
 projection + residual, RMSNorm, SwiGLU MLP + residual.
 
 Storage rounding.  Arithmetic is float64 throughout.  A value is rounded to
@@ -33,7 +33,7 @@ import numpy as np
 from .select import effective_masks, intervals, sorted_positions
 
 __all__ = [
-    "Spec", "round_bf16", "round_store", "rms_norm", "rope", "silu",
+    "Spec", "round_bf16", "round_store", "rms_norm", "qk_norm", "rope", "silu",
     "attention", "layer_rows", "refresh_packed", "refresh_interval",
     "refresh_range", "prefill", "shift", "reposition", "attend", "lora_delta",
 ]
@@ -93,6 +93,17 @@ def rms_norm(x, w, eps):
     """RMSNorm: x / sqrt(mean(x^2) + eps) * w over the last axis."""
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * w
+
+
+def qk_norm(W, q, k, eps):
+    """Q/K normalisation ([BKR] Sec. 13.2, which recomputes the selected
+    rows with the model's own projections, its Q/K normalisation and its
+    rotary map; the Qwen3 block): every query and key head is RMS-normalised
+    over its d_h dimensions with its own weight vector before the rotary map.  q [R, Hq, d_h], k [R, Hkv, d_h]; a layer
+    without q_norm/k_norm weights passes both through."""
+    if W.get("q_norm") is None:
+        return q, k
+    return rms_norm(q, W["q_norm"], eps), rms_norm(k, W["k_norm"], eps)
 
 
 def rope(x, pos, theta):
@@ -183,8 +194,9 @@ def layer_rows(spec: Spec, W, X, K, V, pos, bias):
     if W.get("a_q") is not None:
         q = q + lora_delta(xn, W["a_q"], W["b_q"])
         v = v + lora_delta(xn, W["a_v"], W["b_v"])
-    q = rnd(rope(q.reshape(R, Hq, dh).transpose(1, 0, 2), pos, spec.rope_theta)).transpose(1, 0, 2)
-    k = rnd(rope(k.reshape(R, Hkv, dh).transpose(1, 0, 2), pos, spec.rope_theta))
+    q, k = qk_norm(W, q.reshape(R, Hq, dh), k.reshape(R, Hkv, dh), spec.rms_eps)
+    q = rnd(rope(q.transpose(1, 0, 2), pos, spec.rope_theta)).transpose(1, 0, 2)
+    k = rnd(rope(k.transpose(1, 0, 2), pos, spec.rope_theta))
     v = rnd(v.reshape(R, Hkv, dh).transpose(1, 0, 2))
     K[:, pos, :] = k
     V[:, pos, :] = v
@@ -346,8 +358,9 @@ def prefill(spec: Spec, weights, X_in, block_bounds=None, return_boundary_at=Non
         if W.get("a_q") is not None:
             q = q + lora_delta(xn, W["a_q"], W["b_q"])
             v = v + lora_delta(xn, W["a_v"], W["b_v"])
-        q = rnd(rope(q.reshape(N, Hq, dh).transpose(1, 0, 2), pos, spec.rope_theta))
-        k = rnd(rope(k.reshape(N, Hkv, dh).transpose(1, 0, 2), pos, spec.rope_theta))
+        q, k = qk_norm(W, q.reshape(N, Hq, dh), k.reshape(N, Hkv, dh), spec.rms_eps)
+        q = rnd(rope(q.transpose(1, 0, 2), pos, spec.rope_theta))
+        k = rnd(rope(k.transpose(1, 0, 2), pos, spec.rope_theta))
         v = rnd(v.reshape(N, Hkv, dh).transpose(1, 0, 2))
         Ks[l], Vs[l] = k, v
         o = np.zeros((N, Hq, dh))

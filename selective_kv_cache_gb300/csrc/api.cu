@@ -221,7 +221,12 @@ kvr_status check_layer_weights(const kvr_cache* c, const kvr_layer_weights* w) {
         set_error("layer weights: the model has q/k/v biases but b_qkv is NULL");
         return KVR_EINVAL;
     }
-    const void* ps[] = {w->w_qkv, w->b_qkv, w->w_o, w->w_gate_up, w->w_down, w->norm1, w->norm2};
+    if (c->m.has_qk_norm && (!w->q_norm || !w->k_norm)) {
+        set_error("layer weights: the model has Q/K normalisation but q_norm or k_norm is NULL");
+        return KVR_EINVAL;
+    }
+    const void* ps[] = {w->w_qkv, w->b_qkv, w->w_o, w->w_gate_up, w->w_down, w->norm1, w->norm2,
+                        c->m.has_qk_norm ? w->q_norm : nullptr, c->m.has_qk_norm ? w->k_norm : nullptr};
     for (const void* p : ps)
         if (p && !aligned16(p)) {
             set_error("layer weights must be 16-byte aligned");
@@ -281,6 +286,9 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.n_kv_heads = m.n_kv_heads;
         a.head_dim = m.head_dim;
         a.bias = m.has_qkv_bias ? w->b_qkv : nullptr;
+        a.q_norm = m.has_qk_norm ? w->q_norm : nullptr;
+        a.k_norm = m.has_qk_norm ? w->k_norm : nullptr;
+        a.eps = m.rms_eps;
         a.rope = c->d_rope;
         a.U = c->d_U;
         a.row_seq = c->d_row_seq;

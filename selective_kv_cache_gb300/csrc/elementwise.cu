@@ -124,6 +124,26 @@ __global__ void epi_qkv_kernel(QkvEpi a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) { x1[j] += b1[j]; x2[j] += b2[j]; }
     }
+    if (a.q_norm && hh < a.n_q_heads + a.n_kv_heads) {
+        // Q/K normalisation: RMSNorm of the head over its d_h dims, whose 8-wide
+        // chunks sit in `chunks` consecutive lanes (a group aligned to chunks)
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += x1[j] * x1[j] + x2[j] * x2[j];
+        const int lane = threadIdx.x & 31;
+        const unsigned gm = chunks >= 32 ? 0xffffffffu : ((1u << chunks) - 1u) << (lane & ~(chunks - 1));
+        for (int o = 1; o < chunks; o <<= 1) ss += __shfl_xor_sync(gm, ss, o);
+        const float inv = rsqrtf(ss / (float)dh + a.eps);
+        const T* wn = (const T*)(hh < a.n_q_heads ? a.q_norm : a.k_norm);
+        float w1[8], w2[8];
+        load8<T>(wn + c * 8, w1);
+        load8<T>(wn + half + c * 8, w2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            x1[j] = x1[j] * inv * w1[j];
+            x2[j] = x2[j] * inv * w2[j];
+        }
+    }
     const int u = a.U[r];
     const int seq = a.row_seq[r];
     if (u < 0 || u >= a.capacity) {

@@ -168,6 +168,9 @@ struct QkvEpi {
     const float* part;
     int splits, R, n_q_heads, n_kv_heads, head_dim;
     const void* bias;          // nullable
+    const void* q_norm;        // [head_dim] per-head RMSNorm weights of Q and K, or NULL (no Q/K norm)
+    const void* k_norm;
+    float eps;
     const float2* rope;        // [capacity][head_dim/2]
     const int32_t* U;
     const int32_t* row_seq;

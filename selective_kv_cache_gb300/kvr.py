@@ -45,11 +45,12 @@ class kvr_model_desc(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32),
                 ("rope_theta", C.c_double), ("rms_eps", C.c_float), ("dtype", C.c_int32),
-                ("has_qkv_bias", C.c_int32)]
+                ("has_qkv_bias", C.c_int32), ("has_qk_norm", C.c_int32)]
 
 
 class kvr_layer_weights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in ("w_qkv", "b_qkv", "w_o", "w_gate_up", "w_down", "norm1", "norm2")]
+    _fields_ = [(n, C.c_void_p) for n in ("w_qkv", "b_qkv", "w_o", "w_gate_up", "w_down", "norm1", "norm2",
+                                          "q_norm", "k_norm")]
 
 
 class KvrError(RuntimeError):
@@ -124,13 +125,14 @@ def model_desc(shape) -> kvr_model_desc:
     """kvr_model_desc from any object with the shape attributes."""
     return kvr_model_desc(shape.n_layers, shape.d_model, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                           shape.ffn_dim, float(shape.rope_theta), float(shape.rms_eps),
-                          KVR_BF16 if shape.dtype == "bf16" else KVR_F32, int(bool(shape.qkv_bias)))
+                          KVR_BF16 if shape.dtype == "bf16" else KVR_F32, int(bool(shape.qkv_bias)),
+                          int(bool(getattr(shape, "qk_norm", False))))
 
 
 def layer_weights(L) -> kvr_layer_weights:
     """kvr_layer_weights from a dict of device tensors (keys as the struct)."""
     return kvr_layer_weights(*[_ptr(L.get(k)) for k in ("w_qkv", "b_qkv", "w_o", "w_gate_up", "w_down",
-                                                         "norm1", "norm2")])
+                                                         "norm1", "norm2", "q_norm", "k_norm")])
 
 
 def layer_weights_array(layers: Sequence[dict]):

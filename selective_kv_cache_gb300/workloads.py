@@ -51,6 +51,7 @@ class ModelShape:
     dtype: str          # "f32" or "bf16"
     qkv_bias: bool
     vocab: int = 32000
+    qk_norm: bool = False   # Qwen3: RMSNorm of every Q and K head before RoPE
 
     @property
     def qkv_out(self) -> int:
@@ -89,7 +90,7 @@ QWEN7B = ModelShape(28, 3584, 28, 4, 128, 18944, 1000000.0, 1e-6, "bf16", True)
 # Qwen3-8B geometry (36 layers, hidden 4096, 32 query / 8 K/V heads x 128, FFN
 # 12288, vocabulary 151936): the model of the pages' matched-work benchmark
 # ("Budgeted KV-Cache Repair for Evolving Contexts", Sec. 13.3).
-QWEN3_8B = ModelShape(36, 4096, 32, 8, 128, 12288, 1000000.0, 1e-6, "bf16", False, vocab=151936)
+QWEN3_8B = ModelShape(36, 4096, 32, 8, 128, 12288, 1000000.0, 1e-6, "bf16", False, vocab=151936, qk_norm=True)
 QWEN1P5B = ModelShape(28, 1536, 12, 2, 128, 8960, 1000000.0, 1e-6, "bf16", True)
 
 WORKLOADS = {
@@ -160,6 +161,7 @@ def make_layer_weights(w: Workload, device="cpu", lora: Optional[str] = None):
     w_gate_up [2F, d]               rows 0..F-1 gate, F..2F-1 up
     w_down    [d, F]
     norm1/2   [d]                    ones
+    q_norm/k_norm [dh]               1 + 0.1 N(0, 1), only for shapes with qk_norm
     LoRA (lora='old'|'new'): a_q [r, d], b_q [Hq dh, r], a_v [r, d], b_v [Hkv dh, r]
     """
     m = w.model
@@ -178,6 +180,9 @@ def make_layer_weights(w: Workload, device="cpu", lora: Optional[str] = None):
             "norm1": torch.ones(m.d_model, dtype=dt, device=device),
             "norm2": torch.ones(m.d_model, dtype=dt, device=device),
         }
+        if m.qk_norm:
+            L["q_norm"] = (1.0 + _normal((m.head_dim,), 0.1, s + 6, device, torch.float32, rng)).to(dt)
+            L["k_norm"] = (1.0 + _normal((m.head_dim,), 0.1, s + 7, device, torch.float32, rng)).to(dt)
         if lora is not None and w.lora_rank > 0:
             ls = w.seed(4 if lora == "old" else 5) * 1000 + 17 * l
             lrng = np.random.Generator(np.random.PCG64(ls)) if device == "cpu" else None

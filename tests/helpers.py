@@ -54,10 +54,10 @@ def assert_close(got, want, tol, what=""):
 
 def small_bf16(name="bf16_small", *, n_layers=2, d=512, hq=8, hkv=2, F=1024, capacity=1200, n_tokens=1100,
                suffix_start=300, n_select=150, alpha=0.0, beta=0.0, selection="units", batch=1, qkv_bias=True,
-               theta=500000.0):
+               theta=500000.0, qk_norm=False):
     """A small bf16 workload with the big configs' structure (head_dim 128,
     grouped queries) that the float64 oracle finishes in seconds."""
-    m = wl.ModelShape(n_layers, d, hq, hkv, 128, F, theta, 1e-5, "bf16", qkv_bias, vocab=1000)
+    m = wl.ModelShape(n_layers, d, hq, hkv, 128, F, theta, 1e-5, "bf16", qkv_bias, vocab=1000, qk_norm=qk_norm)
     return wl.Workload(name, 7, m, batch, capacity, n_tokens, suffix_start, n_select, alpha=alpha, beta=beta,
                        selection=selection)
 

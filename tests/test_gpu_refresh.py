@@ -117,6 +117,29 @@ def test_bf16_many_heads(alpha, beta):
     print("many-head worst", worst)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_qk_norm_model_against_oracle(dtype):
+    """Q/K normalisation (Budgeted KV-Cache Repair, Sec. 13.2; the Qwen3
+    block): every Q and K head RMS-normalised with its own weights before
+    RoPE, no q/k/v bias; bf16 (head_dim 128) and fp32 (head_dim 64)."""
+    if dtype == "bf16":
+        w = small_bf16(n_layers=2, qkv_bias=False, qk_norm=True, selection="isolated", alpha=-1.0, beta=-2.0)
+    else:
+        m = wl.ModelShape(1, 256, 4, 2, 64, 512, 10000.0, 1e-5, "f32", False, vocab=500, qk_norm=True)
+        w = wl.Workload("f32_qknorm", 8, m, 1, 700, 640, 200, 40, alpha=-1.0, beta=-2.0, selection="units")
+    layers = wl.make_layer_weights(w, "cuda")
+    rng = np.random.default_rng(17)
+    local = rng.random((1, w.capacity)) < 0.5
+    sink = rng.random((1, w.capacity)) < 0.2
+    s = Setup(w, weights=layers, local=local, sink=sink)
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = f64(s.embed)
+    ids = s.ids.cpu().numpy()
+    worst = run_and_compare(s, LazyWeights(layers), Ks0, Vs0, [emb[ids[0]]], TOL[dtype])
+    s.close()
+    print("qk-norm", dtype, "worst", worst)
+
+
 def test_bf16_batch_of_sequences():
     """Independent sequences sharing weights (seq-major rows, per-sequence
     caches and plans)."""

@@ -7,6 +7,7 @@ equals a prefill of the edited sequence; packed equals interval-wise;
 degeneration of the biased operator), and invariants (unselected K/V rows
 untouched, RoPE relativity).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -380,3 +381,46 @@ def test_reposition_notes_sec5():
     Ks, _ = oracle.shift(K, V, 2, 3, theta)
     np.testing.assert_allclose(Ks[..., 2:, :], oracle.reposition(K[..., 5:, :], V[..., 5:, :], 5, 2, theta)[0],
                                atol=1e-12)
+
+
+def test_qk_norm_invariants():
+    """Q/K normalisation (Budgeted KV-Cache Repair, Sec. 13.2; the Qwen3
+    block): (1) with unit weights every stored key head has norm sqrt(d_h)
+    (the rotary map preserves norms); (2) scaling the Q and K rows of the
+    projection (and their bias) by any c > 0 leaves the layer unchanged."""
+    spec, W = tiny_model(81, L=1, bias=True)
+    spec = dataclasses.replace(spec, rms_eps=1e-12)
+    dh, Hq, Hkv = spec.head_dim, spec.n_q_heads, spec.n_kv_heads
+    for w in W:
+        w["q_norm"] = np.ones(dh)
+        w["k_norm"] = np.ones(dh)
+    rng = np.random.default_rng(82)
+    N = 20
+    X = rng.standard_normal((N, spec.d_model))
+    K = np.zeros((Hkv, N, dh))
+    V = np.zeros((Hkv, N, dh))
+    pos = np.arange(N)
+    out1 = oracle.layer_rows(spec, W[0], X, K, V, pos, None)
+    np.testing.assert_allclose(np.linalg.norm(K, axis=-1), np.sqrt(dh), rtol=1e-9)
+    # scale invariance, with non-unit weights
+    W[0]["q_norm"] = 1 + 0.2 * rng.standard_normal(dh)
+    W[0]["k_norm"] = 1 + 0.2 * rng.standard_normal(dh)
+    K1, V1 = np.zeros((Hkv, N, dh)), np.zeros((Hkv, N, dh))
+    ref = oracle.layer_rows(spec, W[0], X, K1, V1, pos, None)
+    Ws = dict(W[0])
+    qk = slice(0, (Hq + Hkv) * dh)
+    Ws["w_qkv"] = W[0]["w_qkv"].copy()
+    Ws["w_qkv"][qk] *= 7.5
+    Ws["b_qkv"] = W[0]["b_qkv"].copy()
+    Ws["b_qkv"][qk] *= 7.5
+    K2, V2 = np.zeros((Hkv, N, dh)), np.zeros((Hkv, N, dh))
+    out2 = oracle.layer_rows(spec, Ws, X, K2, V2, pos, None)
+    np.testing.assert_allclose(out2, ref, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(K2, K1, rtol=1e-9, atol=1e-12)
+    # without the per-head normalisation the same scaling changes the result
+    Wn = {k: v for k, v in Ws.items() if k not in ("q_norm", "k_norm")}
+    Wn0 = {k: v for k, v in W[0].items() if k not in ("q_norm", "k_norm")}
+    a = oracle.layer_rows(spec, Wn, X, np.zeros((Hkv, N, dh)), np.zeros((Hkv, N, dh)), pos, None)
+    b = oracle.layer_rows(spec, Wn0, X, np.zeros((Hkv, N, dh)), np.zeros((Hkv, N, dh)), pos, None)
+    assert np.max(np.abs(a - b)) > 1e-3
+    assert out1.shape == ref.shape
