@@ -64,11 +64,19 @@ __device__ __forceinline__ void item_coords(const GemmDev& g, int item, int& m_t
 // Persistent: one CTA per SM walks items blockIdx.x, +gridDim.x, ...  The TMA
 // ring runs across item boundaries, and the TMEM accumulator is double
 // buffered, so the epilogue of one item overlaps the main loop of the next.
+//
+// ATOMS (swizzle atoms per ring stage) is a compile-time constant so that the
+// MMA issue block is straight-line code: one elected lane issues the stage's
+// 4 * ATOMS instructions back to back from precomputed descriptors.  A single
+// thread's issue loop bounds narrow (N < 256) tiles, and runtime-shaped loops
+// around tcgen05.mma cost several times the issue time of the instructions.
+template <int ATOMS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmDev g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int BN = g.BN, stages = g.stages, atoms = g.atoms;
+    constexpr int atoms = ATOMS;
+    const int BN = g.BN, stages = g.stages;
     const int tileB = BN * 128;                    // one atom of B
     const int stA = atoms * kTileABytes, stB = atoms * tileB;
     uint8_t* sA = smem;
@@ -170,7 +178,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t idesc = idesc_bf16(128, BN, 0, 0);
         const uint64_t descA = sdesc_sw128(smem_u32(sA), 16, 1024);
         const uint64_t descB = sdesc_sw128(smem_u32(sB), 16, 1024);
-        int it = 0, local = 0;
+        constexpr uint32_t atA16 = kTileABytes >> 4, stA16 = atoms * atA16;   // descriptor units (16 B)
+        const uint32_t atB16 = (uint32_t)tileB >> 4, stB16 = atoms * atB16;
+        const bool leader = elect_one();    // the same lane issues every MMA and commit
+        int s = 0, local = 0;
+        uint32_t phase = 0;
         for (int item = blockIdx.x; ok && item < g.items; item += gridDim.x, ++local) {
             int m_t, n_t, split, kb0, kb1;
             item_coords(g, item, m_t, n_t, split, kb0, kb1);
@@ -181,26 +193,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)ab * acc_stride;
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int s = it % stages;
-                if (!warp_wait_all(&full[s], (uint32_t)(it / stages) & 1u)) {
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!warp_wait_all(&full[s], phase)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int a = 0; a < atoms; ++a) {
-                    const uint64_t da = descA + (uint64_t)(((uint32_t)s * stA + (uint32_t)a * kTileABytes) >> 4);
-                    const uint64_t db = descB + (uint64_t)(((uint32_t)s * stB + (uint32_t)a * tileB) >> 4);
+                if (leader) {
+                    const uint64_t da = descA + (uint64_t)((uint32_t)s * stA16);
+                    const uint64_t db = descB + (uint64_t)((uint32_t)s * stB16);
+                    const uint32_t first = kb > kb0 ? 1u : 0u;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_elect(d, da + 2u * kk, db + 2u * kk, idesc, (kb > kb0 || a > 0 || kk > 0) ? 1u : 0u);
+                    for (int a = 0; a < atoms; ++a)
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(d, da + (uint64_t)(a * atA16 + 2 * kk), db + (uint64_t)(a * atB16 + 2 * kk),
+                                     idesc, (a > 0 || kk > 0) ? 1u : first);
+                    mma_commit(&empty[s]);
                 }
-                mma_commit_elect(&empty[s]);
+                __syncwarp();
+                if (++s == stages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
             if (!ok) break;
-            mma_commit_elect(&acc_full[ab]);
+            if (leader) mma_commit(&acc_full[ab]);
+            __syncwarp();
         }
-        mma_commit_elect(mma_done);
+        if (leader) mma_commit(mma_done);
+        __syncwarp();
         warp_wait_all(mma_done, 0);
     } else {
         // ------------------------------------------------------------ epilogue
@@ -422,13 +444,17 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBudget);
-        if (e != cudaSuccess) return e;
+        for (auto* f : {gemm_bf16_tc_kernel<1>, gemm_bf16_tc_kernel<2>}) {
+            cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     const unsigned grid = (unsigned)std::min(g.items, kNumSMs);
-    KVR_LAUNCH(gemm_bf16_tc_kernel, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+    if (p.atoms == 2)
+        KVR_LAUNCH(gemm_bf16_tc_kernel<2>, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+    else
+        KVR_LAUNCH(gemm_bf16_tc_kernel<1>, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
     return cudaSuccess;
 }
 
