@@ -26,7 +26,9 @@ namespace {
 
 constexpr int kBK = 64;                 // K elements per swizzle atom (128 B of bf16)
 constexpr int kTileABytes = 128 * 128;  // 128 rows x 128 B: one atom of A
-constexpr int kGemmThreads = 192;       // warp0 TMA, warp1 MMA, warps2-5 epilogue
+constexpr int kEpiPer = 3;              // epilogue warps per TMEM lane quarter (store issue is the limit)
+constexpr int kEpiWarps = 4 * kEpiPer;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;   // warp0 TMA, warp1 MMA, warps 2.. epilogue
 constexpr int kSmemBudget = 227 * 1024;
 
 struct GemmDev {
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], kEpiWarps);
         }
         mbar_init(mma_done, 1);
         fence_mbar_init();
@@ -227,6 +229,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
+        // the warps of a lane quarter split its 16-column chunks between them
+        const int n_chunks = BN / 16, part = (warp - 2) >> 2, per = (n_chunks + kEpiPer - 1) / kEpiPer;
+        const int c_lo = 16 * min(n_chunks, part * per), c_hi = 16 * min(n_chunks, (part + 1) * per);
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int local = 0;
         for (int item = blockIdx.x; item < g.items; item += gridDim.x, ++local) {
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // TMEM -> fp32 partials part[split][token][feature]
                 const int feat = m_t * 128 + q * 32 + lane;
                 float* out = g.part + (size_t)split * g.R * g.n_out + feat;
-                for (int c = 0; c < BN; c += 16) {
+                for (int c = c_lo; c < c_hi; c += 16) {
                     float v[16];
                     tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool up_lane = lane >= 16;
                 const int f = m_t * 64 + q * 16 + (lane & 15);
                 __nv_bfloat16* act = g.act + f;
-                for (int c = 0; c < BN; c += 16) {
+                for (int c = c_lo; c < c_hi; c += 16) {
                     float v[16];
                     tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
