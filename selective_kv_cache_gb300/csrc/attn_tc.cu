@@ -315,19 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
             }
             const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-            // O is rescaled only after the previous PV has finished; P[j & 1] is
-            // rewritten only after the PV two tiles back (which read it) has
+            // O is rescaled only after the previous PV has finished.  P[j & 1]
+            // was last read by the PV two tiles back, which the MMA thread
+            // issued before S_j's QK product: the commit that signalled S_j
+            // covers it, so no wait is needed before P_j is written.
             const bool raise = mt > m_run + kRescale;
             const bool rescale = __any_sync(0xffffffffu, raise && j > 0);
             if (rescale) {
                 if (!warp_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            if (j >= 2) {
-                if (!warp_wait(&o_done[j & 1], (uint32_t)((j - 2) >> 1) & 1u)) {
                     ok = false;
                     break;
                 }
