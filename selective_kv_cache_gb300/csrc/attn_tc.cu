@@ -95,8 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* v_full = k_empty + kKStages;                // [kVStages]
     uint64_t* v_empty = v_full + kVStages;                // [kVStages]
     uint64_t* s_full = v_empty + kVStages;                // [2]
-    uint64_t* s_free = s_full + 2;                        // [2]
-    uint64_t* p_full = s_free + 2;                        // [2], per P buffer
+    uint64_t* p_full = s_full + 2;                        // [2], per P buffer
     uint64_t* o_done = p_full + 2;                        // [2], PV of tile j commits o_done[j & 1]
     uint64_t* mma_done = o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -135,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
             mbar_init(&p_full[i], 4);
             mbar_init(&o_done[i], 1);
         }
@@ -221,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](int j) -> bool {
                 const int kst = j % kKStages, sb = j & 1;
                 if (!mbar_wait(&k_full[kst], (uint32_t)(j / kKStages) & 1u)) return false;
-                if (j >= 2 && !mbar_wait(&s_free[sb], (uint32_t)((j - 2) >> 1) & 1u)) return false;
+                // S buffer sb was last read by the softmax of tile j - 2, whose P
+                // (written after that read) this thread has already waited for
                 tc_fence_after();
                 const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + kst * kTile;
 #pragma unroll
@@ -280,9 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             float s[128];
             tmem_ld32x4(tmem + lane_base + (uint32_t)sb * 128u, s);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[sb]);
 
             const int key0 = (jb + j) * 128;
             const bool masked = jb + j >= n_full;
