@@ -250,16 +250,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int tok0 = n_t * BN;
             const uint32_t src = tmem + lane_base + (uint32_t)ab * acc_stride;
             if (!g.swiglu_F) {
-                // TMEM -> fp32 partials part[split][token][feature]
-                const int feat = m_t * 128 + q * 32 + lane;
-                float* out = g.part + (size_t)split * g.R * g.n_out + feat;
+                // TMEM -> fp32 partials part[split][token][feature].  Lane l holds
+                // feature 4a + b (a = l / 4, b = l % 4) for 16 tokens; a 4 x 4
+                // transpose within each quad of lanes (two xor-shuffle stages)
+                // leaves lane l with features 4a..4a+3 of token 4i + b, stored
+                // as one 16-byte vector per 4 tokens.
+                const int b = lane & 3;
+                float* out = g.part + (size_t)split * g.R * g.n_out + m_t * 128 + q * 32 + (lane & ~3);
                 for (int c = c_lo; c < c_hi; c += 16) {
                     float v[16];
                     tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int tok = tok0 + c + j;
-                        if (tok < g.R) out[(size_t)tok * g.n_out] = v[j];
+                    for (int i = 0; i < 4; ++i) {
+                        float x0 = v[4 * i], x1 = v[4 * i + 1], x2 = v[4 * i + 2], x3 = v[4 * i + 3];
+                        float a0 = (b & 2) ? x0 : x2, a1 = (b & 2) ? x1 : x3;
+                        a0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+                        a1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+                        if (b & 2) { x0 = a0; x1 = a1; } else { x2 = a0; x3 = a1; }
+                        float c0 = (b & 1) ? x0 : x1, c1 = (b & 1) ? x2 : x3;
+                        c0 = __shfl_xor_sync(0xffffffffu, c0, 1);
+                        c1 = __shfl_xor_sync(0xffffffffu, c1, 1);
+                        if (b & 1) { x0 = c0; x2 = c1; } else { x1 = c0; x3 = c1; }
+                        const int tok = tok0 + c + 4 * i + b;
+                        if (tok < g.R) *reinterpret_cast<float4*>(out + (size_t)tok * g.n_out) = make_float4(x0, x1, x2, x3);
                     }
                 }
             } else {
