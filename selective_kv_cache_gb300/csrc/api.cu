@@ -313,6 +313,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.loc = c->d_eloc;
         a.snk = c->d_esnk;
         a.n_tiles = c->sel.n_tiles;
+        a.n_rows = c->sel.n_rows;
         a.n_q_heads = m.n_q_heads;
         a.n_kv_heads = m.n_kv_heads;
         a.head_dim = m.head_dim;
@@ -474,6 +475,23 @@ bool make_tmap_4d_bf16(CUtensorMap* out, const void* base, const uint64_t dims_i
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         if (why) *why = "cuTensorMapEncodeTiled (4-d) failed with " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+bool make_tmap_2d_f32_sw128(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                            std::string* why) {
+    if (!get_encode(why)) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled (fp32 rows) failed with " + std::to_string((int)r);
         return false;
     }
     return true;
@@ -1065,6 +1083,7 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
     a.loc = c->d_local;
     a.snk = c->d_sink;
     a.n_tiles = c->sel.n_tiles;
+    a.n_rows = c->sel.n_rows;
     a.n_q_heads = c->m.n_q_heads;
     a.n_kv_heads = c->m.n_kv_heads;
     a.head_dim = c->m.head_dim;

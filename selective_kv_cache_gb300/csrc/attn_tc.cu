@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "kvr_internal.h"
 #include "ptx.cuh"
@@ -85,7 +86,8 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int m, int c) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnLaunch a) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;                        // [2], per P buffer
     uint64_t* o_done = p_full + 2;                        // [2], PV of tile j commits o_done[j & 1]
     uint64_t* mma_done = o_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* q_full = mma_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
 
     const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
@@ -138,11 +141,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_done[i], 1);
         }
         mbar_init(mma_done, 1);
+        mbar_init(q_full, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
+        prefetch_tmap(&tmQ);
+        if (a.part_o) prefetch_tmap(&tmP);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -155,16 +161,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int p = m / G, gi = m % G;
     const bool row_valid = warp >= 2 && m < P * G && p < nrows;
     int g = umin;
-    if (warp >= 2) {
-        const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
-        if (row_valid) g = a.U[row0 + p];
-        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
-            st_shared_v4(tile_chunk(sbase + kOffQ, m, c), v);
+    if (row_valid) g = a.U[row0 + p];
+    // K/V producer: issue order K_0, K_1 V_0, K_2 V_1, ...: K stays one tile
+    // ahead of V.  The Q tile (two boxes of 64 dims x G heads x P positions,
+    // landing as rows p * G + i) and the first two steps go out before the
+    // block-wide barrier, under the tensor-memory allocation.
+    int k_issued = 0, v_issued = 0;
+    auto produce = [&](int t) -> bool {
+        if (t < n_total) {
+            const int st = t % kKStages;
+            if (!mbar_wait(&k_empty[st], ((uint32_t)(t / kKStages) & 1u) ^ 1u)) return false;
+            uint8_t* kd = smem + kOffK + st * kTile;
+            mbar_arrive_expect_tx(&k_full[st], kTile);
+            tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + t) * 128, head_index);
+            tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + t) * 128, head_index);
+            ++k_issued;
         }
-        fence_proxy_async_smem();
+        if (t >= 1) {
+            const int j = t - 1, st = j % kVStages;
+            if (!mbar_wait(&v_empty[st], ((uint32_t)(j / kVStages) & 1u) ^ 1u)) return false;
+            uint8_t* vd = smem + kOffV + st * kTile;
+            mbar_arrive_expect_tx(&v_full[st], kTile);
+            tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
+            tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
+            ++v_issued;
+        }
+        return true;
+    };
+    int t_prod = 0;
+    if (warp == 0 && lane == 0) {
+        // P * G <= 128 rows of 128 bytes in each half (126 when G = 6)
+        mbar_arrive_expect_tx(q_full, 2u * 128u * (uint32_t)(P * G));
+        tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, h * G, row0);
+        tma_load_3d(smem + kOffQ + kHalf, &tmQ, q_full, 64, h * G, row0);
+        for (; t_prod < 2 && t_prod <= n_total && ok; ++t_prod) ok = produce(t_prod);
     }
     tc_fence_before();
     __syncthreads();
@@ -175,36 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // issue order K_0, K_1 V_0, K_2 V_1, ...: K stays one tile ahead of V
         if (lane == 0) {
-            int k_issued = 0, v_issued = 0;
-            for (int t = 0; t <= n_total && ok; ++t) {
-                if (t < n_total) {
-                    const int st = t % kKStages;
-                    if (!mbar_wait(&k_empty[st], ((uint32_t)(t / kKStages) & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* kd = smem + kOffK + st * kTile;
-                    mbar_arrive_expect_tx(&k_full[st], kTile);
-                    tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + t) * 128, head_index);
-                    tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + t) * 128, head_index);
-                    ++k_issued;
-                }
-                if (t >= 1) {
-                    const int j = t - 1, st = j % kVStages;
-                    if (!mbar_wait(&v_empty[st], ((uint32_t)(j / kVStages) & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* vd = smem + kOffV + st * kTile;
-                    mbar_arrive_expect_tx(&v_full[st], kTile);
-                    tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
-                    tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
-                    ++v_issued;
-                }
-            }
+            for (int t = t_prod; t <= n_total && ok; ++t) ok = produce(t);
             if (!ok) {  // let every copy still in flight land before the CTA exits
+                mbar_wait(q_full, 0);
                 for (int j = (k_issued > kKStages ? k_issued - kKStages : 0); j < k_issued; ++j)
                     mbar_wait(&k_full[j % kKStages], (uint32_t)(j / kKStages) & 1u);
                 for (int j = (v_issued > kVStages ? v_issued - kVStages : 0); j < v_issued; ++j)
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&k_empty[kst]);
                 return true;
             };
-            if (n_total > 0) ok = issue_s(0);
+            if (n_total > 0) ok = mbar_wait(q_full, 0) && issue_s(0);
             for (int j = 0; ok && j < n_total; ++j) {
                 if (j + 1 < n_total && !issue_s(j + 1)) {
                     ok = false;
@@ -392,17 +396,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                // unnormalised fp32 partial plus (running max in base 2, sum) for the combine
+                // unnormalised fp32 partial plus (running max in base 2, sum) for
+                // the combine.  The warp's 32 rows go out as four TMA stores of
+                // 32 x 32 floats staged in the idle K ring (every QK product has
+                // completed: the last PV's commit covers them) in the 128-byte
+                // swizzle, which keeps the row-per-lane writes conflict-free.
                 tc_fence_after();
                 const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
-                float* po = a.part_o + (slot * 128 + m) * 128;
+                uint8_t* stg = smem + kOffK + (uint32_t)(warp & 3) * 16384u;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
                     tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        reinterpret_cast<float4*>(po + c * 16)[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+                    for (int t = 0; t < 4; ++t) {
+                        const int j = (c & 1) * 4 + t;   // 16-byte chunk within the box row
+                        const uint32_t addr = smem_u32(stg) + (uint32_t)(c >> 1) * 4096u + (uint32_t)lane * 128u +
+                                              ((uint32_t)(j ^ (lane & 7)) << 4);
+                        st_shared_v4(addr, make_uint4(__float_as_uint(o[4 * t]), __float_as_uint(o[4 * t + 1]),
+                                                      __float_as_uint(o[4 * t + 2]), __float_as_uint(o[4 * t + 3])));
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int cb = 0; cb < 4; ++cb)
+                        tma_store_2d(&tmP, stg + cb * 4096, cb * 32, (int)(slot * 128) + 32 * (warp & 3));
+                    bulk_commit();
+                    bulk_wait_all();
                 }
                 a.part_ml[(slot * 128 + m) * 2] = m_run;
                 a.part_ml[(slot * 128 + m) * 2 + 1] = l_run;
@@ -521,7 +542,19 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         attr = true;
     }
     dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
-    KVR_LAUNCH(attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, b);
+    // Q [rows][H_q][128] as (dims, heads, rows): a {64, G, 128 / G} box is one
+    // half of a query tile, rows p * G + i
+    CUtensorMap tq, tp;
+    const int G = a.n_q_heads / a.n_kv_heads;
+    if (a.n_rows <= 0 ||
+        !make_tmap_3d_bf16(&tq, a.q, 128, (uint64_t)a.n_q_heads, (uint64_t)a.n_rows, 256, (uint64_t)a.n_q_heads * 256,
+                           64, (uint32_t)G, (uint32_t)(128 / G), why))
+        return cudaErrorInvalidValue;
+    memset(&tp, 0, sizeof(tp));
+    if (n_split > 1 &&
+        !make_tmap_2d_f32_sw128(&tp, a.part_o, 128, (uint64_t)n_split * a.n_tiles * a.n_kv_heads * 128, 32, why))
+        return cudaErrorInvalidValue;
+    KVR_LAUNCH(attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
     if (n_split == 1) return cudaSuccess;
     const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
     KVR_LAUNCH(attn_combine_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, s, b, a.n_tiles,

@@ -91,6 +91,9 @@ bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t
 // 4-d: dims[0] innermost (elements), strides of dims 1-3 in bytes
 bool make_tmap_4d_bf16(CUtensorMap* out, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                        const uint32_t box[4], std::string* why);
+// fp32 rows x 128-byte boxes with the 128-byte swizzle (rows of `inner` floats)
+bool make_tmap_2d_f32_sw128(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                            std::string* why);
 
 // ---------------------------------------------------------------- launchers
 struct SelectLaunch {
@@ -205,6 +208,7 @@ struct AttnLaunch {
     const uint32_t* loc;       // [batch][words]
     const uint32_t* snk;
     int n_tiles, n_q_heads, n_kv_heads, head_dim, layer, n_layers, capacity, n_tokens, words, batch;
+    int n_rows;                // packed rows of q and out
     float alpha, beta;
     int32_t* err;
     float* part_o;             // nullable: split-K/V partials [splits][tiles][H_kv][128][128]
