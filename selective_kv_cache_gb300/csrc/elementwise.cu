@@ -223,8 +223,8 @@ __global__ void epi_down_kernel(const float* __restrict__ part, int splits, int 
 // ------------------------------------------------------------------ residual + RMSNorm, one CTA per row
 // Each thread keeps up to kRowChunks 8-element chunks of its row in registers
 // between the sum-of-squares pass and the normalisation.
-constexpr int kRowThreads = 256;
-constexpr int kRowChunks = 4;   // rows up to 256 * 4 * 8 = 8192 elements
+constexpr int kRowThreads = 512;   // one 8-element chunk a thread at d = 4096: every load in flight at once
+constexpr int kRowChunks = 2;   // rows up to 512 * 2 * 8 = 8192 elements
 
 __device__ __forceinline__ float row_rstd(float ss, int d, float eps) {
     __shared__ float red[kRowThreads / 32];
