@@ -342,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (raise) m_run = mt;
             // p = 2^(x - m): one packed FMA per two keys, then ex2; l sums the
-            // probabilities exactly as the PV product sees them (bf16)
+            // fp32 probabilities (the PV product sees them rounded to bf16: a
+            // relative difference of at most 2^-9 per term, unbiased)
             // P goes to tensor memory as the PV product's A operand: column c of
             // the row holds keys 2c, 2c+1 as packed bf16
             const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
@@ -356,9 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 16; ++t) {
                     const int k = 32 * c + 2 * t;
                     const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), sc, nm);
-                    pk[t] = pack_bf16(ex2(x.x), ex2(x.y));
-                    acc[t & 3] = __fadd2_rn(acc[t & 3], make_float2(__uint_as_float(pk[t] << 16),
-                                                                    __uint_as_float(pk[t] & 0xffff0000u)));
+                    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                    pk[t] = pack_bf16(e.x, e.y);
+                    acc[t & 3] = __fadd2_rn(acc[t & 3], e);
                 }
                 tmem_st16_async(ptm + 16u * (uint32_t)c, pk);
             }
