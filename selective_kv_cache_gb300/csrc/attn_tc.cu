@@ -287,11 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key0 = (jb + j) * 128;
             const bool masked = jb + j >= n_full;
             if (biased) {
+                // the mask words are the same for every row of the tile, so the
+                // branches are warp-uniform: words with no bit set cost nothing,
+                // all-local words one add per key
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const int wd = (key0 >> 5) + t;
                     const uint32_t lw = wd < a.words ? loc[wd] : 0u;
                     const uint32_t sw = wd < a.words ? snk[wd] : 0u;
+                    if ((lw | sw) == 0u) continue;
+                    if (sw == 0u && lw == 0xffffffffu) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) s[32 * t + k] += ar;
+                        continue;
+                    }
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         float b = ((lw >> k) & 1u) ? ar : 0.f;
