@@ -2,6 +2,7 @@
 // its query-tile geometry (the plan is built over these tiles): the
 // tensor-core kernel for bf16 models, the CUDA-core kernel for fp32 models.
 #include <algorithm>
+#include <functional>
 
 #include "kvr_internal.h"
 
@@ -17,24 +18,38 @@ size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_hea
     return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_split, n_tiles, n_kv_heads) : 0;
 }
 
-// Pick the chunk size C that minimises the modelled time: CTAs run one per
-// SM, a CTA costs ~6 tile-times of set-up plus one per K/V tile of its chunk,
-// and a launch takes ceil(CTAs / SMs) rounds of its longest chunk; a split
-// adds the merge.  tile_kv[t] = K/V tiles of query tile t.
+// Pick the chunk size C that minimises the modelled time.  The model plays
+// out the hardware's dispatch: CTAs go to the SMs in launch order (query tile
+// fastest, then K/V head, then split), each SM taking the next CTA when its
+// last one ends; a CTA costs ~6 tile-times of set-up plus one per K/V tile of
+// its chunk (an empty chunk almost nothing), and a split adds the merge.
+// tile_kv[t] = K/V tiles of query tile t.
 void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
     *chunk = 1 << 30;
     *n_split = 1;
     if (dtype != KVR_BF16 || tile_kv.empty()) return;
     int max_kv = 1;
     for (int v : tile_kv) max_kv = std::max(max_kv, v);
+    std::vector<double> sm_free;
+    auto makespan = [&](int C, int splits) {
+        // min-heap of the SMs' finish times
+        sm_free.assign(kNumSMs, 0.0);
+        std::greater<double> later;
+        for (int z = 0; z < splits; ++z)
+            for (int y = 0; y < n_kv_heads; ++y)
+                for (int v : tile_kv) {
+                    const int n = std::max(0, std::min(C, v - z * C));
+                    std::pop_heap(sm_free.begin(), sm_free.end(), later);
+                    sm_free.back() += n > 0 ? n + 6.0 : 0.3;
+                    std::push_heap(sm_free.begin(), sm_free.end(), later);
+                }
+        return *std::max_element(sm_free.begin(), sm_free.end());
+    };
     double best = 1e30;
     for (int C = max_kv; C >= 2; --C) {
-        long long ctas = 0;
-        for (int v : tile_kv) ctas += (long long)n_kv_heads * ((v + C - 1) / C);
         const int splits = (max_kv + C - 1) / C;
         if (splits > 1 && (long long)splits * (long long)tile_kv.size() * n_kv_heads > kAttnMaxSplitCTAs) break;
-        const long long rounds = (ctas + kNumSMs - 1) / kNumSMs;
-        const double t = (double)rounds * (std::min(C, max_kv) + 6.0) + (splits > 1 ? 2.0 : 0.0);
+        const double t = makespan(C, splits) + (splits > 1 ? 2.0 : 0.0);
         if (t < best * 0.98) {
             best = t;
             *chunk = C;
