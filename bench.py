@@ -283,6 +283,9 @@ def run_ours(args):
     if args.workload == "llama8b" and not args.no_matched:
         mw = matched_work()
 
+    # ---- the other configurations (block seams, adapter drift), on request
+    oc = other_configs() if args.other_configs else None
+
     # ---- CPU oracle baseline on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -293,13 +296,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random weights, "
         "token ids, embeddings and stale cache)",
-        "config": {"workload": f"{w.name}: Llama-3-8B-shaped stack (32 L, d 4096, 32/8 heads x 128, FFN 14336, "
-                   f"RoPE theta 5e5), N={w.n_tokens}, suffix [{w.suffix_start},{w.n_tokens}), "
-                   f"{rows} refreshed positions in units of 32-64 (5 % budget)",
+        "config": {"workload": describe(w, rows),
                    "rows": rows, "n_tokens": w.n_tokens, "layers": m.n_layers,
                    "refresh_latency_ms": round(ms_total / args.steps, 4),
                    "per_layer_latency_us": round(ms_total / args.steps / m.n_layers * 1e3, 2),
-                   "l2": "no flush: each step streams 14 GB of weights (> 129 MB L2)",
+                   "l2": f"no flush: each step streams {weight_gb(m):.1f} GB of weights (> 129 MB L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
@@ -312,12 +313,96 @@ def run_ours(args):
         "shift": shift,
         "sur_select": sur,
         "matched_work": mw,
+        "other_configs": oc,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
     s.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+FAMILY = {(4096, 32, 8, 14336): "Llama-3-8B-shaped", (3584, 28, 4, 18944): "Qwen2.5-7B-shaped",
+          (1536, 12, 2, 8960): "Qwen2.5-1.5B-shaped", (4096, 32, 8, 12288): "Qwen3-8B-shaped"}
+
+
+def describe(w, rows):
+    """The workload in words: model shape, cache, selection."""
+    m = w.model
+    kind = {"units": "in units of 32-64", "isolated": "isolated", "seams": "in seam windows",
+            "matched": "in matched intervals"}.get(w.selection, w.selection)
+    fam = FAMILY.get((m.d_model, m.n_q_heads, m.n_kv_heads, m.ffn_dim), "random-init")
+    return (f"{w.name}: {fam} stack, {m.n_layers} L, d {m.d_model}, {m.n_q_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
+            f"FFN {m.ffn_dim}, RoPE theta {m.rope_theta:g}{', q/k/v bias' if m.qkv_bias else ''}, "
+            f"batch {w.batch}, N={w.n_tokens}, suffix [{w.suffix_start},{w.n_tokens}), "
+            f"{rows} refreshed positions {kind}, alpha {w.alpha:g}, beta {w.beta:g}")
+
+
+def weight_gb(m):
+    """Weight bytes of the whole stack in GB."""
+    per_layer = (m.qkv_out + m.n_q_heads * m.head_dim) * m.d_model + 3 * m.ffn_dim * m.d_model
+    return per_layer * m.n_layers * (4 if m.dtype == "f32" else 2) / 1e9
+
+
+def other_configs():
+    """The block-seam repair (Qwen2.5-7B shape, 896 seam rows over 8
+    independently prefilled blocks of 2048, alpha -2, beta -4) and the
+    adapter-drift repair (Qwen2.5-1.5B shape, batch 4 x 32768, layers 10-14
+    over the whole 24576-token affected suffix from stored boundary states,
+    492 isolated rows per sequence elsewhere): CUDA events around select +
+    refresh on device-resident inputs, 5 and 3 repetitions after 2 and 1
+    warm-ups."""
+    import numpy as np
+    import torch
+
+    from selective_kv_cache_gb300 import workloads as wl
+    from selective_kv_cache_gb300.harness import Setup
+
+    def timed(fn, reps, warm):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    out = {}
+    w = wl.WORKLOADS["qwen7b_seam"]
+    s = Setup(w)
+    rows, _ = s.select()
+
+    def seam():
+        s.select()
+        s.refresh()
+
+    ms = timed(seam, 5, 2)
+    s.sync()
+    out["qwen7b_seam"] = {"workload": describe(w, rows), "ms_per_refresh": round(ms, 3),
+                          "refreshed_tokens_per_s": round(rows / ms * 1e3, 1)}
+    s.close()
+    del s
+    torch.cuda.empty_cache()
+    w = wl.WORKLOADS["qwen1p5b_drift"]
+    s = Setup(w)
+    g = torch.Generator(device="cuda").manual_seed(w.seed(11))
+    boundary = torch.randn((w.batch, w.capacity, w.model.d_model), device="cuda", generator=g).to(
+        w.model.torch_dtype)
+    r0, r1 = w.range_layers
+    ms = timed(lambda: s.refresh_range(boundary, r0, r1), 3, 1)
+    s.sync()
+    rows = int(np.sum(s.counts))
+    full = w.batch * (w.n_tokens - w.suffix_start)
+    row_layers = rows * (w.model.n_layers - (r1 - r0)) + full * (r1 - r0)
+    out["qwen1p5b_drift"] = {"workload": describe(w, rows) + f"; layers [{r0},{r1}) over all {full} suffix rows",
+                             "ms_per_repair": round(ms, 2), "row_layers_per_s": round(row_layers / ms * 1e3, 1)}
+    s.close()
+    del s
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_shift(w, hbm_peak, reps=10):
@@ -599,6 +684,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the packed vs interval-wise comparison")
     ap.add_argument("--no-matched", action="store_true", help="skip the matched-work benchmark (Qwen3-8B shape)")
+    ap.add_argument("--other-configs", action="store_true",
+                    help="also time the block-seam and adapter-drift repairs (key other_configs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
