@@ -474,7 +474,8 @@ kvr_status kvr_cache_info(kvr_cache* c, int32_t* n_tokens, int32_t* suffix_start
 /* ---------------------------------------------------------------------------
  * Per-kernel timing.  When enabled, every launch of a library kernel on the
  * call's stream is bracketed by CUDA events; kvr_profile_read returns, per
- * kernel class (KVR_K_* below), the number of launches and the summed device
+ * kernel class (KVR_K_* below), the number of kernel launches (the attention
+ * class counts its split merge too) and the summed device
  * time in milliseconds since the last read (synchronous), and resets them.
  * ------------------------------------------------------------------------- */
 enum {

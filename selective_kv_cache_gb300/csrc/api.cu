@@ -129,6 +129,7 @@ struct Prof {
     int kind;
     cudaStream_t s;
     cudaEvent_t a = nullptr;
+    int launches = 1;   // kernels launched inside the scope
     Prof(kvr_cache* c_, int k, cudaStream_t s_) : c(c_), kind(k), s(s_) {
         if (c->profiling) {
             a = take_event(c);
@@ -139,7 +140,7 @@ struct Prof {
         if (a) {
             cudaEvent_t b = take_event(c);
             cudaEventRecord(b, s);
-            c->prof.push_back({kind, a, b});
+            c->prof.push_back({kind, a, b, launches});
         }
     }
 };
@@ -327,6 +328,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.beta = c->beta;
         a.err = c->d_err;
         set_attention_scratch(&a, part, L.part_size, c);
+        p.launches = attention_launches(dt, a);
         cudaError_t e = launch_attention(dt, a, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     }
@@ -1100,6 +1102,7 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
         set_attention_scratch(&a, static_cast<float*>(workspace), ws_bytes, c);
     std::string why;
     Prof p(c, KVR_K_ATTN, s);
+    p.launches = attention_launches(c->m.dtype, a);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);
     if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     return KVR_OK;
@@ -1203,7 +1206,7 @@ kvr_status kvr_profile_read(kvr_cache* c, double* ms, int64_t* launches, int32_t
         float t = 0.f;
         cudaEventElapsedTime(&t, r.a, r.b);
         c->prof_ms[r.kind] += t;
-        c->prof_n[r.kind] += 1;
+        c->prof_n[r.kind] += r.launches;
         c->ev_pool.push_back(r.a);
         c->ev_pool.push_back(r.b);
     }

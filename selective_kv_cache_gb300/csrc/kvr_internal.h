@@ -36,7 +36,9 @@ struct Selection {
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
+    int launches;   // kernels launched between the two events
 };
+
 
 struct kvr_cache_impl {
     kvr_model_desc m{};
@@ -217,6 +219,10 @@ struct AttnLaunch {
     int n_split;               // CTAs per (query tile, K/V head); 1 = unsplit
 };
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why);
+// kernels one attention call launches (the split merge is a second one)
+inline int attention_launches(int dtype, const AttnLaunch& a) {
+    return (dtype == KVR_BF16 && a.part_o && a.n_split > 1) ? 2 : 1;
+}
 // Query tile geometry of the attention kernel for a model.
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile);
 // Split of each query tile's K/V range over CTAs, from the per-tile K/V tile
