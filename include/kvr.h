@@ -30,6 +30,9 @@
  *   - Arguments are validated on the host before anything is enqueued; a
  *     failed validation enqueues nothing and leaves the cache unchanged.
  *   - After any error the cache can still be destroyed.
+ *   - KVR_PDL=0 in the environment (read once per process) turns off
+ *     programmatic dependent launch between the kernels of a call; it
+ *     changes how work is launched, never what it computes.
  */
 #ifndef KVR_H
 #define KVR_H
