@@ -12,15 +12,18 @@
 // of them read the same K/V tiles and one causal limit g_p serves a whole
 // group.  Per 128-key tile:
 //   warp 0      TMA: K and V tiles (two 64-column boxes each, 128-B swizzle)
-//               into a 2-stage ring; keys >= n_tokens arrive as zeros;
-//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers,
-//               then O += P V into the TMEM output accumulator (V read
-//               MN-major straight from its cache layout);
+//               into 3-stage rings, K one tile ahead of V; keys >= n_tokens
+//               arrive as zeros;
+//   warp 1      tcgen05.mma: S = Q K^T into one of three TMEM score buffers,
+//               up to three tiles ahead of the PV product;
+//   warp 6      tcgen05.mma: O += P V into the TMEM output accumulator (V
+//               read MN-major straight from its cache layout);
 //   warps 2-5   one thread per row: scores from TMEM, scale + bias + causal
 //               mask, online softmax in base 2 (the running max is only
 //               raised, and O rescaled in TMEM, when it grows by more than
-//               2^8, so P stays <= 256), P as bf16 into shared memory for the
-//               PV product; at the end O / l to global memory.
+//               2^8, so P stays <= 256), P as bf16 pairs over the tile's
+//               scores in TMEM, the A operand of the PV product; at the end
+//               O / l to global memory, or an fp32 partial for the merge.
 // Tiles below the plan's n_full are wholly visible to every row and skip the
 // causal test.  Every wait is bounded; on a timeout the CTA records the error,
 // drains its copies and MMAs, frees TMEM and returns.
@@ -35,18 +38,19 @@
 namespace kvr {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
-constexpr int kKStages = 3;                     // K runs one tile ahead of V: S needs K first
-constexpr int kVStages = 3;
+constexpr int kStages = 3;                      // K and V ring depth; K runs one tile ahead of V
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTile;
-constexpr uint32_t kOffV = kOffK + kKStages * kTile;
-constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
-constexpr uint32_t kTmemO = 256;                 // TMEM columns: S[0] 0-127, S[1] 128-255, O 256-383,
-constexpr uint32_t kTmemP = 384;                 // P[0] 384-447, P[1] 448-511 (bf16 pairs)
+constexpr int kSBufs = 3;                       // score buffers: the QK product runs two tiles ahead
+// TMEM columns: S[b] at 128 b (P, bf16 pairs, over its first 64 once the
+// scores are read), O 384-511
+constexpr uint32_t kTmemO = 384;
 constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
 
 // max of three (one instruction on sm_100 and later)
@@ -92,14 +96,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* k_full = bars + 0;                          // [kKStages]
-    uint64_t* k_empty = k_full + kKStages;                // [kKStages]
-    uint64_t* v_full = k_empty + kKStages;                // [kVStages]
-    uint64_t* v_empty = v_full + kVStages;                // [kVStages]
-    uint64_t* s_full = v_empty + kVStages;                // [2]
-    uint64_t* p_full = s_full + 2;                        // [2], per P buffer
-    uint64_t* o_done = p_full + 2;                        // [2], PV of tile j commits o_done[j & 1]
-    uint64_t* mma_done = o_done + 2;
+    // kv_full[t % 3]: producer step t, K_t and V_{t-1}; s_full[j % 3]: scores
+    // of tile j; p_full[j & 3]: P of tile j; o_done[j & 3]: PV of tile j.
+    // Four P and O phases keep every waiter ahead of the next completion of
+    // the barrier it polls.
+    uint64_t* kv_full = bars + 0;                         // [kStages]
+    uint64_t* s_full = kv_full + kStages;                 // [kSBufs]
+    uint64_t* p_full = s_full + kSBufs;                   // [4]
+    uint64_t* o_done = p_full + 4;                        // [4]
+    uint64_t* mma_done = o_done + 4;                      // both MMA issuers' last products
     uint64_t* q_full = mma_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
 
@@ -127,20 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kKStages; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
-        }
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&o_done[i], 1);
-        }
-        mbar_init(mma_done, 1);
+        for (int i = 0; i < kStages; ++i) mbar_init(&kv_full[i], 1);
+        for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 4);
+        for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
+        mbar_init(mma_done, 2);
         mbar_init(q_full, 1);
         fence_mbar_init();
     }
@@ -159,33 +155,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of this thread (softmax warps): m = 32 * (warp % 4) + lane
     const int m = 32 * (warp & 3) + lane;
     const int p = m / G, gi = m % G;
-    const bool row_valid = warp >= 2 && m < P * G && p < nrows;
+    const bool row_valid = warp >= 2 && warp < 6 && m < P * G && p < nrows;
     int g = umin;
     if (row_valid) g = a.U[row0 + p];
-    // K/V producer: issue order K_0, K_1 V_0, K_2 V_1, ...: K stays one tile
-    // ahead of V.  The Q tile (two boxes of 64 dims x G heads x P positions,
-    // landing as rows p * G + i) and the first two steps go out before the
-    // block-wide barrier, under the tensor-memory allocation.
-    int k_issued = 0, v_issued = 0;
+    // K/V producer, steps t = 0 .. n_total: K_t and V_{t-1} on one barrier,
+    // so K stays one tile ahead of V.  The ring slots are freed by the
+    // signals the products already send: K_t replaces K_{t-3}, read by the
+    // QK product of tile t - 3 (s_full); V_{t-1} replaces V_{t-4}, read by the
+    // PV product of tile t - 4 (o_done).  The Q tile (two boxes of 64 dims x
+    // G heads x P positions, landing as rows p * G + i) and the first two
+    // steps go out before the block-wide barrier, under the tensor-memory
+    // allocation.
+    int issued = 0;
     auto produce = [&](int t) -> bool {
+        const int st = t % kStages;
+        if (t >= kStages) {
+            // The slot's barrier finished its previous phase (step t - 3), and
+            // every thread that polls that phase has seen it: the QK issuer
+            // (its product S_{t-3} is done, which also frees K_{t-3}'s slot)
+            // and the PV issuer (its product of tile t - 4 is done, which
+            // frees V_{t-4}'s slot).  Only then is the barrier re-armed.
+            if (!mbar_wait(&kv_full[st], (uint32_t)((t - kStages) / kStages) & 1u) ||
+                !mbar_wait(&s_full[(t - 3) % kSBufs], (uint32_t)((t - 3) / kSBufs) & 1u))
+                return false;
+            if (t >= 4 && !mbar_wait(&o_done[(t - 4) & 3], (uint32_t)((t - 4) >> 2) & 1u)) return false;
+        }
+        mbar_arrive_expect_tx(&kv_full[st], (t < n_total ? kTile : 0u) + (t >= 1 ? kTile : 0u));
         if (t < n_total) {
-            const int st = t % kKStages;
-            if (!mbar_wait(&k_empty[st], ((uint32_t)(t / kKStages) & 1u) ^ 1u)) return false;
             uint8_t* kd = smem + kOffK + st * kTile;
-            mbar_arrive_expect_tx(&k_full[st], kTile);
-            tma_load_3d(kd, &tmK, &k_full[st], 0, (jb + t) * 128, head_index);
-            tma_load_3d(kd + kHalf, &tmK, &k_full[st], 64, (jb + t) * 128, head_index);
-            ++k_issued;
+            tma_load_3d(kd, &tmK, &kv_full[st], 0, (jb + t) * 128, head_index);
+            tma_load_3d(kd + kHalf, &tmK, &kv_full[st], 64, (jb + t) * 128, head_index);
         }
         if (t >= 1) {
-            const int j = t - 1, st = j % kVStages;
-            if (!mbar_wait(&v_empty[st], ((uint32_t)(j / kVStages) & 1u) ^ 1u)) return false;
-            uint8_t* vd = smem + kOffV + st * kTile;
-            mbar_arrive_expect_tx(&v_full[st], kTile);
-            tma_load_3d(vd, &tmV, &v_full[st], 0, (jb + j) * 128, head_index);
-            tma_load_3d(vd + kHalf, &tmV, &v_full[st], 64, (jb + j) * 128, head_index);
-            ++v_issued;
+            uint8_t* vd = smem + kOffV + ((t - 1) % kStages) * kTile;
+            tma_load_3d(vd, &tmV, &kv_full[st], 0, (jb + t - 1) * 128, head_index);
+            tma_load_3d(vd + kHalf, &tmV, &kv_full[st], 64, (jb + t - 1) * 128, head_index);
         }
+        ++issued;
         return true;
     };
     int t_prod = 0;
@@ -209,55 +215,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = t_prod; t <= n_total && ok; ++t) ok = produce(t);
             if (!ok) {  // let every copy still in flight land before the CTA exits
                 mbar_wait(q_full, 0);
-                for (int j = (k_issued > kKStages ? k_issued - kKStages : 0); j < k_issued; ++j)
-                    mbar_wait(&k_full[j % kKStages], (uint32_t)(j / kKStages) & 1u);
-                for (int j = (v_issued > kVStages ? v_issued - kVStages : 0); j < v_issued; ++j)
-                    mbar_wait(&v_full[j % kVStages], (uint32_t)(j / kVStages) & 1u);
+                for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
+                    mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 6) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads feed the tensor pipe: warp 1 the score products S_j =
+        // Q K_j^T, warp 6 the output products O += P_j V_j.  An issuing thread
+        // stalls while the pipe's short queue is full, so while one waits on a
+        // barrier the other keeps the pipe busy.  The scores run up to three
+        // tiles ahead: S_j goes into buffer j % 3 once the PV product of tile
+        // j - 3 has read the P stored over that buffer's scores.  Each thread
+        // commits its own products.
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
-            const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);   // V is MN-major
-            auto issue_s = [&](int j) -> bool {
-                const int kst = j % kKStages, sb = j & 1;
-                if (!mbar_wait(&k_full[kst], (uint32_t)(j / kKStages) & 1u)) return false;
-                // S buffer sb was last read by the softmax of tile j - 2, whose P
-                // (written after that read) this thread has already waited for
-                tc_fence_after();
-                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + kst * kTile;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16(tmem + (uint32_t)sb * 128u, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                             idesc_s, kk > 0);
-                }
-                mma_commit(&s_full[sb]);
-                mma_commit(&k_empty[kst]);
-                return true;
+            auto step_landed = [&](int t) {
+                return mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u);
             };
-            if (n_total > 0) ok = mbar_wait(q_full, 0) && issue_s(0);
-            for (int j = 0; ok && j < n_total; ++j) {
-                if (j + 1 < n_total && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                const int st = j % kVStages;
-                if (!mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u) ||
-                    !mbar_wait(&v_full[st], (uint32_t)(j / kVStages) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t pt = tmem + kTmemP + (uint32_t)(j & 1) * 64u, va = sbase + kOffV + st * kTile;
+            if (warp == 1) {
+                const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+                if (n_total > 0) ok = mbar_wait(q_full, 0);
+                for (int j = 0; ok && j < n_total; ++j) {
+                    if (!step_landed(j) ||   // K_j
+                        (j >= kSBufs && !mbar_wait(&o_done[(j - kSBufs) & 3], (uint32_t)((j - kSBufs) >> 2) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + (uint32_t)(j % kStages) * kTile;
+                    const uint32_t d = tmem + (uint32_t)(j % kSBufs) * 128u;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)kk * 8u, sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024),
-                                idesc_o, (j > 0 || kk > 0));
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+                        mma_bf16(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+                    }
+                    mma_commit(&s_full[j % kSBufs]);
                 }
-                mma_commit(&o_done[j & 1]);
-                mma_commit(&v_empty[st]);
+            } else {
+                const uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);   // V is MN-major
+                for (int j = 0; ok && j < n_total; ++j) {
+                    if (!mbar_wait(&p_full[j & 3], (uint32_t)(j >> 2) & 1u) || !step_landed(j + 1)) {   // P_j, V_j
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // O += P V_j: P over the scores of tile j
+                    const uint32_t pt = tmem + (uint32_t)(j % kSBufs) * 128u;
+                    const uint32_t va = sbase + kOffV + (uint32_t)(j % kStages) * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)kk * 8u,
+                                    sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
+                    }
+                    mma_commit(&o_done[j & 3]);
+                }
             }
             mma_commit(mma_done);
             mbar_wait(mma_done, 0);
@@ -274,9 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* snk = a.snk + (size_t)seq * a.words;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         float m_run = -INFINITY, l_run = 0.f;
+        // S_j is probed without blocking while tile j - 1 is still being
+        // worked on, so the probe's latency hides behind that work; the
+        // blocking wait runs only if some lane saw the scores not yet there.
+        bool s_ready = false;
         for (int j = 0; j < n_total; ++j) {
-            const int sb = j & 1;
-            if (!warp_wait(&s_full[sb], (uint32_t)(j >> 1) & 1u)) {
+            const int sb = j % kSBufs;
+            if (__any_sync(0xffffffffu, !s_ready) && !warp_wait(&s_full[sb], (uint32_t)(j / kSBufs) & 1u)) {
                 ok = false;
                 break;
             }
@@ -324,14 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
             }
             const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-            // O is rescaled only after the previous PV has finished.  P[j & 1]
-            // was last read by the PV two tiles back, which the MMA thread
-            // issued before S_j's QK product: the commit that signalled S_j
-            // covers it, so no wait is needed before P_j is written.
+            s_ready = j + 1 < n_total && mbar_test(&s_full[(j + 1) % kSBufs], (uint32_t)((j + 1) / kSBufs) & 1u);
+            // O is rescaled only after the previous PV has finished.  P_j goes
+            // over the scores just read; the buffer's earlier P (tile j - 3)
+            // was read before S_j's product was issued, so P_j needs no wait.
             const bool raise = mt > m_run + kRescale;
             const bool rescale = __any_sync(0xffffffffu, raise && j > 0);
             if (rescale) {
-                if (!warp_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) {
+                if (!warp_wait(&o_done[(j - 1) & 3], (uint32_t)((j - 1) >> 2) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P goes to tensor memory as the PV product's A operand: column c of
             // the row holds keys 2c, 2c+1 as packed bf16
             const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
-            const uint32_t ptm = tmem + lane_base + kTmemP + (uint32_t)(j & 1) * 64u;
+            const uint32_t ptm = tmem + lane_base + (uint32_t)sb * 128u;
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
 #pragma unroll
@@ -378,10 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run += a03.x + a03.y;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[j & 1]);
+            if (lane == 0) mbar_arrive(&p_full[j & 3]);
         }
         if (ok && n_total > 0) {
-            if (!warp_wait(&o_done[(n_total - 1) & 1], (uint32_t)((n_total - 1) >> 1) & 1u)) {
+            if (!warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u)) {
                 ok = false;
             } else if (n_split == 1) {
                 tc_fence_after();
@@ -433,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cb = 0; cb < 4; ++cb)
                         tma_store_2d(&tmP, stg + cb * 4096, cb * 32, (int)(slot * 128) + 32 * (warp & 3));
                     bulk_commit();
-                    bulk_wait_all();
+                    bulk_wait_read_all();   // the staging may be released; the writes land before the grid ends
                 }
                 a.part_ml[(slot * 128 + m) * 2] = m_run;
                 a.part_ml[(slot * 128 + m) * 2 + 1] = l_run;
