@@ -83,12 +83,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// address of 16-byte chunk c (0..15, 8 elements each) of row m in a 128 x 128
-// bf16 tile stored as two K-major 128-B-swizzled halves
-__device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int m, int c) {
-    return base + (uint32_t)(c >> 3) * kHalf + (uint32_t)m * 128u + ((uint32_t)((c & 7) ^ (m & 7)) << 4);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
