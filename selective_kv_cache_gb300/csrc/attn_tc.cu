@@ -83,6 +83,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// kBiased: the alpha/beta logit bias is on (the mask words are read); the
+// unbiased instance carries none of that code.
+template <bool kBiased>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -inf past the row's causal limit
         const float sl2 = 1.4426950408889634f / sqrtf(128.0f);
         const float ar = a.alpha * sqrtf(128.0f), br = a.beta * sqrtf(128.0f);
-        const bool biased = a.alpha != 0.f || a.beta != 0.f;
+        constexpr bool biased = kBiased;
         const uint32_t* loc = a.loc + (size_t)seq * a.words;
         const uint32_t* snk = a.snk + (size_t)seq * a.words;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -283,6 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // worked on, so the probe's latency hides behind that work; the
         // blocking wait runs only if some lane saw the scores not yet there.
         bool s_ready = false;
+        // mask words of the tile, loaded one tile ahead so their latency hides
+        // behind the previous tile's work
+        uint32_t lw[4] = {0u, 0u, 0u, 0u}, sw[4] = {0u, 0u, 0u, 0u};
+        auto load_words = [&](int key0, uint32_t* l, uint32_t* k) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int wd = (key0 >> 5) + t;
+                l[t] = wd < a.words ? loc[wd] : 0u;
+                k[t] = wd < a.words ? snk[wd] : 0u;
+            }
+        };
+        if (biased && n_total > 0) load_words(jb * 128, lw, sw);
         for (int j = 0; j < n_total; ++j) {
             const int sb = j % kSBufs;
             if (__any_sync(0xffffffffu, !s_ready) && !warp_wait(&s_full[sb], (uint32_t)(j / kSBufs) & 1u)) {
@@ -301,19 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // all-local words one add per key
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const int wd = (key0 >> 5) + t;
-                    const uint32_t lw = wd < a.words ? loc[wd] : 0u;
-                    const uint32_t sw = wd < a.words ? snk[wd] : 0u;
-                    if ((lw | sw) == 0u) continue;
-                    if (sw == 0u && lw == 0xffffffffu) {
+                    if ((lw[t] | sw[t]) == 0u) continue;
+                    if (sw[t] == 0u && lw[t] == 0xffffffffu) {
 #pragma unroll
                         for (int k = 0; k < 32; ++k) s[32 * t + k] += ar;
                         continue;
                     }
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        float b = ((lw >> k) & 1u) ? ar : 0.f;
-                        b += ((sw >> k) & 1u) ? br : 0.f;
+                        float b = ((lw[t] >> k) & 1u) ? ar : 0.f;
+                        b += ((sw[t] >> k) & 1u) ? br : 0.f;
                         s[32 * t + k] += b;
                     }
                 }
@@ -334,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
             s_ready = j + 1 < n_total && mbar_test(&s_full[(j + 1) % kSBufs], (uint32_t)((j + 1) / kSBufs) & 1u);
+            if (biased && j + 1 < n_total) load_words(key0 + 128, lw, sw);
             // O is rescaled only after the previous PV has finished.  P_j goes
             // over the scores just read; the buffer's earlier P (tile j - 3)
             // was read before S_j's product was issued, so P_j needs no wait.
@@ -555,9 +568,10 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
+        for (auto* f : {attn_tc_kernel<false>, attn_tc_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         attr = true;
     }
     dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
@@ -573,7 +587,10 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
     if (n_split > 1 &&
         !make_tmap_2d_f32_sw128(&tp, a.part_o, 128, (uint64_t)n_split * a.n_tiles * a.n_kv_heads * 128, 32, why))
         return cudaErrorInvalidValue;
-    KVR_LAUNCH(attn_tc_kernel, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
+    if (a.alpha != 0.f || a.beta != 0.f)
+        KVR_LAUNCH(attn_tc_kernel<true>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
+    else
+        KVR_LAUNCH(attn_tc_kernel<false>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
     if (n_split == 1) return cudaSuccess;
     const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
     KVR_LAUNCH(attn_combine_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, s, b, a.n_tiles,
