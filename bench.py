@@ -113,7 +113,7 @@ def ncu_traffic(kernel_class, sha):
     return None
 
 
-# per-kernel algorithmic work at the workload (measurement)
+# per-kernel algorithmic work at the workload: bytes and FLOPs per launch from the model shape
 def algorithmic(shape, R, M_pairs_per_head, u_max):
     """Algorithmic FLOPs and bytes per launch of each kernel class for R packed
     rows: a projection reads its weights once and the rows once and writes
