@@ -266,7 +266,8 @@ kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, 
  *   (kvr_workspace_bytes(c, 0) > 64 MiB) is rejected with EINVAL before
  *   anything is enqueued.
  *   The first call on a device looks up the array's address; make that call
- *   before any stream capture on the device.  Calls share the array: calls
+ *   before any stream capture on the device.  The cache's device must be the
+ *   current device (else EINVAL).  Calls share the array: calls
  *   whose GPU work overlaps race on it and must be serialised by the caller.
  *   The array keeps the last call's contents; a layer never reads scratch it
  *   has not written in the same call.

@@ -18,7 +18,9 @@
 //     need; the Llama-3-8B-shaped refresh of 282 rows needs about 55 MB).
 //   - The first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and keeps it; make
-//     that first call before any stream capture on that device.
+//     that first call before any stream capture on that device.  A call
+//     whose current device is not the cache's device is rejected with
+//     KVR_EINVAL.
 //   - Every call shares the one array.  Calls whose GPU work overlaps (other
 //     streams, other threads, other caches) race on it: serialise them.
 //   - The array keeps whatever the last call left in it.  Nothing in a layer
@@ -74,6 +76,18 @@ extern "C" kvr_status kvr_refresh_layer_noalloc(kvr_cache* c, int32_t layer, con
     if (!c->sel.valid) {
         set_error("no selection: call kvr_select first");
         return KVR_ESTATE;
+    }
+    // the array's address is looked up on the current device; the layer's
+    // kernels work on the cache's buffers, which live on the device the
+    // cache was created on
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != c->device) {
+        set_error("kvr_refresh_layer_noalloc: the current device (" + std::to_string(dev) +
+                  ") is not the device the cache was created on (" + std::to_string(c->device) +
+                  "); make that device current first");
+        return KVR_EINVAL;
     }
     const size_t need = kvr_workspace_bytes(c, 0);
     if (need > kNoAllocScratchBytes) {

@@ -6,6 +6,10 @@ Llama-shaped full-size test), so each run is checked on outputs the oracle can
 compute from the inputs alone, plus properties that hold at any size:
   - layer 0's written K/V rows (their inputs are the gathered embedding rows)
     elementwise against the oracle's layer 0;
+  - the refreshed rows after layer 0 (X^1, from a run of layer 0 alone)
+    elementwise against the oracle's layer 0: they pass through the biased
+    attention over the whole cache, the output projection and the MLP, and
+    depend on the inputs alone, so no GPU value enters the oracle;
   - every K/V row outside the refreshed set bit-identical to the input cache;
   - the metadata commit bit-exact; every refreshed value finite."""
 import dataclasses
@@ -35,9 +39,19 @@ def layer0_oracle(s, seq, rows, alpha, beta, sink_static=False, weights=None):
     W = LazyWeights(weights if weights is not None else s.layers)
     K0 = f64(s.K_in[seq, :1])
     V0 = f64(s.V_in[seq, :1])
-    _, K, V, _, _ = oracle.refresh_packed(spec, W, K0, V0, s.local_mask[seq], s.sink_mask[seq], U, X_src, alpha,
-                                          beta, sink_static, n_layers=1)
-    return U, K[0], V[0]
+    X1, K, V, _, _ = oracle.refresh_packed(spec, W, K0, V0, s.local_mask[seq], s.sink_mask[seq], U, X_src, alpha,
+                                           beta, sink_static, n_layers=1)
+    return U, K[0], V[0], X1
+
+
+def run_layer0(s, flags=0):
+    """Layer 0 alone on the current selection; returns the refreshed rows X^1.
+    It writes only layer 0's selected K/V rows, which a later full refresh
+    rewrites before reading them, so the full run's results do not change."""
+    s.select()
+    s.refresh(0, 1, flags=flags)
+    s.sync()
+    return f64(s.hidden[:s.n_rows])
 
 
 def check_untouched(s, seq, layer, rows):
@@ -55,12 +69,14 @@ def test_fragmented_packed_and_interval_wise_full_size():
     a.K_in, a.V_in = a.K.clone(), a.V.clone()
     b = Setup(w, weights=a.layers, cache=(a.K_in.clone(), a.V_in.clone()))
     b.K_in, b.V_in = a.K_in, a.V_in
+    X1_gpu = run_layer0(a)
     a.select()
     a.refresh()
     a.sync()
     n_iv = b.refresh_interval_wise()
     b.sync()
-    U, K0, V0 = layer0_oracle(a, 0, a.positions[0], 0.0, 0.0)
+    U, K0, V0, X1 = layer0_oracle(a, 0, a.positions[0], 0.0, 0.0)
+    assert_close(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0")
     assert n_iv == oracle.intervals(U).shape[0] and n_iv > 250
     Ut = torch.from_numpy(U)
     for s in (a, b):
@@ -85,11 +101,13 @@ def test_block_seam_full_size(sink_static):
     w = wl.WORKLOADS["qwen7b_seam"]
     s = Setup(w, flags=kvr.KVR_SINK_STATIC if sink_static else 0)
     s.K_in, s.V_in = s.K.clone(), s.V.clone()
+    X1_gpu = run_layer0(s)
     rows, ivs = s.select()
     assert rows == 896 and ivs == 8
     s.refresh()
     s.sync()
-    U, K0, V0 = layer0_oracle(s, 0, s.positions[0], w.alpha, w.beta, sink_static)
+    U, K0, V0, X1 = layer0_oracle(s, 0, s.positions[0], w.alpha, w.beta, sink_static)
+    assert_close(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0 (alpha/beta bias, 7 heads per K/V head)")
     Ut = torch.from_numpy(U)
     assert_close(f64(s.K[0, 0][:, Ut]), K0[:, U], TOL["bf16"], "K layer 0")
     assert_close(f64(s.V[0, 0][:, Ut]), V0[:, U], TOL["bf16"], "V layer 0")
@@ -133,6 +151,7 @@ def test_adapter_drift_full_size():
         L["w_qkv"] = None
     s = Setup(w, weights=merged)
     s.K_in, s.V_in = s.K.clone(), s.V.clone()
+    X1_gpu = run_layer0(s)      # the 492 isolated rows per sequence, through layer 0 under the merged adapter
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed(6) * 1000 + 7)
     boundary = torch.empty((w.batch, w.capacity, w.model.d_model), device="cuda", dtype=torch.float32)
@@ -144,9 +163,12 @@ def test_adapter_drift_full_size():
     plain = [{k: v for k, v in L.items() if k not in ("a_q", "b_q", "a_v", "b_v")} for L in merged]
     s.sync()
     full = np.arange(w.suffix_start, w.n_tokens)
+    off = 0
     for seq in range(w.batch):
         # layer 0 runs the selected rows only, under the merged adapter
-        U, K0, V0 = layer0_oracle(s, seq, s.positions[seq], 0.0, 0.0, weights=plain)
+        U, K0, V0, X1 = layer0_oracle(s, seq, s.positions[seq], 0.0, 0.0, weights=plain)
+        assert_close(X1_gpu[off:off + len(U)], X1, TOL["bf16"], f"refreshed rows of seq {seq} after layer 0")
+        off += len(U)
         Ut = torch.from_numpy(U)
         assert_close(f64(s.K[seq, 0][:, Ut]), K0[:, U], TOL["bf16"], f"K seq {seq} layer 0")
         assert_close(f64(s.V[seq, 0][:, Ut]), V0[:, U], TOL["bf16"], f"V seq {seq} layer 0")

@@ -2,9 +2,9 @@
 Contexts, Sec. 13.3): a Qwen3-8B-shaped block (d 4096, 32/8 heads x 128, FFN
 12288) cut to two layers so the oracle stays cheap, a prompt of 2056 tokens
 that loses 8 at 64 (Shift), and 64 positions in R intervals with the M(U) the
-pages state.  Layer 0's written K/V rows against the oracle (same Shift, same
-refresh), every other cache row bit-identical to the shifted cache, the
-interval count and M(U) exact."""
+pages state.  Layer 0's written K/V rows and the refreshed rows after layer
+0 against the oracle (same Shift, same refresh), every other cache row
+bit-identical to the shifted cache, the interval count and M(U) exact."""
 import dataclasses
 
 import numpy as np
@@ -36,6 +36,12 @@ def test_matched_work_geometry_layer0(R):
     K_s, V_s = s.K.clone(), s.V.clone()
     rows, ivs = s.select()
     assert (rows, ivs) == (64, R)
+    # layer 0 alone first (the refreshed rows X^1 depend on the inputs only);
+    # the full run rewrites layer 0's selected rows before reading them
+    s.refresh(0, 1, flags=0)
+    s.sync()
+    X1_gpu = f64(s.hidden[:64])
+    s.select()
     s.refresh()
     s.sync()
     # oracle: the same Shift on the input cache, then layer 0 of the packed refresh
@@ -47,8 +53,9 @@ def test_matched_work_geometry_layer0(R):
     X_src[U] = f64(s.embed[torch.from_numpy(ids[U].astype(np.int64)).cuda()])
     loc = oracle.shift_mask(s.local_mask[0], at, d_del)[:N]     # the bits moved with their tokens
     snk = oracle.shift_mask(s.sink_mask[0], at, d_del)[:N]
-    _, K, V, _, _ = oracle.refresh_packed(spec, LazyWeights(s.layers), K0, V0, loc, snk, U, X_src, 0.0, 0.0, False,
-                                          n_layers=1)
+    X1, K, V, _, _ = oracle.refresh_packed(spec, LazyWeights(s.layers), K0, V0, loc, snk, U, X_src, 0.0, 0.0, False,
+                                           n_layers=1)
+    assert_close(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0")
     Ut = torch.from_numpy(U)
     assert_close(f64(s.K[0, 0][:, Ut]), K[0][:, U], TOL["bf16"], "K layer 0")
     assert_close(f64(s.V[0, 0][:, Ut]), V[0][:, U], TOL["bf16"], "V layer 0")

@@ -194,10 +194,20 @@ def test_llama8b_full_size_against_oracle():
     X_src = np.zeros((w.capacity, w.model.d_model))
     X_src[U] = f64(emb[torch.from_numpy(ids[0][U].astype(np.int64)).cuda()])
     K_in, V_in = s.K.clone(), s.V.clone()
+    spec = oracle_spec(w)
+    # layer 0 alone first: the refreshed rows X^1 depend on the inputs only,
+    # so they are held elementwise to the tolerance; this run rewrites only
+    # layer 0's selected K/V rows, which the full refresh rewrites before
+    # reading them, so it leaves the full run's results unchanged
+    s.select()
+    s.refresh(0, 1, flags=0)
+    s.sync()
+    X1 = oracle.refresh_packed(spec, LazyWeights(s.layers), Ks0[:1], Vs0[:1], s.local_mask[0], s.sink_mask[0], U,
+                               X_src, n_layers=1)[0]
+    assert_close(f64(s.hidden[:len(U)]), X1, TOL["bf16"], "refreshed rows after layer 0")
     s.select()
     s.refresh()
     s.sync()
-    spec = oracle_spec(w)
     exact = dataclasses.replace(spec, dtype="f64")
     W = LazyWeights(s.layers)
     Xb, Kb, Vb, lb, sb = oracle.refresh_packed(spec, W, Ks0, Vs0, s.local_mask[0], s.sink_mask[0], U, X_src)
@@ -229,3 +239,27 @@ def test_llama8b_full_size_against_oracle():
     local_after, sink_after = kvr.kvr_read_meta(s.handle, 1, s.words)
     np.testing.assert_array_equal(local_after[0], oracle.bitmask_words(lb)[:s.words])
     s.close()
+
+
+@pytest.mark.parametrize("sink_static", [False, True])
+def test_bf16_seven_query_heads_per_kv_head_block_seams(sink_static):
+    """The block-seam geometry at the Qwen2.5-7B head grouping: 7 query heads
+    per K/V head (14 / 2 heads x 128, so a query tile holds 18 positions x 7
+    heads = 126 MMA rows), q/k/v bias, alpha = -2, beta = -4; N = 2112 as 8
+    independently prefilled blocks of 264 with seam windows tau = 64 under the
+    asymmetric rule (896 rows, 8 intervals); blocks 2..8 local and their first
+    4 positions the sinks S' ("kv-cross-attention-reuse", Sec. 6.3-6.4).  With
+    a static sink set the beta penalty also reaches the refreshed S'."""
+    base = wl.WORKLOADS["qwen7b_seam"]
+    m = dataclasses.replace(base.model, n_layers=2, d_model=1792, n_q_heads=14, n_kv_heads=2, ffn_dim=1024,
+                            vocab=1000)
+    w = dataclasses.replace(base, name="seam_g7", model=m, capacity=2112, n_tokens=2112)
+    layers = wl.make_layer_weights(w, "cuda")
+    s = Setup(w, weights=layers, flags=kvr.KVR_SINK_STATIC if sink_static else 0)
+    assert len(s.positions[0]) == 896
+    Ks0, Vs0 = f64(s.K), f64(s.V)
+    emb = f64(s.embed)
+    ids = s.ids.cpu().numpy()
+    worst = run_and_compare(s, LazyWeights(layers), Ks0, Vs0, [emb[ids[0]]], TOL["bf16"], sink_static=sink_static)
+    s.close()
+    print("7 heads per K/V head, sink_static", sink_static, "worst", worst)
