@@ -242,6 +242,40 @@ kvr_status kvr_reselect(kvr_cache* c, const int32_t* positions, const int32_t* c
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * kvr_refresh_range -- the adapter-drift repair of one edit in one call
+ * ("CacheReforge", Bounded Recovery, "Executable restart"): layers
+ * [range_begin, range_end) are recomputed over every position of the
+ * affected suffix [suffix_start, n_tokens) of every sequence, all other
+ * layers only over the selected positions.  In order, on one stream:
+ *   1. select `positions` (as kvr_select, no budget check; rows from
+ *      token_ids + embed_table, or from hidden_src) into hidden_sel;
+ *   2. layers [0, range_begin) over the selected rows;
+ *   3. switch to the whole suffix (kvr_reselect): a selected position keeps
+ *      its refreshed row, every other suffix position enters from
+ *      `boundary`, the stored hidden states at layer range_begin; rows go to
+ *      hidden_full;
+ *   4. layers [range_begin, range_end) over the whole suffix;
+ *   5. switch back to the selected positions, carrying their rows;
+ *   6. layers [range_end, n_layers) over the selected rows, then `flags`
+ *      (KVR_COMMIT_META clears local/sink of the selected positions only).
+ * With range_begin == range_end steps 3-5 are skipped (a plain refresh).
+ *   boundary    device [batch][capacity][d_model], model dtype.
+ *   hidden_sel  device [sum(counts)][d_model]: the selected rows' output.
+ *   hidden_full device [batch * (n_tokens - suffix_start)][d_model]
+ *               (scratch for the range; may be NULL when the range is empty).
+ *   workspace   at least kvr_workspace_bytes(c, batch * (n_tokens -
+ *               suffix_start)) bytes when the range is not empty, else
+ *               kvr_workspace_bytes(c, sum(counts)); 256-byte aligned.
+ * Errors as the calls it makes; ERANGE for a range outside [0, n_layers].
+ * On an error the selection may be either one; select again before reuse.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_refresh_range(kvr_cache* c, const kvr_layer_weights* w, int32_t range_begin, int32_t range_end,
+                             const int32_t* positions, const int32_t* counts, const int32_t* token_ids,
+                             const void* embed_table, int32_t vocab, const void* hidden_src, const void* boundary,
+                             void* hidden_sel, void* hidden_full, void* workspace, size_t ws_bytes, uint32_t flags,
+                             void* stream);
+
+/* ---------------------------------------------------------------------------
  * kvr_lora_merge -- fold a low-rank adapter into a projection
  * ("CacheReforge", Implementation: a LoRA on the cache-producing projections):
  *   w_out[i][k] = w[i][k] + scale * sum_j b[i - row_begin][j] * a[j][k]

@@ -894,6 +894,46 @@ kvr_status kvr_refresh_interval_wise(kvr_cache* c, const int32_t* positions, con
     return KVR_OK;
 }
 
+kvr_status kvr_refresh_range(kvr_cache* c, const kvr_layer_weights* w, int32_t range_begin, int32_t range_end,
+                             const int32_t* positions, const int32_t* counts, const int32_t* token_ids,
+                             const void* embed_table, int32_t vocab, const void* hidden_src, const void* boundary,
+                             void* hidden_sel, void* hidden_full, void* workspace, size_t ws_bytes, uint32_t flags,
+                             void* stream) {
+    if (!c || !counts) {
+        set_error("cache or counts is NULL");
+        return KVR_EINVAL;
+    }
+    if (range_begin < 0 || range_end > c->m.n_layers || range_begin > range_end) {
+        set_error("layer range outside [0, n_layers]");
+        return KVR_ERANGE;
+    }
+    const bool ranged = range_end > range_begin;
+    if (ranged && (!boundary || !hidden_full)) {
+        set_error("a non-empty layer range needs the boundary rows and the hidden_full buffer");
+        return KVR_EINVAL;
+    }
+    const int L = c->m.n_layers;
+    kvr_status st = kvr_select(c, positions, counts, -1, token_ids, embed_table, vocab, hidden_src, hidden_sel,
+                               nullptr, nullptr, stream);
+    if (st != KVR_OK) return st;
+    if (!ranged) return kvr_refresh(c, w, 0, L, hidden_sel, workspace, ws_bytes, flags, stream);
+    if ((st = kvr_refresh(c, w, 0, range_begin, hidden_sel, workspace, ws_bytes, 0, stream)) != KVR_OK) return st;
+    // the whole affected suffix of every sequence, sequence-major
+    const int S = c->n_tokens - c->suffix_start;
+    std::vector<int32_t> full((size_t)c->batch * S), full_counts(c->batch, S);
+    for (int b = 0; b < c->batch; ++b)
+        for (int i = 0; i < S; ++i) full[(size_t)b * S + i] = c->suffix_start + i;
+    if ((st = kvr_reselect(c, full.data(), full_counts.data(), hidden_sel, boundary, hidden_full, nullptr, nullptr,
+                           stream)) != KVR_OK)
+        return st;
+    if ((st = kvr_refresh(c, w, range_begin, range_end, hidden_full, workspace, ws_bytes, 0, stream)) != KVR_OK)
+        return st;
+    if ((st = kvr_reselect(c, positions, counts, hidden_full, boundary, hidden_sel, nullptr, nullptr, stream)) !=
+        KVR_OK)
+        return st;
+    return kvr_refresh(c, w, range_end, L, hidden_sel, workspace, ws_bytes, flags, stream);
+}
+
 kvr_status kvr_lora_merge(const void* w, void* w_out, int32_t n_out, int32_t K, int32_t row_begin,
                           int32_t row_count, const void* a, const void* b, int32_t rank, float scale, int32_t dtype,
                           void* stream) {

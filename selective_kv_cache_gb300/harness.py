@@ -4,6 +4,8 @@ drives the C entry points.  Shared by the GPU tests and bench.py; it holds
 none of the method's arithmetic (that runs in libkvr's kernels)."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -42,6 +44,18 @@ def pack_adapter(layers):
     return torch.cat(parts)
 
 
+def shard_sequences(batch: int, world: int, rank: int):
+    """Sequences [lo, hi) of a batch that rank `rank` of `world` owns: the
+    sequences are independent problems (own cache, own selection), so they
+    split into contiguous, near-equal shards with no exchange between ranks;
+    the first batch % world ranks take one more."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("need 0 <= rank < world")
+    base, extra = divmod(batch, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
 class Setup:
     """One workload bound to a libkvr cache on the current CUDA device.
 
@@ -50,17 +64,27 @@ class Setup:
     selection (list of int arrays, one per sequence)."""
 
     def __init__(self, w: wl.Workload, cache="random", positions=None, weights=None, flags=0,
-                 local=None, sink=None, device="cuda", embed=None):
+                 local=None, sink=None, device="cuda", embed=None, seqs=None):
+        # seqs = (lo, hi): bind only sequences [lo, hi) of the workload's batch
+        # (a rank's shard); their inputs are the full batch's, sliced
+        full = w
+        lo, hi = (0, w.batch) if seqs is None else seqs
+        if seqs is not None:
+            w = dataclasses.replace(w, batch=hi - lo)
+        self.seqs = (lo, hi)
         self.w = w
         self.shape = w.model
         self.device = device
         self.layers = weights if weights is not None else wl.make_layer_weights(w, device)
         self.warr = kvr.layer_weights_array(self.layers)
         if isinstance(cache, str):
-            self.K, self.V = wl.make_random_cache(w, device)
+            K, V = wl.make_random_cache(full, device)
+            self.K, self.V = (K, V) if seqs is None else (K[lo:hi].clone(), V[lo:hi].clone())
+            del K, V
         else:
             self.K, self.V = cache
-        lm, sm = wl.make_metadata(w)
+        lm, sm = wl.make_metadata(full)
+        lm, sm = lm[lo:hi], sm[lo:hi]
         if local is not None:
             lm = local
         if sink is not None:
@@ -74,12 +98,12 @@ class Setup:
         self.words = (w.capacity + 31) // 32
         if w.uses_embeddings:
             self.embed = embed if embed is not None else wl.make_embeddings(w, device)
-            self.ids = wl.make_token_ids(w, device)
+            self.ids = wl.make_token_ids(full, device)[lo:hi].contiguous()
             self.hidden_src = None
         else:
             self.embed = self.ids = None
-            self.hidden_src = wl.make_hidden_inputs(w, device)
-        self.positions = positions if positions is not None else wl.make_positions(w)
+            self.hidden_src = wl.make_hidden_inputs(full, device)[lo:hi].contiguous()
+        self.positions = positions if positions is not None else wl.make_positions(full)[lo:hi]
         self.pos_host = np.ascontiguousarray(np.concatenate(self.positions).astype(np.int32))
         self.counts = np.array([len(p) for p in self.positions], np.int32)
         self.n_rows = int(self.counts.sum())
@@ -133,31 +157,29 @@ class Setup:
             workspace=self.ws, ws_bytes=self.ws_bytes, flags=flags, stream=stream)
 
     def refresh_range(self, boundary, r0, r1, stream=None):
-        """Adapter-drift recovery: the selected rows through layers [0, r0),
-        the whole affected suffix through [r0, r1) (rows not selected enter from
-        `boundary` [batch, capacity, d], the stored hidden states at layer r0),
-        then the selected rows again through [r1, L) and the commit."""
+        """Adapter-drift recovery through kvr_refresh_range: the selected rows
+        through layers [0, r0), the whole affected suffix through [r0, r1)
+        (rows not selected enter from `boundary` [batch, capacity, d], the
+        stored hidden states at layer r0), then the selected rows again through
+        [r1, L) and the commit."""
         w = self.w
-        L = self.shape.n_layers
-        full = [np.arange(w.suffix_start, w.n_tokens, dtype=np.int32) for _ in range(w.batch)]
-        full_pos = np.ascontiguousarray(np.concatenate(full))
-        full_cnt = np.array([len(f) for f in full], np.int32)
-        n_full = int(full_cnt.sum())
+        n_full = w.batch * (w.n_tokens - w.suffix_start)
         if getattr(self, "hidden_full", None) is None or self.hidden_full.shape[0] < n_full:
             self.hidden_full = torch.empty((n_full, self.shape.d_model), dtype=self.shape.torch_dtype,
                                            device=self.device)
+        n = int(np.asarray(self.counts).sum())
+        if n > self.hidden.shape[0]:
+            self.hidden = torch.empty((n, self.shape.d_model), dtype=self.shape.torch_dtype, device=self.device)
+        self.n_rows = n
         need = kvr.kvr_workspace_bytes(self.handle, n_full)
         if self.ws is None or need > self.ws_bytes:
             self.ws_bytes = need
             self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
-        self.select(stream=stream)
-        kvr.kvr_refresh(self.handle, self.warr, 0, r0, self.hidden, self.ws, self.ws_bytes, 0, stream=stream)
-        kvr.kvr_reselect(self.handle, full_pos, full_cnt, self.hidden, boundary, self.hidden_full, stream=stream)
-        kvr.kvr_refresh(self.handle, self.warr, r0, r1, self.hidden_full, self.ws, self.ws_bytes, 0, stream=stream)
-        kvr.kvr_reselect(self.handle, self.pos_host, self.counts, self.hidden_full, boundary, self.hidden,
-                         stream=stream)
-        kvr.kvr_refresh(self.handle, self.warr, r1, L, self.hidden, self.ws, self.ws_bytes, kvr.KVR_COMMIT_META,
-                        stream=stream)
+        kvr.kvr_refresh_range(self.handle, self.warr, r0, r1, self.pos_host, self.counts, token_ids=self.ids,
+                              embed_table=self.embed, vocab=self.shape.vocab if self.embed is not None else 0,
+                              hidden_src=self.hidden_src, boundary=boundary, hidden_sel=self.hidden,
+                              hidden_full=self.hidden_full, workspace=self.ws, ws_bytes=self.ws_bytes,
+                              flags=kvr.KVR_COMMIT_META, stream=stream)
 
     def sync(self, stream=None):
         kvr.kvr_sync_status(self.handle, stream)

@@ -38,7 +38,7 @@ EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace
            "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge",
            "kvr_shift", "kvr_splice", "kvr_cache_info", "kvr_restart_layer", "kvr_policy_sensitivity",
            "kvr_policy_create", "kvr_policy_destroy", "kvr_policy_plan", "kvr_policy_commit", "kvr_policy_versions",
-           "kvr_sur_workspace_bytes", "kvr_sur_select", "kvr_sur_status"]
+           "kvr_sur_workspace_bytes", "kvr_sur_select", "kvr_sur_status", "kvr_refresh_range"]
 
 
 class kvr_model_desc(C.Structure):
@@ -73,6 +73,8 @@ lib.kvr_refresh_layer_noalloc.argtypes = [P, I32, C.POINTER(kvr_layer_weights), 
 lib.kvr_refresh_interval_wise.argtypes = [P, P, P, I32, P, P, I32, P, C.POINTER(kvr_layer_weights), I32, I32, P, P,
                                           C.c_size_t, C.c_uint32, P, P]
 lib.kvr_reselect.argtypes = [P, P, P, P, P, P, P, P, P]
+lib.kvr_refresh_range.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, P, P, I32, P, P, P, P, P,
+                                  C.c_size_t, C.c_uint32, P]
 lib.kvr_lora_merge.argtypes = [P, P, I32, I32, I32, I32, P, P, I32, C.c_float, I32, P]
 lib.kvr_shift.argtypes = [P, I32, I32, P]
 lib.kvr_splice.argtypes = [P, I32, I32, I32, P, P, I32, C.c_uint32, P]
@@ -219,6 +221,17 @@ def kvr_reselect(c: int, positions, counts, carry_rows, fill_rows, hidden_out, s
     _check(lib.kvr_reselect(c, pp, cp, _ptr(carry_rows), _ptr(fill_rows), _ptr(hidden_out), C.byref(n_rows),
                             C.byref(n_iv), _stream(stream)), "kvr_reselect")
     return n_rows.value, n_iv.value
+
+
+def kvr_refresh_range(c: int, weights_array, range_begin: int, range_end: int, positions, counts, token_ids=None,
+                      embed_table=None, vocab: int = 0, hidden_src=None, boundary=None, hidden_sel=None,
+                      hidden_full=None, workspace=None, ws_bytes: int = 0, flags: int = KVR_COMMIT_META, stream=None):
+    pp = positions.ctypes.data if hasattr(positions, "ctypes") else _ptr(positions)
+    cp = counts.ctypes.data if hasattr(counts, "ctypes") else _ptr(counts)
+    _check(lib.kvr_refresh_range(c, weights_array, range_begin, range_end, pp, cp, _ptr(token_ids),
+                                 _ptr(embed_table), vocab, _ptr(hidden_src), _ptr(boundary), _ptr(hidden_sel),
+                                 _ptr(hidden_full), _ptr(workspace), ws_bytes, flags, _stream(stream)),
+           "kvr_refresh_range")
 
 
 def kvr_lora_merge(w, w_out, n_out: int, K: int, row_begin: int, row_count: int, a, b, rank: int, scale: float,

@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 kvr = pytest.importorskip("selective_kv_cache_gb300.kvr")
 from selective_kv_cache_gb300.harness import Setup  # noqa: E402
-from helpers import TOL, assert_close, f64, small_bf16  # noqa: E402
+from helpers import TOL, assert_close, assert_rel_heads, f64, small_bf16  # noqa: E402
 
 
 @pytest.mark.parametrize("dtype,alpha,beta", [("bf16", 0.0, 0.0), ("bf16", -2.0, -4.0), ("f32", -2.0, -4.0)])
@@ -43,6 +43,7 @@ def test_attend_matches_oracle(dtype, alpha, beta):
             kvr.kvr_attend(s.handle, layer, q, out, workspace, 0 if workspace is None else ws.numel())
             s.sync()
             assert_close(f64(out), want, TOL[dtype], f"attend layer {layer} workspace={workspace is not None}")
+            assert_rel_heads(f64(out), want, TOL[dtype], m.head_dim, f"attend layer {layer}")
     assert torch.equal(s.K, K_in)
     s.close()
 
@@ -73,6 +74,7 @@ def test_attend_block_seam_full_shape():
         kvr.kvr_attend(s.handle, 0, q, out, workspace, 0 if workspace is None else ws.numel())
         s.sync()
         assert_close(f64(out), want, TOL["bf16"], f"attend, workspace={workspace is not None}")
+        assert_rel_heads(f64(out), want, TOL["bf16"], m.head_dim, f"attend, workspace={workspace is not None}")
     s.close()
 
 
@@ -140,4 +142,5 @@ def test_attend_peaked_softmax_rescales_output(kind):
         kvr.kvr_attend(s.handle, 0, q, out, workspace, 0 if workspace is None else ws.numel())
         s.sync()
         assert_close(f64(out), want, TOL["bf16"], f"{kind}, workspace={workspace is not None}")
+        assert_rel_heads(f64(out), want, TOL["bf16"], m.head_dim, f"{kind}, workspace={workspace is not None}")
     s.close()

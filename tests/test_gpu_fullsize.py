@@ -25,7 +25,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 kvr = pytest.importorskip("selective_kv_cache_gb300.kvr")
 from selective_kv_cache_gb300.harness import Setup, merge_lora, pack_adapter  # noqa: E402
-from helpers import TOL, LazyWeights, assert_close, f64, oracle_spec  # noqa: E402
+from helpers import TOL, LazyWeights, assert_close, assert_close_rows, f64, oracle_spec  # noqa: E402
 
 
 def layer0_oracle(s, seq, rows, alpha, beta, sink_static=False, weights=None):
@@ -76,7 +76,7 @@ def test_fragmented_packed_and_interval_wise_full_size():
     n_iv = b.refresh_interval_wise()
     b.sync()
     U, K0, V0, X1 = layer0_oracle(a, 0, a.positions[0], 0.0, 0.0)
-    assert_close(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0")
+    assert_close_rows(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0")
     assert n_iv == oracle.intervals(U).shape[0] and n_iv > 250
     Ut = torch.from_numpy(U)
     for s in (a, b):
@@ -107,7 +107,7 @@ def test_block_seam_full_size(sink_static):
     s.refresh()
     s.sync()
     U, K0, V0, X1 = layer0_oracle(s, 0, s.positions[0], w.alpha, w.beta, sink_static)
-    assert_close(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0 (alpha/beta bias, 7 heads per K/V head)")
+    assert_close_rows(X1_gpu, X1, TOL["bf16"], "refreshed rows after layer 0 (alpha/beta bias, 7 heads per K/V head)")
     Ut = torch.from_numpy(U)
     assert_close(f64(s.K[0, 0][:, Ut]), K0[:, U], TOL["bf16"], "K layer 0")
     assert_close(f64(s.V[0, 0][:, Ut]), V0[:, U], TOL["bf16"], "V layer 0")
@@ -167,7 +167,7 @@ def test_adapter_drift_full_size():
     for seq in range(w.batch):
         # layer 0 runs the selected rows only, under the merged adapter
         U, K0, V0, X1 = layer0_oracle(s, seq, s.positions[seq], 0.0, 0.0, weights=plain)
-        assert_close(X1_gpu[off:off + len(U)], X1, TOL["bf16"], f"refreshed rows of seq {seq} after layer 0")
+        assert_close_rows(X1_gpu[off:off + len(U)], X1, TOL["bf16"], f"refreshed rows of seq {seq} after layer 0")
         off += len(U)
         Ut = torch.from_numpy(U)
         assert_close(f64(s.K[seq, 0][:, Ut]), K0[:, U], TOL["bf16"], f"K seq {seq} layer 0")

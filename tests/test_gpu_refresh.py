@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 kvr = pytest.importorskip("selective_kv_cache_gb300.kvr")
 from selective_kv_cache_gb300.harness import Setup  # noqa: E402
-from helpers import TOL, LazyWeights, assert_close, f64, oracle_spec, small_bf16  # noqa: E402
+from helpers import TOL, LazyWeights, assert_close, assert_close_rows, f64, oracle_spec, small_bf16  # noqa: E402
 
 
 def run_and_compare(s: Setup, W_oracle, Ks0, Vs0, X_src_seqs, tol, sink_static=False, check_layers=None):
@@ -204,7 +204,7 @@ def test_llama8b_full_size_against_oracle():
     s.sync()
     X1 = oracle.refresh_packed(spec, LazyWeights(s.layers), Ks0[:1], Vs0[:1], s.local_mask[0], s.sink_mask[0], U,
                                X_src, n_layers=1)[0]
-    assert_close(f64(s.hidden[:len(U)]), X1, TOL["bf16"], "refreshed rows after layer 0")
+    assert_close_rows(f64(s.hidden[:len(U)]), X1, TOL["bf16"], "refreshed rows after layer 0")
     s.select()
     s.refresh()
     s.sync()
