@@ -33,6 +33,16 @@
  *   - KVR_PDL=0 in the environment (read once per process) turns off
  *     programmatic dependent launch between the kernels of a call; it
  *     changes how work is launched, never what it computes.
+ *   - KVR_FAULT in the environment (read at the start of every call) makes
+ *     one host-side step fail, for tests of the error paths; no GPU fault is
+ *     made.  "alloc" or "alloc:N": the device allocations of
+ *     kvr_create_cache (the N-th one; 1-based) return out-of-memory, so the
+ *     call returns ENOMEM after freeing what it had allocated.  "upload": the
+ *     position upload of a selection fails (ECUDA); the cache then has no
+ *     valid selection (ESTATE until the next successful select).  "launch":
+ *     every kernel launch of the call fails before it is issued (ECUDA).
+ *     "timeout": each refresh layer marks the device error word as a bounded
+ *     device wait does when it gives up, so kvr_sync_status reports ETIMEOUT.
  */
 #ifndef KVR_H
 #define KVR_H
@@ -486,6 +496,19 @@ kvr_status kvr_sync_status(kvr_cache* c, void* stream);
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* kvr_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * kvr_wait_check -- a health check of the bounded device waits.  The pages
+ * have no counterpart: every pipeline wait in the library's kernels (TMA
+ * copies, tensor-core products, stage hand-offs) gives up after a cycle
+ * budget and records a timeout instead of hanging the GPU.  This call runs
+ * one thread block whose wait, with a budget of `cycles` SM clock cycles,
+ * is on an mbarrier phase that nothing completes; when the budget runs out
+ * it records the timeout in the cache's error word and returns, touching
+ * nothing else (no copy or product is in flight).  kvr_sync_status then
+ * reports ETIMEOUT.  cycles in [1, 2^31); EINVAL otherwise.
+ * ------------------------------------------------------------------------- */
+kvr_status kvr_wait_check(kvr_cache* c, int64_t cycles, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Inspection (synchronous; copies device state to host buffers).

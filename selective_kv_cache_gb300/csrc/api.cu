@@ -366,6 +366,12 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         else
             KVR_CHECK_LAUNCH(launch_epi_down(dt, part, g.down.splits, R, m.d_model, h, hidden, s), "down epilogue");
     }
+    if (fault_at("timeout")) {
+        // injected: the error word as a bounded device wait leaves it when it gives up
+        static const int32_t kTimeoutWord = DEV_ERR_TIMEOUT;
+        KVR_CHECK_LAUNCH(cudaMemcpyAsync(c->d_err, &kTimeoutWord, sizeof(int32_t), cudaMemcpyHostToDevice, s),
+                         "timeout injection");
+    }
     return KVR_OK;
 }
 
@@ -410,6 +416,8 @@ void set_error(const std::string& msg) { g_err = msg; }
 
 namespace {
 thread_local bool t_pdl_armed = false;
+thread_local std::string t_fault;      // KVR_FAULT as read at the start of this thread's current call
+thread_local int t_alloc_count = 0;
 bool pdl_enabled() {
     static const bool on = [] {
         const char* v = std::getenv("KVR_PDL");
@@ -418,7 +426,19 @@ bool pdl_enabled() {
     return on;
 }
 }  // namespace
-void pdl_begin_call() { t_pdl_armed = false; }
+void pdl_begin_call() {
+    t_pdl_armed = false;
+    const char* v = std::getenv("KVR_FAULT");
+    t_fault = v ? v : "";
+    t_alloc_count = 0;
+}
+bool fault_at(const char* point) { return !t_fault.empty() && t_fault == point; }
+bool alloc_fault() {
+    ++t_alloc_count;
+    if (t_fault == "alloc") return true;
+    if (t_fault.rfind("alloc:", 0) == 0) return t_alloc_count == std::atoi(t_fault.c_str() + 6);
+    return false;
+}
 bool pdl_take() {
     const bool r = t_pdl_armed && pdl_enabled();
     t_pdl_armed = true;
@@ -606,7 +626,12 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
         raw += counts[i];
     }
     if (total) std::memcpy(st + 8 * B, positions, (size_t)total * sizeof(int32_t));
-    e = cudaMemcpyAsync(c->d_seqinfo, st, (8 * B + total) * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    // from here on the device selection state changes: the old selection is
+    // no longer valid, whether or not the new one completes
+    c->sel.valid = false;
+    e = fault_at("upload") ? cudaErrorUnknown
+                           : cudaMemcpyAsync(c->d_seqinfo, st, (8 * B + total) * sizeof(int32_t),
+                                             cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "position upload");
     e = cudaEventRecord(c->stage_ev, s);
     if (e != cudaSuccess) return cuda_fail(e, "position upload");
@@ -673,6 +698,7 @@ kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capa
                             int32_t n_tokens, int32_t suffix_start, const uint32_t* local_bits,
                             const uint32_t* sink_bits, float alpha, float beta, uint32_t flags, void* stream,
                             kvr_cache** out) {
+    pdl_begin_call();
     if (!out) {
         set_error("out is NULL");
         return KVR_EINVAL;
@@ -717,7 +743,7 @@ kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capa
     c->stage_elems = (size_t)batch * 8 + rows;
     cudaError_t e = cudaSuccess;
     auto A = [&](void** p, size_t n) {
-        if (e == cudaSuccess) e = cudaMalloc(p, n);
+        if (e == cudaSuccess) e = alloc_fault() ? cudaErrorMemoryAllocation : cudaMalloc(p, n);
     };
     A((void**)&c->d_local, wbytes);
     A((void**)&c->d_sink, wbytes);
@@ -1145,6 +1171,21 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
     p.launches = attention_launches(c->m.dtype, a);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);
     if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
+    return KVR_OK;
+}
+
+kvr_status kvr_wait_check(kvr_cache* c, int64_t cycles, void* stream) {
+    pdl_begin_call();
+    if (!c) {
+        set_error("cache is NULL");
+        return KVR_EINVAL;
+    }
+    if (cycles < 1 || cycles >= (int64_t(1) << 31)) {
+        set_error("cycles must be in [1, 2^31)");
+        return KVR_EINVAL;
+    }
+    KVR_CHECK_LAUNCH(launch_wait_check(c->d_err, (long long)cycles, reinterpret_cast<cudaStream_t>(stream)),
+                     "wait check");
     return KVR_OK;
 }
 

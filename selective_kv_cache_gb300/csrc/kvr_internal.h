@@ -119,6 +119,10 @@ cudaError_t launch_gather(int dtype, const int32_t* U, const int32_t* row_seq, i
                           int capacity, const int32_t* token_ids, const void* embed, const void* hidden_src,
                           void* out, int32_t* err, int vocab_guard, cudaStream_t s);
 
+// One thread block waiting, with a budget of `cycles`, on an mbarrier phase
+// that nothing completes; records DEV_ERR_TIMEOUT in err[0] when it gives up.
+cudaError_t launch_wait_check(int32_t* err, long long cycles, cudaStream_t s);
+
 cudaError_t launch_commit(uint32_t* local, uint32_t* sink, const uint32_t* sel, int total_words, int sink_static,
                           cudaStream_t s);
 cudaError_t launch_map_rows(const int32_t* U, const int32_t* row_seq, int n_rows, int capacity, int32_t* map,
@@ -253,6 +257,13 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 void pdl_begin_call();
 bool pdl_take();   // returns the current permission and grants it to later launches
 
+// Host-side fault injection (KVR_FAULT, read by pdl_begin_call at the start
+// of every call): whether the named step fails in this call.  "alloc" counts
+// allocations: alloc_fault() is true for the N-th one of "alloc:N" (every
+// one for plain "alloc").
+bool fault_at(const char* point);
+bool alloc_fault();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                           Args&&... args) {
@@ -268,6 +279,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    if (fault_at("launch")) return cudaErrorLaunchFailure;   // injected: nothing is issued
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

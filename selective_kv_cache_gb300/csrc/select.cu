@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "kvr_internal.h"
+#include "ptx.cuh"
 
 namespace kvr {
 namespace {
@@ -194,7 +195,25 @@ __global__ void commit_kernel(uint32_t* local, uint32_t* sink, const uint32_t* s
     if (!sink_static) sink[i] &= ~s;
 }
 
+// The bounded wait of the library's pipelines, exercised alone: one thread
+// waits on phase 0 of a fresh barrier that nothing arrives on, with the
+// budget given, and records the timeout when the budget runs out.  No copy
+// or product targets this block's memory, so returning is always safe.
+__global__ void wait_check_kernel(int32_t* err, long long cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0u, cycles)) atomicOr(err, DEV_ERR_TIMEOUT);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_check(int32_t* err, long long cycles, cudaStream_t s) {
+    KVR_LAUNCH(wait_check_kernel, dim3(1), dim3(32), 0, s, err, cycles);
+    return cudaSuccess;
+}
 
 cudaError_t launch_select(const SelectLaunch& a, int batch, cudaStream_t s) {
     select_kernel<<<batch, kSelThreads, 0, s>>>(a);

@@ -38,7 +38,8 @@ EXPORTS = ["kvr_create_cache", "kvr_destroy_cache", "kvr_select", "kvr_workspace
            "kvr_refresh_layer_noalloc", "kvr_refresh_interval_wise", "kvr_reselect", "kvr_lora_merge",
            "kvr_shift", "kvr_splice", "kvr_cache_info", "kvr_restart_layer", "kvr_policy_sensitivity",
            "kvr_policy_create", "kvr_policy_destroy", "kvr_policy_plan", "kvr_policy_commit", "kvr_policy_versions",
-           "kvr_sur_workspace_bytes", "kvr_sur_select", "kvr_sur_status", "kvr_refresh_range"]
+           "kvr_sur_workspace_bytes", "kvr_sur_select", "kvr_sur_status", "kvr_refresh_range",
+           "kvr_wait_check"]
 
 
 class kvr_model_desc(C.Structure):
@@ -93,6 +94,7 @@ lib.kvr_sur_status.argtypes = [P, P]
 lib.kvr_refresh.argtypes = [P, C.POINTER(kvr_layer_weights), I32, I32, P, P, C.c_size_t, C.c_uint32, P]
 lib.kvr_attend.argtypes = [P, I32, P, P, P, C.c_size_t, P]
 lib.kvr_sync_status.argtypes = [P, P]
+lib.kvr_wait_check.argtypes = [P, C.c_int64, P]
 lib.kvr_last_error.restype = C.c_char_p
 lib.kvr_restart_layer.restype = C.c_int32
 lib.kvr_read_selection.argtypes = [P, I32, P, I32, P, I32, P, P, P, P, I32, P, P, P]
@@ -232,6 +234,10 @@ def kvr_refresh_range(c: int, weights_array, range_begin: int, range_end: int, p
                                  _ptr(embed_table), vocab, _ptr(hidden_src), _ptr(boundary), _ptr(hidden_sel),
                                  _ptr(hidden_full), _ptr(workspace), ws_bytes, flags, _stream(stream)),
            "kvr_refresh_range")
+
+
+def kvr_wait_check(c: int, cycles: int, stream=None):
+    _check(lib.kvr_wait_check(c, cycles, _stream(stream)), "kvr_wait_check")
 
 
 def kvr_lora_merge(w, w_out, n_out: int, K: int, row_begin: int, row_count: int, a, b, rank: int, scale: float,
