@@ -627,7 +627,10 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
     }
     if (total) std::memcpy(st + 8 * B, positions, (size_t)total * sizeof(int32_t));
     // from here on the device selection state changes: the old selection is
-    // no longer valid, whether or not the new one completes
+    // no longer valid, whether or not the new one completes (its device lists
+    // stay intact until the select kernel runs, so a carried selection can
+    // still map its rows below)
+    const bool had_sel = c->sel.valid;
     c->sel.valid = false;
     e = fault_at("upload") ? cudaErrorUnknown
                            : cudaMemcpyAsync(c->d_seqinfo, st, (8 * B + total) * sizeof(int32_t),
@@ -659,7 +662,7 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
         // position -> row map of the selection being replaced (rows carry over)
         const size_t map_bytes = (size_t)c->batch * c->capacity * sizeof(int32_t);
         KVR_CHECK_LAUNCH(cudaMemsetAsync(c->d_map, 0xff, map_bytes, s), "row map");
-        if (c->sel.valid)
+        if (had_sel)
             KVR_CHECK_LAUNCH(launch_map_rows(c->d_U, c->d_row_seq, c->sel.n_rows, c->capacity, c->d_map, s),
                              "row map");
     }
