@@ -81,18 +81,13 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
     return g;
 }
 
-// The projections' split-K partials and the attention's split-K/V partials
-// share one region: they are never live at the same time.
-size_t part_bytes(const kvr_model_desc& m, int R, size_t attn_scratch) {
+// The projections' split-K partials (the attention merges its splits inside
+// a thread-block cluster and needs no scratch).
+size_t part_bytes(const kvr_model_desc& m, int R) {
     const Gemms g = plan_all(m, R);
     const size_t gu = g.gu.swiglu_F ? 0 : gemm_partial_bytes(g.gu);
-    const size_t gemm = std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
-                                 std::max(gu, gemm_partial_bytes(g.down)));
-    return std::max(gemm, attn_scratch);
-}
-
-size_t sel_attn_scratch(const kvr_cache* c) {
-    return attention_scratch_bytes(c->m.dtype, c->sel.attn_split, c->sel.n_tiles, c->m.n_kv_heads);
+    return std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
+                    std::max(gu, gemm_partial_bytes(g.down)));
 }
 
 WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
@@ -236,19 +231,6 @@ kvr_status check_layer_weights(const kvr_cache* c, const kvr_layer_weights* w) {
     return KVR_OK;
 }
 
-// Point the attention at its split-K/V scratch when the region holds it.
-void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr_cache* c) {
-    const size_t need = sel_attn_scratch(c);
-    a->part_o = nullptr;
-    a->part_ml = nullptr;
-    a->chunk = c->sel.attn_chunk;
-    a->n_split = c->sel.attn_split;
-    if (need == 0 || !region || bytes < need) return;
-    const size_t o_floats = need / sizeof(float) / 130 * 128;
-    a->part_o = region;
-    a->part_ml = region + o_floats;
-}
-
 // One layer of the packed refresh over the current selection.
 // xn_ready: the previous layer's down epilogue already wrote this layer's
 // normalised rows into the workspace; next_norm1: fuse the next layer's first
@@ -327,8 +309,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.alpha = c->alpha;
         a.beta = c->beta;
         a.err = c->d_err;
-        set_attention_scratch(&a, part, L.part_size, c);
-        p.launches = attention_launches(dt, a);
+        a.n_split = c->sel.attn_split;
         cudaError_t e = launch_attention(dt, a, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     }
@@ -393,7 +374,7 @@ kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_by
         return KVR_ESTATE;
     }
     const int R = c->sel.n_rows;
-    *L = layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c)));
+    *L = layout(c->m, R, part_bytes(c->m, R));
     if (R == 0) return KVR_OK;
     if (!hidden || !ws) {
         set_error("hidden rows or workspace is NULL");
@@ -607,7 +588,7 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
     sel.n_rows = rows;
     sel.n_intervals = ivs;
     sel.n_tiles = tiles;
-    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split);
+    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_split);
 
     // the staging buffer may still feed the previous upload
     cudaError_t e = cudaEventSynchronize(c->stage_ev);
@@ -1062,16 +1043,14 @@ kvr_status kvr_cache_info(kvr_cache* c, int32_t* n_tokens, int32_t* suffix_start
 size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
     if (!c) return 0;
     int R = max_rows > 0 ? max_rows : c->sel.n_rows;
-    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c))).total;
+    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R)).total;
     // the projections' split choice changes with the row count: take the
     // largest partial region over every row count up to max_rows (it peaks at
-    // row-tile edges); a split attention never uses more than kAttnMaxSplitCTAs
-    // CTAs' worth of partials
-    const size_t attn = c->m.dtype == KVR_BF16 ? (size_t)kAttnMaxSplitCTAs * 128 * 130 * sizeof(float) : 0;
+    // row-tile edges)
     const int step = c->m.dtype == KVR_BF16 ? 256 : 64;
     size_t part = 0;
-    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R), attn));
-    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r, attn));
+    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R)));
+    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r));
     return layout(c->m, R, part).total;
 }
 
@@ -1167,11 +1146,11 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
     a.alpha = c->alpha;
     a.beta = c->beta;
     a.err = c->d_err;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
-        set_attention_scratch(&a, static_cast<float*>(workspace), ws_bytes, c);
+    (void)workspace;   // the split K/V ranges merge inside a thread-block cluster
+    (void)ws_bytes;
+    a.n_split = c->sel.attn_split;
     std::string why;
     Prof p(c, KVR_K_ATTN, s);
-    p.launches = attention_launches(c->m.dtype, a);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);
     if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     return KVR_OK;

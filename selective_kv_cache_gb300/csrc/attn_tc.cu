@@ -7,10 +7,10 @@
 // Repair for Evolving Contexts", Sec. 13.2, Eq. 22, and Eqs. 23-24 for the
 // per-query-tile K/V tile counts that bound the loop.)
 //
-// One CTA per (query tile, K/V head).  The 128 MMA rows are the tile's
-// positions times the G query heads of that K/V head (row = p*G + i), so all
-// of them read the same K/V tiles and one causal limit g_p serves a whole
-// group.  Per 128-key tile:
+// One CTA per (query tile, K/V head, K/V chunk).  The 128 MMA rows are the
+// tile's positions times the G query heads of that K/V head (row = p*G + i),
+// so all of them read the same K/V tiles and one causal limit g_p serves a
+// whole group.  Per 128-key tile:
 //   warp 0      TMA: K and V tiles (two 64-column boxes each, 128-B swizzle)
 //               into 3-stage rings, K one tile ahead of V; keys >= n_tokens
 //               arrive as zeros;
@@ -22,11 +22,17 @@
 //               mask, online softmax in base 2 (the running max is only
 //               raised, and O rescaled in TMEM, when it grows by more than
 //               2^8, so P stays <= 256), P as bf16 pairs over the tile's
-//               scores in TMEM, the A operand of the PV product; at the end
-//               O / l to global memory, or an fp32 partial for the merge.
+//               scores in TMEM, the A operand of the PV product.
+// A query tile's K/V range is split over the n CTAs of one thread-block
+// cluster (chunk = ceil(tiles / n) each).  At the end every CTA stages its
+// unnormalised O rows and (running max, sum) in its own shared memory; after
+// a cluster barrier, CTA r merges output columns [128 r / n, 128 (r + 1) / n)
+// of every row from all n CTAs over distributed shared memory and writes
+// them in bf16, so the split needs no global scratch and no second kernel.
 // Tiles below the plan's n_full are wholly visible to every row and skip the
 // causal test.  Every wait is bounded; on a timeout the CTA records the error,
-// drains its copies and MMAs, frees TMEM and returns.
+// drains its copies and MMAs, takes part in the cluster barriers, frees TMEM
+// and returns.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -46,7 +52,14 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kOffML = kOffBar + 256;          // [128] (running max, sum) for the cluster merge
+constexpr uint32_t kSmemBytes = kOffML + 1024 + 1024;
+// the merge stages each CTA's O rows in the (then idle) K ring: rows of 128
+// floats 528 bytes apart, so a warp's 32 rows at one column chunk fall in
+// distinct banks
+constexpr uint32_t kStageRowBytes = 528;
+static_assert(128 * kStageRowBytes <= kStages * kTile, "merge staging must fit in the K ring");
+constexpr int kMaxClusterSplit = 8;
 constexpr int kSBufs = 3;                       // score buffers: the QK product runs two tiles ahead
 // TMEM columns: S[b] at 128 b (P, bf16 pairs, over its first 64 once the
 // scores are read), O 384-511
@@ -88,7 +101,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <bool kBiased>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
+                   const __grid_constant__ CUtensorMap tmQ, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -105,23 +118,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* q_full = mma_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
 
-    const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
+    // grid (K/V head, query tile from the last, split): the longest query
+    // tiles (latest positions) are dispatched first; the splits of one
+    // (tile, head) form one cluster
+    const int h = blockIdx.x, tile = gridDim.y - 1 - blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
     const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], seq = plan[6];
-    // this CTA's chunk of the query tile's K/V tiles [0, plan n_total)
-    const int jb = split * a.chunk;
-    const int n_total = min(plan[5], jb + a.chunk) - jb;   // tiles handled here
-    if (n_split > 1 && n_total <= 0) {
-        // nothing to read: an empty partial for the merge, and no set-up at all
-        pdl_trigger();
-        pdl_wait();
-        if (threadIdx.x < 128) {
-            const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
-            a.part_ml[(slot * 128 + threadIdx.x) * 2] = -INFINITY;
-            a.part_ml[(slot * 128 + threadIdx.x) * 2 + 1] = 0.f;
-        }
-        return;
-    }
+    // this CTA's chunk of the query tile's K/V tiles [0, plan n_total); a CTA
+    // whose chunk is empty still takes part in the cluster merge
+    const int chunk = (plan[5] + n_split - 1) / n_split;
+    const int jb = split * chunk;
+    const int n_total = max(0, min(plan[5], jb + chunk) - jb);   // tiles handled here
     const int G = a.n_q_heads / a.n_kv_heads;
     const int P = 128 / G;
     const int head_index = (seq * a.n_layers + a.layer) * a.n_kv_heads + h;
@@ -141,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmQ);
-        if (a.part_o) prefetch_tmap(&tmP);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     int t_prod = 0;
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && n_total > 0) {
         // P * G <= 128 rows of 128 bytes in each half (126 when G = 6)
         mbar_arrive_expect_tx(q_full, 2u * 128u * (uint32_t)(P * G));
         tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, h * G, row0);
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && n_total > 0) {
             for (int t = t_prod; t <= n_total && ok; ++t) ok = produce(t);
             if (!ok) {  // let every copy still in flight land before the CTA exits
                 mbar_wait(q_full, 0);
@@ -402,10 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[j & 3]);
         }
-        if (ok && n_total > 0) {
-            if (!warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u)) {
-                ok = false;
-            } else if (n_split == 1) {
+        if (ok && n_total > 0 && !warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u))
+            ok = false;
+        const bool have = ok && n_total > 0;   // warp-uniform
+        if (n_split == 1) {
+            if (have) {
                 tc_fence_after();
                 const float inv = 1.0f / l_run;
                 __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
@@ -427,45 +434,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                         reinterpret_cast<uint4*>(out + c * 16)[1] = v1;
                     }
                 }
-            } else {
-                // unnormalised fp32 partial plus (running max in base 2, sum) for
-                // the combine.  The warp's 32 rows go out as four TMA stores of
-                // 32 x 32 floats staged in the idle K ring (every QK product has
-                // completed: the last PV's commit covers them) in the 128-byte
-                // swizzle, which keeps the row-per-lane writes conflict-free.
+            }
+        } else {
+            // stage the unnormalised O row and (running max in base 2, sum) for
+            // the cluster merge; the K ring is idle (every QK product was
+            // waited for through its scores, every copy through the products)
+            reinterpret_cast<float2*>(smem + kOffML)[m] = have ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+            if (have) {
                 tc_fence_after();
-                const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
-                uint8_t* stg = smem + kOffK + (uint32_t)(warp & 3) * 16384u;
+                const uint32_t row = sbase + kOffK + (uint32_t)m * kStageRowBytes;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
                     tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int j = (c & 1) * 4 + t;   // 16-byte chunk within the box row
-                        const uint32_t addr = smem_u32(stg) + (uint32_t)(c >> 1) * 4096u + (uint32_t)lane * 128u +
-                                              ((uint32_t)(j ^ (lane & 7)) << 4);
-                        st_shared_v4(addr, make_uint4(__float_as_uint(o[4 * t]), __float_as_uint(o[4 * t + 1]),
-                                                      __float_as_uint(o[4 * t + 2]), __float_as_uint(o[4 * t + 3])));
-                    }
+                    for (int t = 0; t < 4; ++t)
+                        st_shared_v4(row + (uint32_t)(4 * c + t) * 16u,
+                                     make_uint4(__float_as_uint(o[4 * t]), __float_as_uint(o[4 * t + 1]),
+                                                __float_as_uint(o[4 * t + 2]), __float_as_uint(o[4 * t + 3])));
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    for (int cb = 0; cb < 4; ++cb)
-                        tma_store_2d(&tmP, stg + cb * 4096, cb * 32, (int)(slot * 128) + 32 * (warp & 3));
-                    bulk_commit();
-                    bulk_wait_read_all();   // the staging may be released; the writes land before the grid ends
-                }
-                a.part_ml[(slot * 128 + m) * 2] = m_run;
-                a.part_ml[(slot * 128 + m) * 2 + 1] = l_run;
             }
-        } else if (ok && n_split > 1) {
-            // no K/V tile for this split: an empty partial
-            const size_t slot = ((size_t)split * gridDim.x + tile) * gridDim.y + h;
-            a.part_ml[(slot * 128 + m) * 2] = -INFINITY;
-            a.part_ml[(slot * 128 + m) * 2 + 1] = 0.f;
         }
+    }
+    if (n_split > 1) {
+        // ------------------------------------------------------------ cluster merge
+        // every thread of every CTA of the cluster passes both barriers: the
+        // first publishes the staged rows, the second keeps each CTA (and so
+        // its shared memory) alive until every peer has read it
+        __syncwarp();
+        cluster_sync();
+        if (warp >= 2 && warp < 6 && row_valid) {
+            const uint32_t rank = cluster_rank();
+            float ms[kMaxClusterSplit], w[kMaxClusterSplit];
+            float M = -INFINITY;
+            const uint32_t ml_addr = sbase + kOffML + (uint32_t)m * 8u;
+#pragma unroll
+            for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
+                ms[sp] = -INFINITY;
+                w[sp] = 0.f;
+                if (sp < n_split) {
+                    const float2 v = ld_cluster_f2(cluster_map(ml_addr, (uint32_t)sp));
+                    ms[sp] = v.x;
+                    w[sp] = v.y;   // the split's sum, until the weights below
+                    M = fmaxf(M, v.x);
+                }
+            }
+            float L = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
+                const float e = (sp < n_split && ms[sp] != -INFINITY) ? ex2(ms[sp] - M) : 0.f;
+                L += e * w[sp];
+                w[sp] = e;
+            }
+            const float inv = 1.0f / L;
+            const int c0 = (32 * (int)rank) / n_split, c1 = (32 * ((int)rank + 1)) / n_split;   // 16-byte chunks
+            const uint32_t row = sbase + kOffK + (uint32_t)m * kStageRowBytes;
+            __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
+            for (int c = c0; c < c1; ++c) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
+                    if (w[sp] == 0.f) continue;
+                    const float4 v = ld_cluster_f4(cluster_map(row + (uint32_t)c * 16u, (uint32_t)sp));
+                    acc.x += w[sp] * v.x;
+                    acc.y += w[sp] * v.y;
+                    acc.z += w[sp] * v.z;
+                    acc.w += w[sp] * v.w;
+                }
+                uint2 v;
+                v.x = pack_bf16(acc.x * inv, acc.y * inv);
+                v.y = pack_bf16(acc.z * inv, acc.w * inv);
+                reinterpret_cast<uint2*>(out)[c] = v;
+            }
+        }
+        __syncwarp();
+        cluster_sync();
     }
     if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
@@ -477,95 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Merge the split partials of one (query tile, K/V head): one warp per MMA
-// row, 4 output dimensions per lane.  Splits that saw no key are skipped.
-__global__ void __launch_bounds__(256) attn_combine_kernel(AttnLaunch a, int n_tiles, int n_split) {
-    pdl_trigger();
-    pdl_wait();
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int rows_total = n_tiles * a.n_kv_heads * 128;
-    if (warp >= rows_total) return;
-    const int m = warp & 127;
-    const int h = (warp >> 7) % a.n_kv_heads;
-    const int tile = (warp >> 7) / a.n_kv_heads;
-    const int G = a.n_q_heads / a.n_kv_heads;
-    const int p = m / G, gi = m % G;
-    const int* plan = a.plan + 8 * tile;
-    if (m >= (128 / G) * G || p >= plan[1]) return;
-    // splits in groups of 8: all loads of a group are independent (one L2
-    // round trip), folded into a running (max, sum, o) in split order
-    constexpr int kGroup = 8;
-    float mx = -INFINITY, l = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_split; s0 += kGroup) {
-        float ms[kGroup], ls[kGroup];
-        float4 os[kGroup];
-#pragma unroll
-        for (int k = 0; k < kGroup; ++k) {
-            ms[k] = -INFINITY;
-            if (s0 + k < n_split) {
-                const size_t slot = ((size_t)(s0 + k) * n_tiles + tile) * a.n_kv_heads + h;
-                const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[slot * 128 + m];
-                ms[k] = ml.x;
-                ls[k] = ml.y;
-                os[k] = reinterpret_cast<const float4*>(a.part_o + (slot * 128 + m) * 128)[lane];
-            }
-        }
-        float gm = mx;
-#pragma unroll
-        for (int k = 0; k < kGroup; ++k) gm = fmaxf(gm, ms[k]);
-        if (gm == -INFINITY) continue;
-        const float r = ex2(mx - gm);   // rescale of what is accumulated so far (0 before the first split)
-        l *= r;
-        acc.x *= r;
-        acc.y *= r;
-        acc.z *= r;
-        acc.w *= r;
-#pragma unroll
-        for (int k = 0; k < kGroup; ++k) {
-            if (ms[k] == -INFINITY) continue;
-            const float w = ex2(ms[k] - gm);
-            l += w * ls[k];
-            acc.x += w * os[k].x;
-            acc.y += w * os[k].y;
-            acc.z += w * os[k].z;
-            acc.w += w * os[k].w;
-        }
-        mx = gm;
-    }
-    const float inv = 1.0f / l;
-    __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan[0] + p) * a.n_q_heads + h * G + gi) * 128;
-    uint2 v;
-    v.x = pack_bf16(acc.x * inv, acc.y * inv);
-    v.y = pack_bf16(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(out)[lane] = v;
-}
-
 }  // namespace
 
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads) { return 128 / (n_q_heads / n_kv_heads); }
 
-size_t attn_tc_scratch_bytes(int n_split, int n_tiles, int n_kv_heads) {
-    if (n_split <= 1) return 0;
-    return (size_t)n_split * n_tiles * n_kv_heads * 128 * (128 + 2) * sizeof(float);
-}
-
-cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
-    if (a.n_tiles <= 0) return cudaSuccess;
-    if (a.head_dim != 128 || a.n_q_heads / a.n_kv_heads > 128) {
-        if (why) *why = "tensor-core attention needs head_dim 128";
-        return cudaErrorInvalidValue;
-    }
-    const int n_split = (a.part_o && a.n_split > 1) ? a.n_split : 1;
-    AttnLaunch b = a;
-    if (n_split == 1) b.chunk = 1 << 30;   // one CTA walks the whole range
-    CUtensorMap tk, tv;
-    const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
-    const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
-    if (!make_tmap_3d_bf16(&tk, a.k_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
-        return cudaErrorInvalidValue;
-    if (!make_tmap_3d_bf16(&tv, a.v_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
-        return cudaErrorInvalidValue;
+namespace {
+cudaError_t set_smem_attr() {
     static bool attr = false;
     if (!attr) {
         for (auto* f : {attn_tc_kernel<false>, attn_tc_kernel<true>}) {
@@ -574,28 +534,85 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         }
         attr = true;
     }
-    dim3 grid(a.n_tiles, a.n_kv_heads, n_split);
+    return cudaSuccess;
+}
+}  // namespace
+
+// Clusters of n CTAs of this kernel that the GPU holds at once (the CTAs of
+// a cluster run together on SMs of one GPC); 0 if it cannot say.
+int attn_tc_max_clusters(int n) {
+    static int cache[kMaxClusterSplit + 1] = {};
+    if (n < 1 || n > kMaxClusterSplit) return 0;
+    if (cache[n]) return cache[n];
+    if (set_smem_attr() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, (unsigned)n);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)n;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<false>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        clusters = 0;
+    }
+    cache[n] = clusters;
+    return clusters;
+}
+
+cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
+    if (a.n_tiles <= 0) return cudaSuccess;
+    if (a.head_dim != 128 || a.n_q_heads / a.n_kv_heads > 128) {
+        if (why) *why = "tensor-core attention needs head_dim 128";
+        return cudaErrorInvalidValue;
+    }
+    const int n_split = std::max(1, std::min(a.n_split, kMaxClusterSplit));
+    CUtensorMap tk, tv;
+    const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
+    const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
+    if (!make_tmap_3d_bf16(&tk, a.k_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_3d_bf16(&tv, a.v_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_attr();
+    if (e != cudaSuccess) return e;
     // Q [rows][H_q][128] as (dims, heads, rows): a {64, G, 128 / G} box is one
     // half of a query tile, rows p * G + i
-    CUtensorMap tq, tp;
+    CUtensorMap tq;
     const int G = a.n_q_heads / a.n_kv_heads;
     if (a.n_rows <= 0 ||
         !make_tmap_3d_bf16(&tq, a.q, 128, (uint64_t)a.n_q_heads, (uint64_t)a.n_rows, 256, (uint64_t)a.n_q_heads * 256,
                            64, (uint32_t)G, (uint32_t)(128 / G), why))
         return cudaErrorInvalidValue;
-    memset(&tp, 0, sizeof(tp));
-    if (n_split > 1 &&
-        !make_tmap_2d_f32_sw128(&tp, a.part_o, 128, (uint64_t)n_split * a.n_tiles * a.n_kv_heads * 128, 32, why))
-        return cudaErrorInvalidValue;
-    if (a.alpha != 0.f || a.beta != 0.f)
-        KVR_LAUNCH(attn_tc_kernel<true>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
-    else
-        KVR_LAUNCH(attn_tc_kernel<false>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
-    if (n_split == 1) return cudaSuccess;
-    const long long warps = (long long)a.n_tiles * a.n_kv_heads * 128;
-    KVR_LAUNCH(attn_combine_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, s, b, a.n_tiles,
-               n_split);
-    return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_kv_heads, (unsigned)a.n_tiles, (unsigned)n_split);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n_attr = 0;
+    if (pdl_take()) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (n_split > 1) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 1;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = (unsigned)n_split;
+        ++n_attr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    if (fault_at("launch")) return cudaErrorLaunchFailure;   // injected: nothing is issued
+    if (a.alpha != 0.f || a.beta != 0.f) return cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tk, tv, tq, a);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tk, tv, tq, a);
 }
 
 }  // namespace kvr
