@@ -479,11 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     M = fmaxf(M, v.x);
                 }
             }
+            // a split whose keys all lie past this row's causal limit kept the
+            // max at -inf (its sum and O are not numbers): it takes no part
             float L = 0.f;
 #pragma unroll
             for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
-                const float e = (sp < n_split && ms[sp] != -INFINITY) ? ex2(ms[sp] - M) : 0.f;
-                L += e * w[sp];
+                const bool live = sp < n_split && ms[sp] != -INFINITY;
+                const float e = live ? ex2(ms[sp] - M) : 0.f;
+                if (live) L += e * w[sp];
                 w[sp] = e;
             }
             const float inv = 1.0f / L;
