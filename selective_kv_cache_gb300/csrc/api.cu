@@ -81,13 +81,36 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
     return g;
 }
 
-// The projections' split-K partials (the attention merges its splits inside
-// a thread-block cluster and needs no scratch).
-size_t part_bytes(const kvr_model_desc& m, int R) {
+// The projections' split-K partials and the attention's split partials
+// share one region: they are never live at the same time.
+size_t part_bytes(const kvr_model_desc& m, int R, size_t attn_scratch) {
     const Gemms g = plan_all(m, R);
     const size_t gu = g.gu.swiglu_F ? 0 : gemm_partial_bytes(g.gu);
-    return std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
-                    std::max(gu, gemm_partial_bytes(g.down)));
+    const size_t gemm = std::max(std::max(gemm_partial_bytes(g.qkv), gemm_partial_bytes(g.o)),
+                                 std::max(gu, gemm_partial_bytes(g.down)));
+    return std::max(gemm, attn_scratch);
+}
+
+size_t sel_attn_scratch(const kvr_cache* c) {
+    return attention_scratch_bytes(c->m.dtype, c->sel.attn_split, c->sel.n_tiles, c->m.n_kv_heads);
+}
+
+// Point the attention at its split scratch when the region holds it (else it
+// runs unsplit).
+void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr_cache* c) {
+    const size_t need = sel_attn_scratch(c);
+    a->part_o = nullptr;
+    a->part_ml = nullptr;
+    a->sync = c->d_attn_sync;
+    a->chunk = c->sel.attn_chunk;
+    a->n_split = c->sel.attn_split;
+    if (need == 0 || !region || bytes < need) {
+        a->n_split = 1;
+        return;
+    }
+    const size_t o_floats = need / sizeof(float) / 130 * 128;
+    a->part_o = region;
+    a->part_ml = region + o_floats;
 }
 
 WsLayout layout(const kvr_model_desc& m, int R, size_t part) {
@@ -198,6 +221,7 @@ void free_cache(kvr_cache* c) {
     cudaFree(c->d_rope);
     cudaFree(c->d_err);
     cudaFree(c->d_map);
+    cudaFree(c->d_attn_sync);
     if (c->h_stage) cudaFreeHost(c->h_stage);
     if (c->stage_ev) cudaEventDestroy(c->stage_ev);
     for (auto& r : c->prof) {
@@ -309,7 +333,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.alpha = c->alpha;
         a.beta = c->beta;
         a.err = c->d_err;
-        a.n_split = c->sel.attn_split;
+        set_attention_scratch(&a, part, L.part_size, c);
         cudaError_t e = launch_attention(dt, a, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     }
@@ -374,7 +398,7 @@ kvr_status check_refresh_args(kvr_cache* c, void* hidden, void* ws, size_t ws_by
         return KVR_ESTATE;
     }
     const int R = c->sel.n_rows;
-    *L = layout(c->m, R, part_bytes(c->m, R));
+    *L = layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c)));
     if (R == 0) return KVR_OK;
     if (!hidden || !ws) {
         set_error("hidden rows or workspace is NULL");
@@ -588,7 +612,7 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
     sel.n_rows = rows;
     sel.n_intervals = ivs;
     sel.n_tiles = tiles;
-    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_split);
+    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split);
 
     // the staging buffer may still feed the previous upload
     cudaError_t e = cudaEventSynchronize(c->stage_ev);
@@ -647,6 +671,10 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
             KVR_CHECK_LAUNCH(launch_map_rows(c->d_U, c->d_row_seq, c->sel.n_rows, c->capacity, c->d_map, s),
                              "row map");
     }
+    // the attention's merge counters return to zero after every complete
+    // launch; a new selection starts them from zero whatever came before
+    KVR_CHECK_LAUNCH(cudaMemsetAsync(c->d_attn_sync, 0, (size_t)2 * c->max_tiles * c->m.n_kv_heads * sizeof(int32_t), s),
+                     "attention counters");
     {
         Prof p(c, KVR_K_SELECT, s);
         KVR_CHECK_LAUNCH(launch_select(a, B, s), "select");
@@ -742,6 +770,7 @@ kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capa
     A((void**)&c->d_rope, (size_t)capacity * half * sizeof(float2));
     A((void**)&c->d_err, 4 * sizeof(int32_t));
     A((void**)&c->d_map, rows * sizeof(int32_t));
+    A((void**)&c->d_attn_sync, (size_t)2 * c->max_tiles * m->n_kv_heads * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMallocHost((void**)&c->h_stage, c->stage_elems * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->stage_ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
@@ -767,6 +796,8 @@ kvr_status kvr_create_cache(const kvr_model_desc* m, int32_t batch, int32_t capa
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(c->d_sink, sink_bits ? sink_bits : zeros.data(), wbytes, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->d_err, 0, 4 * sizeof(int32_t), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(c->d_attn_sync, 0, (size_t)2 * c->max_tiles * m->n_kv_heads * sizeof(int32_t), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->d_sel, 0, wbytes, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_eloc, c->d_local, wbytes, cudaMemcpyDeviceToDevice, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_esnk, c->d_sink, wbytes, cudaMemcpyDeviceToDevice, s);
@@ -1043,14 +1074,16 @@ kvr_status kvr_cache_info(kvr_cache* c, int32_t* n_tokens, int32_t* suffix_start
 size_t kvr_workspace_bytes(const kvr_cache* c, int32_t max_rows) {
     if (!c) return 0;
     int R = max_rows > 0 ? max_rows : c->sel.n_rows;
-    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R)).total;
+    if (max_rows <= 0) return layout(c->m, R, part_bytes(c->m, R, sel_attn_scratch(c))).total;
     // the projections' split choice changes with the row count: take the
     // largest partial region over every row count up to max_rows (it peaks at
-    // row-tile edges)
+    // row-tile edges); a split attention never uses more than kAttnMaxSplitCTAs
+    // CTAs' worth of partials
+    const size_t attn = c->m.dtype == KVR_BF16 ? (size_t)kAttnMaxSplitCTAs * 128 * 130 * sizeof(float) : 0;
     const int step = c->m.dtype == KVR_BF16 ? 256 : 64;
     size_t part = 0;
-    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R)));
-    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r));
+    for (int r = step; r < R + step; r += step) part = std::max(part, part_bytes(c->m, std::min(r, R), attn));
+    for (int r = 1; r <= std::min(R, 2 * step); ++r) part = std::max(part, part_bytes(c->m, r, attn));
     return layout(c->m, R, part).total;
 }
 
@@ -1146,9 +1179,9 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
     a.alpha = c->alpha;
     a.beta = c->beta;
     a.err = c->d_err;
-    (void)workspace;   // the split K/V ranges merge inside a thread-block cluster
-    (void)ws_bytes;
-    a.n_split = c->sel.attn_split;
+    set_attention_scratch(&a, (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+                                  ? static_cast<float*>(workspace) : nullptr,
+                          ws_bytes, c);
     std::string why;
     Prof p(c, KVR_K_ATTN, s);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);

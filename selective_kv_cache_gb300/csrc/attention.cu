@@ -12,39 +12,53 @@ int attn_simt_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_simt(const AttnLaunch& a, cudaStream_t s);
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads);
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why);
-int attn_tc_max_clusters(int n);
+size_t attn_tc_scratch_bytes(int n_split, int n_tiles, int n_kv_heads);
 
-// Pick the number n of CTAs (one thread-block cluster) that share each query
-// tile's K/V range, by the modelled time.  The model plays out the
-// hardware's dispatch: clusters go out in launch order (K/V head fastest,
-// then the query tiles from the last, whose ranges are the longest), each
-// taking the earliest free one of the cluster slots the GPU holds at once
-// (the occupancy query), and a cluster lasts its longest chunk,
-// ceil(tiles / n), plus ~6 tile-times of set-up and one more for the merge
-// when n > 1.  tile_kv[t] = K/V tiles of query tile t.
-void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* n_split) {
+size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_heads) {
+    return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_split, n_tiles, n_kv_heads) : 0;
+}
+
+// Pick the chunk size C that minimises the modelled time.  The model plays
+// out the hardware's dispatch: CTAs go to the SMs in launch order (K/V head
+// fastest, then the query tiles from the last, whose ranges are the longest,
+// then the split), each SM taking the next CTA when its last one ends; a CTA
+// costs ~6 tile-times of set-up plus one per K/V tile of its chunk (an empty
+// chunk almost nothing), and one more when it stores or merges split rows.
+// tile_kv[t] = K/V tiles of query tile t.
+void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
+    *chunk = 1 << 30;
     *n_split = 1;
     if (dtype != KVR_BF16 || tile_kv.empty()) return;
-    std::vector<double> slot_free;
+    int max_kv = 1;
+    for (int v : tile_kv) max_kv = std::max(max_kv, v);
+    std::vector<double> sm_free;
     std::greater<double> later;
+    auto makespan = [&](int C, int splits) {
+        sm_free.assign(kNumSMs, 0.0);
+        for (int z = 0; z < splits; ++z)
+            for (int t = (int)tile_kv.size() - 1; t >= 0; --t)
+                for (int y = 0; y < n_kv_heads; ++y) {
+                    const int v = tile_kv[t];
+                    const int n = std::max(0, std::min(C, v - z * C));
+                    const bool shared = (v + C - 1) / C > 1;
+                    std::pop_heap(sm_free.begin(), sm_free.end(), later);
+                    sm_free.back() += n > 0 ? n + 6.0 + (shared ? 1.0 : 0.0) : 0.3;
+                    std::push_heap(sm_free.begin(), sm_free.end(), later);
+                }
+        return *std::max_element(sm_free.begin(), sm_free.end());
+    };
     double best = 1e30;
-    for (int n = 1; n <= 8; ++n) {
-        const int slots = n == 1 ? kNumSMs : attn_tc_max_clusters(n);
-        if (slots <= 0) continue;
-        slot_free.assign(slots, 0.0);
-        for (int t = (int)tile_kv.size() - 1; t >= 0; --t)
-            for (int y = 0; y < n_kv_heads; ++y) {
-                const double cost = (tile_kv[t] + n - 1) / n + 6.0 + (n > 1 ? 1.0 : 0.0);
-                std::pop_heap(slot_free.begin(), slot_free.end(), later);
-                slot_free.back() += cost;
-                std::push_heap(slot_free.begin(), slot_free.end(), later);
-            }
-        const double t = *std::max_element(slot_free.begin(), slot_free.end());
+    for (int C = max_kv; C >= 2; --C) {
+        const int splits = (max_kv + C - 1) / C;
+        if (splits > 1 && (long long)splits * (long long)tile_kv.size() * n_kv_heads > kAttnMaxSplitCTAs) break;
+        const double t = makespan(C, splits);
         if (t < best * 0.98) {
             best = t;
-            *n_split = n;
+            *chunk = C;
+            *n_split = splits;
         }
     }
+    if (*n_split == 1) *chunk = 1 << 30;
 }
 
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile) {

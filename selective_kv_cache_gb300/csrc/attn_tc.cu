@@ -23,16 +23,16 @@
 //               raised, and O rescaled in TMEM, when it grows by more than
 //               2^8, so P stays <= 256), P as bf16 pairs over the tile's
 //               scores in TMEM, the A operand of the PV product.
-// A query tile's K/V range is split over the n CTAs of one thread-block
-// cluster (chunk = ceil(tiles / n) each).  At the end every CTA stages its
-// unnormalised O rows and (running max, sum) in its own shared memory; after
-// a cluster barrier, CTA r merges output columns [128 r / n, 128 (r + 1) / n)
-// of every row from all n CTAs over distributed shared memory and writes
-// them in bf16, so the split needs no global scratch and no second kernel.
+// A query tile's K/V range may be split into chunks of C tiles over several
+// CTAs.  At the end of its chunk each of them takes a ticket; all but the
+// last store their unnormalised O rows and (running max, sum) in fp32 to the
+// workspace and count themselves done; the last one waits for that count
+// (its peers are past their main loops, so the wait ends), loads their rows
+// by TMA, merges them with its own and writes the bf16 output: no second
+// kernel, and the last CTA never stores its own partial.
 // Tiles below the plan's n_full are wholly visible to every row and skip the
 // causal test.  Every wait is bounded; on a timeout the CTA records the error,
-// drains its copies and MMAs, takes part in the cluster barriers, frees TMEM
-// and returns.
+// drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -52,14 +52,12 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
-constexpr uint32_t kOffML = kOffBar + 256;          // [128] (running max, sum) for the cluster merge
-constexpr uint32_t kSmemBytes = kOffML + 1024 + 1024;
-// the merge stages each CTA's O rows in the (then idle) K ring: rows of 128
-// floats 528 bytes apart, so a warp's 32 rows at one column chunk fall in
-// distinct banks
-constexpr uint32_t kStageRowBytes = 528;
-static_assert(128 * kStageRowBytes <= kStages * kTile, "merge staging must fit in the K ring");
-constexpr int kMaxClusterSplit = 8;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+// split merge: each softmax warp loads the other splits' rows of its 32 rows
+// as 128-byte-swizzled 32 x 32-float boxes into its share of the (then idle)
+// K and V rings, up to kMergeRound partials at a time
+constexpr uint32_t kMergeWarpBytes = 2 * kStages * kTile / 4;     // 48 KB per softmax warp
+constexpr int kMergeRound = (int)(kMergeWarpBytes / 16384u);      // 3 partial quarters of 16 KB
 constexpr int kSBufs = 3;                       // score buffers: the QK product runs two tiles ahead
 // TMEM columns: S[b] at 128 b (P, bf16 pairs, over its first 64 once the
 // scores are read), O 384-511
@@ -101,7 +99,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <bool kBiased>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const __grid_constant__ CUtensorMap tmQ, AttnLaunch a) {
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -116,19 +114,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* o_done = p_full + 4;                        // [4]
     uint64_t* mma_done = o_done + 4;                      // both MMA issuers' last products
     uint64_t* q_full = mma_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
+    uint64_t* merge_full = q_full + 1;                    // [4] one per softmax warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(merge_full + 4);
+    int* ticket = reinterpret_cast<int*>(tmem_slot + 1);
 
     // grid (K/V head, query tile from the last, split): the longest query
-    // tiles (latest positions) are dispatched first; the splits of one
-    // (tile, head) form one cluster
+    // tiles (latest positions) are dispatched first
     const int h = blockIdx.x, tile = gridDim.y - 1 - blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
     const int* plan = a.plan + 8 * tile;
     const int row0 = plan[0], nrows = plan[1], umin = plan[2], n_full = plan[4], seq = plan[6];
-    // this CTA's chunk of the query tile's K/V tiles [0, plan n_total); a CTA
-    // whose chunk is empty still takes part in the cluster merge
-    const int chunk = (plan[5] + n_split - 1) / n_split;
+    // this CTA's chunk of the query tile's K/V tiles [0, plan n_total)
+    const int chunk = n_split > 1 ? a.chunk : plan[5];
     const int jb = split * chunk;
-    const int n_total = max(0, min(plan[5], jb + chunk) - jb);   // tiles handled here
+    const int n_total = min(plan[5], jb + chunk) - jb;           // tiles handled here
+    if (n_total <= 0) return;                                     // nothing to read, nothing to merge
+    const int n_live = min(n_split, (plan[5] + chunk - 1) / chunk);   // CTAs with work on this tile
     const int G = a.n_q_heads / a.n_kv_heads;
     const int P = 128 / G;
     const int head_index = (seq * a.n_layers + a.layer) * a.n_kv_heads + h;
@@ -142,12 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
         mbar_init(mma_done, 2);
         mbar_init(q_full, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&merge_full[i], 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmQ);
+        if (n_live > 1) prefetch_tmap(&tmP);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     int t_prod = 0;
-    if (warp == 0 && lane == 0 && n_total > 0) {
+    if (warp == 0 && lane == 0) {
         // P * G <= 128 rows of 128 bytes in each half (126 when G = 6)
         mbar_arrive_expect_tx(q_full, 2u * 128u * (uint32_t)(P * G));
         tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, h * G, row0);
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_total > 0) {
+        if (lane == 0) {
             for (int t = t_prod; t <= n_total && ok; ++t) ok = produce(t);
             if (!ok) {  // let every copy still in flight land before the CTA exits
                 mbar_wait(q_full, 0);
@@ -408,14 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[j & 3]);
         }
-        if (ok && n_total > 0 && !warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u))
-            ok = false;
-        const bool have = ok && n_total > 0;   // warp-uniform
-        if (n_split == 1) {
-            if (have) {
+        if (ok && !warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u)) ok = false;
+        __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
+        if (n_live == 1) {
+            if (ok) {
                 tc_fence_after();
                 const float inv = 1.0f / l_run;
-                __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
@@ -436,82 +436,146 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // stage the unnormalised O row and (running max in base 2, sum) for
-            // the cluster merge; the K ring is idle (every QK product was
-            // waited for through its scores, every copy through the products)
-            reinterpret_cast<float2*>(smem + kOffML)[m] = have ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
-            if (have) {
+            // ------------------------------------------------ split merge
+            const int pair = tile * a.n_kv_heads + h;
+            int* count = a.sync + pair;                                   // tickets taken
+            int* done = a.sync + (size_t)a.n_tiles * a.n_kv_heads + pair;  // partials stored
+            const int q4 = warp & 3;
+            if (warp == 2 && lane == 0) *ticket = atomicAdd(count, 1);
+            named_bar_sync(1, 128);
+            const bool last = *ticket == n_live - 1;   // CTA-uniform
+            if (!last) {
+                // unnormalised fp32 rows plus (running max in base 2, sum): the
+                // warp's 32 rows leave as four TMA stores of 32 x 32 floats
+                // staged in the idle K ring in the 128-byte swizzle
                 tc_fence_after();
-                const uint32_t row = sbase + kOffK + (uint32_t)m * kStageRowBytes;
+                const size_t slot = ((size_t)split * a.n_tiles + tile) * a.n_kv_heads + h;
+                uint8_t* stg = smem + kOffK + (uint32_t)q4 * 16384u;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     float o[16];
                     tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        st_shared_v4(row + (uint32_t)(4 * c + t) * 16u,
-                                     make_uint4(__float_as_uint(o[4 * t]), __float_as_uint(o[4 * t + 1]),
-                                                __float_as_uint(o[4 * t + 2]), __float_as_uint(o[4 * t + 3])));
+                    for (int t = 0; t < 4; ++t) {
+                        const int j = (c & 1) * 4 + t;   // 16-byte chunk within the box row
+                        const uint32_t addr = smem_u32(stg) + (uint32_t)(c >> 1) * 4096u + (uint32_t)lane * 128u +
+                                              ((uint32_t)(j ^ (lane & 7)) << 4);
+                        st_shared_v4(addr, make_uint4(__float_as_uint(o[4 * t]), __float_as_uint(o[4 * t + 1]),
+                                                      __float_as_uint(o[4 * t + 2]), __float_as_uint(o[4 * t + 3])));
+                    }
+                }
+                a.part_ml[(slot * 128 + m) * 2] = m_run;
+                a.part_ml[(slot * 128 + m) * 2 + 1] = l_run;
+                __threadfence();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int cb = 0; cb < 4; ++cb)
+                        tma_store_2d(&tmP, stg + cb * 4096, cb * 32, (int)(slot * 128) + 32 * q4);
+                    bulk_commit();
+                    bulk_wait_all();            // the rows are in global memory
+                    fence_proxy_async_global();
+                    __threadfence();
+                }
+                named_bar_sync(1, 128);
+                if (warp == 2 && lane == 0) {   // after every warp's stores and fences: a release
+                    __threadfence();
+                    atomicAdd(done, 1);
+                }
+            } else {
+                // every peer took its ticket after its main loop, so each is
+                // only storing its rows now: wait for all n_live - 1 of them
+                if (warp == 2 && lane == 0) *ticket = spin_ge_acquire(done, n_live - 1) ? 1 : 0;
+                named_bar_sync(1, 128);
+                if (!*ticket) ok = false;
+                __threadfence();
+                float acc[128];
+                tc_fence_after();
+                tmem_ld32x4(tmem + lane_base + kTmemO, acc);
+                // weights of the splits: w_s = 2^(m_s - M), L = sum_s w_s l_s; a
+                // split that saw no visible key of this row kept m = -inf and
+                // takes no part (its sum and rows are not numbers)
+                float M = m_run;
+                for (int sp = 0; sp < n_live; ++sp) {
+                    if (sp == split) continue;
+                    const size_t slot = ((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h;
+                    M = fmaxf(M, a.part_ml[(slot * 128 + m) * 2]);
+                }
+                const bool own_live = m_run != -INFINITY;
+                const float w_own = own_live ? ex2(m_run - M) : 0.f;
+                float L = own_live ? w_own * l_run : 0.f;
+#pragma unroll
+                for (int k = 0; k < 128; ++k) acc[k] = own_live ? acc[k] * w_own : 0.f;
+                const uint32_t region = sbase + kOffK + (uint32_t)q4 * kMergeWarpBytes;
+                uint32_t phase = 0;
+                // the other splits in rounds of up to kMergeRound
+                for (int next = 0; next < n_live && ok;) {
+                    int ids[kMergeRound];
+                    int n_in = 0;
+                    for (; next < n_live && n_in < kMergeRound; ++next)
+                        if (next != split) ids[n_in++] = next;
+                    if (n_in == 0) break;
+                    if (lane == 0) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(&merge_full[q4], (uint32_t)n_in * 16384u);
+                        for (int i = 0; i < n_in; ++i) {
+                            const int slot = (ids[i] * a.n_tiles + tile) * a.n_kv_heads + h;
+                            for (int cb = 0; cb < 4; ++cb)
+                                tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)i * 16384u +
+                                                (uint32_t)cb * 4096u,
+                                            &tmP, &merge_full[q4], cb * 32, slot * 128 + 32 * q4);
+                        }
+                    }
+                    float ws[kMergeRound];
+                    for (int i = 0; i < n_in; ++i) {
+                        const size_t slot = ((size_t)ids[i] * a.n_tiles + tile) * a.n_kv_heads + h;
+                        const float ms = a.part_ml[(slot * 128 + m) * 2];
+                        const float ls = a.part_ml[(slot * 128 + m) * 2 + 1];
+                        ws[i] = ms == -INFINITY ? 0.f : ex2(ms - M);
+                        if (ms != -INFINITY) L += ws[i] * ls;
+                    }
+                    if (!warp_wait(&merge_full[q4], phase)) {
+                        ok = false;
+                        break;
+                    }
+                    phase ^= 1u;
+                    for (int i = 0; i < n_in; ++i) {
+                        if (ws[i] == 0.f) continue;
+                        const uint32_t base = region + (uint32_t)i * 16384u + (uint32_t)lane * 128u;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            float4 v;
+                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                         : "r"(base + (uint32_t)(c >> 3) * 4096u +
+                                               ((uint32_t)((c & 7) ^ (lane & 7)) << 4)));
+                            acc[4 * c] += ws[i] * v.x;
+                            acc[4 * c + 1] += ws[i] * v.y;
+                            acc[4 * c + 2] += ws[i] * v.z;
+                            acc[4 * c + 3] += ws[i] * v.w;
+                        }
+                    }
+                    __syncwarp();   // the next round's loads reuse this warp's region
+                }
+                if (ok && row_valid) {
+                    const float inv = 1.0f / L;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        uint4 v;
+                        v.x = pack_bf16(acc[8 * c] * inv, acc[8 * c + 1] * inv);
+                        v.y = pack_bf16(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv);
+                        v.z = pack_bf16(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv);
+                        v.w = pack_bf16(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv);
+                        reinterpret_cast<uint4*>(out)[c] = v;
+                    }
+                }
+                named_bar_sync(1, 128);
+                if (warp == 2 && lane == 0) {   // every peer has counted itself: ready for the next launch
+                    *count = 0;
+                    *done = 0;
                 }
             }
         }
-    }
-    if (n_split > 1) {
-        // ------------------------------------------------------------ cluster merge
-        // every thread of every CTA of the cluster passes both barriers: the
-        // first publishes the staged rows, the second keeps each CTA (and so
-        // its shared memory) alive until every peer has read it
-        __syncwarp();
-        cluster_sync();
-        if (warp >= 2 && warp < 6 && row_valid) {
-            const uint32_t rank = cluster_rank();
-            float ms[kMaxClusterSplit], w[kMaxClusterSplit];
-            float M = -INFINITY;
-            const uint32_t ml_addr = sbase + kOffML + (uint32_t)m * 8u;
-#pragma unroll
-            for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
-                ms[sp] = -INFINITY;
-                w[sp] = 0.f;
-                if (sp < n_split) {
-                    const float2 v = ld_cluster_f2(cluster_map(ml_addr, (uint32_t)sp));
-                    ms[sp] = v.x;
-                    w[sp] = v.y;   // the split's sum, until the weights below
-                    M = fmaxf(M, v.x);
-                }
-            }
-            // a split whose keys all lie past this row's causal limit kept the
-            // max at -inf (its sum and O are not numbers): it takes no part
-            float L = 0.f;
-#pragma unroll
-            for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
-                const bool live = sp < n_split && ms[sp] != -INFINITY;
-                const float e = live ? ex2(ms[sp] - M) : 0.f;
-                if (live) L += e * w[sp];
-                w[sp] = e;
-            }
-            const float inv = 1.0f / L;
-            const int c0 = (32 * (int)rank) / n_split, c1 = (32 * ((int)rank + 1)) / n_split;   // 16-byte chunks
-            const uint32_t row = sbase + kOffK + (uint32_t)m * kStageRowBytes;
-            __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
-            for (int c = c0; c < c1; ++c) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int sp = 0; sp < kMaxClusterSplit; ++sp) {
-                    if (w[sp] == 0.f) continue;
-                    const float4 v = ld_cluster_f4(cluster_map(row + (uint32_t)c * 16u, (uint32_t)sp));
-                    acc.x += w[sp] * v.x;
-                    acc.y += w[sp] * v.y;
-                    acc.z += w[sp] * v.z;
-                    acc.w += w[sp] * v.w;
-                }
-                uint2 v;
-                v.x = pack_bf16(acc.x * inv, acc.y * inv);
-                v.y = pack_bf16(acc.z * inv, acc.w * inv);
-                reinterpret_cast<uint2*>(out)[c] = v;
-            }
-        }
-        __syncwarp();
-        cluster_sync();
     }
     if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
     tc_fence_before();
@@ -541,31 +605,9 @@ cudaError_t set_smem_attr() {
 }
 }  // namespace
 
-// Clusters of n CTAs of this kernel that the GPU holds at once (the CTAs of
-// a cluster run together on SMs of one GPC); 0 if it cannot say.
-int attn_tc_max_clusters(int n) {
-    static int cache[kMaxClusterSplit + 1] = {};
-    if (n < 1 || n > kMaxClusterSplit) return 0;
-    if (cache[n]) return cache[n];
-    if (set_smem_attr() != cudaSuccess) return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, (unsigned)n);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = (unsigned)n;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<false>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        clusters = 0;
-    }
-    cache[n] = clusters;
-    return clusters;
+size_t attn_tc_scratch_bytes(int n_split, int n_tiles, int n_kv_heads) {
+    if (n_split <= 1) return 0;
+    return (size_t)n_split * n_tiles * n_kv_heads * 128 * (128 + 2) * sizeof(float);
 }
 
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string* why) {
@@ -574,7 +616,7 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         if (why) *why = "tensor-core attention needs head_dim 128";
         return cudaErrorInvalidValue;
     }
-    const int n_split = std::max(1, std::min(a.n_split, kMaxClusterSplit));
+    const int n_split = (a.part_o && a.sync && a.n_split > 1) ? a.n_split : 1;
     CUtensorMap tk, tv;
     const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
     const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
@@ -586,36 +628,25 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
     if (e != cudaSuccess) return e;
     // Q [rows][H_q][128] as (dims, heads, rows): a {64, G, 128 / G} box is one
     // half of a query tile, rows p * G + i
-    CUtensorMap tq;
+    CUtensorMap tq, tp;
     const int G = a.n_q_heads / a.n_kv_heads;
     if (a.n_rows <= 0 ||
         !make_tmap_3d_bf16(&tq, a.q, 128, (uint64_t)a.n_q_heads, (uint64_t)a.n_rows, 256, (uint64_t)a.n_q_heads * 256,
                            64, (uint32_t)G, (uint32_t)(128 / G), why))
         return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.n_kv_heads, (unsigned)a.n_tiles, (unsigned)n_split);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    int n_attr = 0;
-    if (pdl_take()) {
-        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
-        ++n_attr;
-    }
-    if (n_split > 1) {
-        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-        attr[n_attr].val.clusterDim.x = 1;
-        attr[n_attr].val.clusterDim.y = 1;
-        attr[n_attr].val.clusterDim.z = (unsigned)n_split;
-        ++n_attr;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = n_attr;
-    if (fault_at("launch")) return cudaErrorLaunchFailure;   // injected: nothing is issued
-    if (a.alpha != 0.f || a.beta != 0.f) return cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tk, tv, tq, a);
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tk, tv, tq, a);
+    // the split partials: fp32 rows of 128, stored and loaded as 32 x 32 boxes
+    memset(&tp, 0, sizeof(tp));
+    if (n_split > 1 &&
+        !make_tmap_2d_f32_sw128(&tp, a.part_o, 128, (uint64_t)n_split * a.n_tiles * a.n_kv_heads * 128, 32, why))
+        return cudaErrorInvalidValue;
+    AttnLaunch b = a;
+    b.n_split = n_split;
+    dim3 grid((unsigned)a.n_kv_heads, (unsigned)a.n_tiles, (unsigned)n_split);
+    if (a.alpha != 0.f || a.beta != 0.f)
+        KVR_LAUNCH(attn_tc_kernel<true>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
+    else
+        KVR_LAUNCH(attn_tc_kernel<false>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
+    return cudaSuccess;
 }
 
 }  // namespace kvr

@@ -28,7 +28,7 @@ constexpr int kSimtKeysPerTile = 64;
 struct Selection {
     int32_t n_rows = 0, n_intervals = 0, n_tiles = 0;
     int32_t rows_per_tile = 0, keys_per_tile = 0;
-    int32_t attn_split = 1;   // CTAs per (query tile, K/V head) of the attention
+    int32_t attn_chunk = 1 << 30, attn_split = 1;   // K/V split of the attention
     std::vector<int32_t> counts, row_off, iv_count, iv_off, tile_count, tile_off;
     bool valid = false;
 };
@@ -64,6 +64,7 @@ struct kvr_cache_impl {
     float2* d_rope = nullptr;      // [capacity][head_dim/2] (cos, sin)
     int32_t* d_err = nullptr;      // [4]
     int32_t* d_map = nullptr;      // [batch][capacity] position -> row (carry selections)
+    int32_t* d_attn_sync = nullptr;  // [2][max_tiles][n_kv_heads] attention merge counters
     int32_t max_tiles = 0;
 
     // pinned staging for the position upload
@@ -217,14 +218,22 @@ struct AttnLaunch {
     int n_rows;                // packed rows of q and out
     float alpha, beta;
     int32_t* err;
-    int n_split;               // CTAs (one thread-block cluster) per (query tile, K/V head); 1 = unsplit
+    float* part_o;             // nullable: split partials [splits][tiles][H_kv][128][128]
+    float* part_ml;            // [splits][tiles][H_kv][128][2] (running max in base 2, sum)
+    int* sync;                 // [2][tiles][H_kv] merge counters, zero between launches
+    int chunk;                 // K/V tiles per CTA when split
+    int n_split;               // CTAs per (query tile, K/V head); 1 = unsplit
 };
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why);
 // Query tile geometry of the attention kernel for a model.
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile);
-// Split of each query tile's K/V range over the CTAs of one cluster, from the
-// per-tile K/V tile counts of a selection: n_split CTAs per (tile, head).
-void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* n_split);
+// Split of each query tile's K/V range over CTAs, from the per-tile K/V tile
+// counts of a selection: chunk tiles per CTA, n_split CTAs per (tile, head).
+void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split);
+// Scratch bytes of the split partials (0 = unsplit); never above
+// kAttnMaxSplitCTAs CTAs' worth.
+constexpr int kAttnMaxSplitCTAs = 4 * kNumSMs;
+size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_heads);
 
 // ---------------------------------------------------------------- dependent launch
 // Kernels of one library call run back to back on one stream.  Each kernel

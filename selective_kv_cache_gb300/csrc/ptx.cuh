@@ -104,6 +104,31 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // global writes may still be in flight; they are performed before the grid
 // completes)
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Order this thread's global accesses of the generic proxy with those of
+// the async proxy (bulk copies and TMA): between a completed bulk store and a
+// release that publishes it, and between an acquire and a bulk load of what
+// another CTA published.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Wait until *p >= target (acquire at GPU scope); false after the budget.
+__device__ __forceinline__ bool spin_ge_acquire(const int* p, int target, long long budget = kWaitLimitCycles) {
+    auto ld = [&]() {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        return v;
+    };
+    if (ld() >= target) return true;
+    const long long t0 = clock64();
+    while (ld() < target) {
+        if (clock64() - t0 > budget) return false;
+    }
+    return true;
+}
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

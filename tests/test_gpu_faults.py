@@ -41,7 +41,7 @@ def small():
     return small_bf16(n_layers=1, selection="isolated", n_select=40)
 
 
-@pytest.mark.parametrize("spec", ["alloc", "alloc:1", "alloc:5", "alloc:13"])
+@pytest.mark.parametrize("spec", ["alloc", "alloc:1", "alloc:5", "alloc:14"])
 def test_create_reports_enomem_and_frees_what_it_allocated(spec):
     w = small()
     K = torch.zeros((1, 1, 2, w.capacity, 128), dtype=torch.bfloat16, device="cuda")
