@@ -21,9 +21,10 @@ size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_hea
 // Pick the chunk size C that minimises the modelled time.  The model plays
 // out the hardware's dispatch: CTAs go to the SMs in launch order (K/V head
 // fastest, then the query tiles from the last, whose ranges are the longest,
-// then the split), each SM taking the next CTA when its last one ends; a CTA
-// costs ~6 tile-times of set-up plus one per K/V tile of its chunk (an empty
-// chunk almost nothing), and one more when it stores or merges split rows.
+// then the split), each of the kAttnCTAsPerSM slots of an SM taking the next
+// CTA when its last one ends; a CTA costs ~6 tile-times of set-up plus one per
+// K/V tile of its chunk (an empty chunk almost nothing), and one more when it
+// stores or merges split rows.
 // tile_kv[t] = K/V tiles of query tile t.
 void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
     *chunk = 1 << 30;
@@ -34,7 +35,7 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
     std::vector<double> sm_free;
     std::greater<double> later;
     auto makespan = [&](int C, int splits) {
-        sm_free.assign(kNumSMs, 0.0);
+        sm_free.assign(kNumSMs * kAttnCTAsPerSM, 0.0);
         for (int z = 0; z < splits; ++z)
             for (int t = (int)tile_kv.size() - 1; t >= 0; --t)
                 for (int y = 0; y < n_kv_heads; ++y) {

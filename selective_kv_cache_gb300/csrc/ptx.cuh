@@ -262,6 +262,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 64 consecutive columns of this thread's lane: two x32 loads, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+#define KVR_LD32(OFF, B)                                                                                           \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"    \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                       \
+                 : "=r"(B[0]), "=r"(B[1]), "=r"(B[2]), "=r"(B[3]), "=r"(B[4]), "=r"(B[5]), "=r"(B[6]),             \
+                   "=r"(B[7]), "=r"(B[8]), "=r"(B[9]), "=r"(B[10]), "=r"(B[11]), "=r"(B[12]), "=r"(B[13]),        \
+                   "=r"(B[14]), "=r"(B[15]), "=r"(B[16]), "=r"(B[17]), "=r"(B[18]), "=r"(B[19]), "=r"(B[20]),     \
+                   "=r"(B[21]), "=r"(B[22]), "=r"(B[23]), "=r"(B[24]), "=r"(B[25]), "=r"(B[26]), "=r"(B[27]),     \
+                   "=r"(B[28]), "=r"(B[29]), "=r"(B[30]), "=r"(B[31])                                             \
+                 : "r"(taddr + (OFF)) : "memory")
+    KVR_LD32(0u, r);
+    KVR_LD32(32u, (r + 32));
+#undef KVR_LD32
+    // the wait takes every destination register as an operand so no use of them
+    // can be scheduled above it
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]),
+                 "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                 "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+    asm volatile("" : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]),
+                 "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]),
+                 "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]),
+                 "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
+                 "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])::"memory");
+}
 // 128 consecutive columns of this thread's lane: four x32 loads, one wait.
 __device__ __forceinline__ void tmem_ld32x4(uint32_t taddr, float* v) {
     uint32_t* r = reinterpret_cast<uint32_t*>(v);

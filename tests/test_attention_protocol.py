@@ -5,23 +5,26 @@ The kernel's five roles are played out as coroutines under random
 interleavings, with TMA landings in any order and tensor-core products
 completing in issue order per issuing thread:
 
-  producer   steps t = 0..n: K_t and V_{t-1} on kv_full[t % 3]; before step
-             t >= 3 it waits for the slot's previous phase, for S_{t-3}
-             (s_full) and, for t >= 4, for the PV product of tile t - 4;
-  QK issuer  S_j = Q K_j^T into score buffer j % 3 once step j has landed and
-             (j >= 3) the PV product of tile j - 3 is done;
+  producer   steps t = 0..n: K_t and V_{t-1} on kv_full[t % KS]; before step
+             t >= KS it waits for the slot's previous phase, for S_{t-KS}
+             (s_full) and, for t >= KS + 1, for the PV product of tile
+             t - 1 - KS;
+  QK issuer  S_j = Q K_j^T into score buffer j % SB once step j has landed
+             and (j >= SB) the PV product of tile j - SB is done;
   PV issuer  O += P_j V_j once P_j (p_full[j & 3]) and step j + 1 are there;
   softmax    waits for S_j, sometimes for the previous PV (an O rescale),
              writes P_j over S_j; at the end waits for the last PV.
 
+KS (ring stages) and SB (score buffers) are the kernel's kStages and kSBufs:
+2 and 2 (64-key tiles, two CTAs per SM); the deeper 3 and 3 is checked too.
 An mbarrier poll succeeds when the barrier's completed-phase count has the
 other parity than the one asked for, so a waiter that falls two phases
 behind, or polls a phase two ahead, would be fooled: the model asserts that
 never happens, that no barrier is re-armed with a phase still open, and that
 no shared-memory slot or tensor-memory buffer is overwritten while a product
 or the softmax still reads it.  The variant without the producer's wait for
-S_{t-3} on the last (K-less) step is shown to alias, which is why that wait
-is unconditional in the kernel.
+S_{t-KS} on the last (K-less) step is shown to alias (at KS = 3), which is
+why that wait is unconditional in the kernel.
 """
 import random
 
@@ -32,7 +35,9 @@ class Alias(AssertionError):
     pass
 
 
-def simulate(n, seed, wait_s_on_last_step=True):
+def simulate(n, seed, wait_s_on_last_step=True, KS=2, SB=2):
+    """KS: K and V ring stages; SB: score buffers (the kernel's kStages and
+    kSBufs)."""
     R = random.Random(seed)
     done = {}                    # barrier -> completed phases
     fin = {"QK": set(), "PV": set(), "P": set(), "land": set()}
@@ -51,31 +56,31 @@ def simulate(n, seed, wait_s_on_last_step=True):
 
     def producer():
         for t in range(n + 1):
-            if t >= 3:
-                while not poll(("kv", t % 3), (t - 3) // 3):
+            if t >= KS:
+                while not poll(("kv", t % KS), (t - KS) // KS):
                     yield
                 if wait_s_on_last_step or t < n:
-                    while not poll(("s", (t - 3) % 3), (t - 3) // 3):
+                    while not poll(("s", (t - KS) % SB), (t - KS) // SB):
                         yield
-                if t >= 4:
-                    while not poll(("o", (t - 4) & 3), (t - 4) >> 2):
+                if t >= KS + 1:
+                    while not poll(("o", (t - 1 - KS) & 3), (t - 1 - KS) >> 2):
                         yield
-            assert count(("kv", t % 3)) == t // 3, "barrier re-armed with a phase open"
-            if 3 <= t < n:
-                assert t - 3 in fin["QK"], "K slot overwritten before its product read it"
-            if t >= 4:
-                assert t - 4 in fin["PV"], "V slot overwritten before its product read it"
+            assert count(("kv", t % KS)) == t // KS, "barrier re-armed with a phase open"
+            if KS <= t < n:
+                assert t - KS in fin["QK"], "K slot overwritten before its product read it"
+            if t >= KS + 1:
+                assert t - 1 - KS in fin["PV"], "V slot overwritten before its product read it"
             tma.append(t)
             yield
 
     def qk_issuer():
         for j in range(n):
-            while not poll(("kv", j % 3), j // 3):
+            while not poll(("kv", j % KS), j // KS):
                 yield
-            if j >= 3:
-                while not poll(("o", (j - 3) & 3), (j - 3) >> 2):
+            if j >= SB:
+                while not poll(("o", (j - SB) & 3), (j - SB) >> 2):
                     yield
-                assert j - 3 in fin["PV"] and j - 3 in fin["P"], "score buffer reused too early"
+                assert j - SB in fin["PV"] and j - SB in fin["P"], "score buffer reused too early"
             qk_q.append(j)
             yield
 
@@ -83,7 +88,7 @@ def simulate(n, seed, wait_s_on_last_step=True):
         for j in range(n):
             while not poll(("p", j & 3), j >> 2):
                 yield
-            while not poll(("kv", (j + 1) % 3), (j + 1) // 3):
+            while not poll(("kv", (j + 1) % KS), (j + 1) // KS):
                 yield
             assert j in fin["P"] and j + 1 in fin["land"]
             pv_q.append(j)
@@ -91,13 +96,13 @@ def simulate(n, seed, wait_s_on_last_step=True):
 
     def softmax():
         for j in range(n):
-            while not poll(("s", j % 3), j // 3):
+            while not poll(("s", j % SB), j // SB):
                 yield
             assert j in fin["QK"]
             if j > 0 and R.random() < 0.3:   # an O rescale waits for the previous PV
                 while not poll(("o", (j - 1) & 3), (j - 1) >> 2):
                     yield
-            assert j < 3 or j - 3 in fin["PV"], "P written over a P still being read"
+            assert j < SB or j - SB in fin["PV"], "P written over a P still being read"
             fin["P"].add(j)
             done[("p", j & 3)] = count(("p", j & 3)) + 1
             yield
@@ -121,11 +126,11 @@ def simulate(n, seed, wait_s_on_last_step=True):
         elif kind == "tma":
             t = tma.pop(R.randrange(len(tma)))
             fin["land"].add(t)
-            done[("kv", t % 3)] = count(("kv", t % 3)) + 1
+            done[("kv", t % KS)] = count(("kv", t % KS)) + 1
         elif kind == "qk":
             j = qk_q.pop(0)
             fin["QK"].add(j)
-            done[("s", j % 3)] = count(("s", j % 3)) + 1
+            done[("s", j % SB)] = count(("s", j % SB)) + 1
         else:
             j = pv_q.pop(0)
             fin["PV"].add(j)
@@ -134,9 +139,12 @@ def simulate(n, seed, wait_s_on_last_step=True):
 
 
 @pytest.mark.parametrize("n", list(range(0, 12)))
-def test_protocol_has_no_alias_deadlock_or_overwrite(n):
-    for seed in range(600):
-        simulate(n, seed)
+@pytest.mark.parametrize("KS,SB", [(2, 2), (3, 3)])
+def test_protocol_has_no_alias_deadlock_or_overwrite(n, KS, SB):
+    """(2, 2) is the kernel's depth (64-key tiles, two CTAs per SM); (3, 3) the
+    deeper form the same protocol also supports."""
+    for seed in range(400):
+        simulate(n, seed, KS=KS, SB=SB)
 
 
 def test_last_step_without_score_wait_aliases():
@@ -145,7 +153,7 @@ def test_last_step_without_score_wait_aliases():
     hits = 0
     for seed in range(600):
         try:
-            simulate(3, seed, wait_s_on_last_step=False)
+            simulate(3, seed, wait_s_on_last_step=False, KS=3, SB=3)
         except Alias:
             hits += 1
     assert hits > 0
