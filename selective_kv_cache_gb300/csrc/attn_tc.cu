@@ -503,86 +503,102 @@ __global__ void __maxnreg__(144)
                 __threadfence();
                 // weights of the splits: w_s = 2^(m_s - M), L = sum_s w_s l_s; a
                 // split that saw no visible key of this row kept m = -inf and
-                // takes no part (its sum and rows are not numbers).  The merged
-                // rows build up in the tensor-memory accumulator, 16 columns at
-                // a time, so few registers are live.
-                float M = m_run;
+                // takes no part (its sum and rows are not numbers).  The sums
+                // run in split order whichever CTA merges, with products and
+                // sums rounded separately, so the output does not depend on
+                // which CTA came last.  The merged rows build up 16 columns at a
+                // time in the (now idle) score-buffer columns of tensor memory,
+                // beside this CTA's own rows, so few registers are live.
+                float msp[8], lsp[8];   // n_live <= n_split <= 8 is not assumed: read on demand past 8
+                float M = -INFINITY;
                 for (int sp = 0; sp < n_live; ++sp) {
-                    if (sp == split) continue;
-                    const size_t slot = ((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h;
-                    M = fmaxf(M, a.part_ml[(slot * 128 + m) * 2]);
+                    float ms = m_run, ls = l_run;
+                    if (sp != split) {
+                        const size_t slot = ((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h;
+                        ms = a.part_ml[(slot * 128 + m) * 2];
+                        ls = a.part_ml[(slot * 128 + m) * 2 + 1];
+                    }
+                    if (sp < 8) {
+                        msp[sp] = ms;
+                        lsp[sp] = ls;
+                    }
+                    M = fmaxf(M, ms);
                 }
-                const bool own_live = m_run != -INFINITY;
-                const float w_own = own_live ? ex2(m_run - M) : 0.f;
-                float L = own_live ? w_own * l_run : 0.f;
+                auto ml_of = [&](int sp, float* ms, float* ls) {
+                    if (sp < 8) {
+                        *ms = msp[sp];
+                        *ls = lsp[sp];
+                    } else if (sp == split) {
+                        *ms = m_run;
+                        *ls = l_run;
+                    } else {
+                        const size_t slot = ((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h;
+                        *ms = a.part_ml[(slot * 128 + m) * 2];
+                        *ls = a.part_ml[(slot * 128 + m) * 2 + 1];
+                    }
+                };
+                float L = 0.f;
+                for (int sp = 0; sp < n_live; ++sp) {
+                    float ms, ls;
+                    ml_of(sp, &ms, &ls);
+                    if (ms != -INFINITY) L = __fadd_rn(L, __fmul_rn(ex2(ms - M), ls));
+                }
                 tc_fence_after();
                 const uint32_t region = sbase + kOffK + (uint32_t)q4 * kMergeWarpBytes;
+                const uint32_t acc_cols = tmem + lane_base;   // the score buffers' 128 columns
                 uint32_t phase = 0;
-                bool first = true;   // the accumulator still holds this CTA's own unscaled rows
-                // the other splits in rounds of up to kMergeRound
-                for (int next = 0; next < n_live && ok;) {
-                    int ids[kMergeRound];
-                    int n_in = 0;
-                    for (; next < n_live && n_in < kMergeRound; ++next)
-                        if (next != split) ids[n_in++] = next;
-                    if (n_in == 0) break;
-                    if (lane == 0) {
-                        fence_proxy_async_global();
-                        mbar_arrive_expect_tx(&merge_full[q4], (uint32_t)n_in * 16384u);
-                        for (int i = 0; i < n_in; ++i) {
-                            const int slot = (ids[i] * a.n_tiles + tile) * a.n_kv_heads + h;
+                for (int sp = 0; sp < n_live && ok; ++sp) {
+                    float ms, ls;
+                    ml_of(sp, &ms, &ls);
+                    const float w = ms == -INFINITY ? 0.f : ex2(ms - M);
+                    const bool own = sp == split;
+                    if (!own) {
+                        if (lane == 0) {
+                            const int slot = (sp * a.n_tiles + tile) * a.n_kv_heads + h;
+                            fence_proxy_async_global();
+                            mbar_arrive_expect_tx(&merge_full[q4], 16384u);
                             for (int cb = 0; cb < 4; ++cb)
-                                tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)i * 16384u +
-                                                (uint32_t)cb * 4096u,
+                                tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)cb * 4096u,
                                             &tmP, &merge_full[q4], cb * 32, slot * 128 + 32 * q4);
                         }
+                        if (!warp_wait(&merge_full[q4], phase)) {
+                            ok = false;
+                            break;
+                        }
+                        phase ^= 1u;
                     }
-                    float ws[kMergeRound];
-                    for (int i = 0; i < n_in; ++i) {
-                        const size_t slot = ((size_t)ids[i] * a.n_tiles + tile) * a.n_kv_heads + h;
-                        const float ms = a.part_ml[(slot * 128 + m) * 2];
-                        const float ls = a.part_ml[(slot * 128 + m) * 2 + 1];
-                        ws[i] = ms == -INFINITY ? 0.f : ex2(ms - M);
-                        if (ms != -INFINITY) L += ws[i] * ls;
-                    }
-                    if (!warp_wait(&merge_full[q4], phase)) {
-                        ok = false;
-                        break;
-                    }
-                    phase ^= 1u;
+                    const uint32_t base = region + (uint32_t)lane * 128u;
                     for (int c = 0; c < 8; ++c) {   // 16 output columns at a time
-                        float o[16];
-                        tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) o[k] = first ? (own_live ? o[k] * w_own : 0.f) : o[k];
-                        for (int i = 0; i < n_in; ++i) {
-                            if (ws[i] == 0.f) continue;
-                            const uint32_t base = region + (uint32_t)i * 16384u + (uint32_t)lane * 128u;
+                        float acc[16], v[16];
+                        if (sp > 0) tmem_ld16(acc_cols + (uint32_t)c * 16u, acc);
+                        if (own) {
+                            tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, v);
+                        } else {
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
                                 const int q16 = 4 * c + t;   // 16-byte chunk of the row
-                                float4 v;
                                 asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                             : "=f"(v[4 * t]), "=f"(v[4 * t + 1]), "=f"(v[4 * t + 2]),
+                                               "=f"(v[4 * t + 3])
                                              : "r"(base + (uint32_t)(q16 >> 3) * 4096u +
                                                    ((uint32_t)((q16 & 7) ^ (lane & 7)) << 4)));
-                                o[4 * t] += ws[i] * v.x;
-                                o[4 * t + 1] += ws[i] * v.y;
-                                o[4 * t + 2] += ws[i] * v.z;
-                                o[4 * t + 3] += ws[i] * v.w;
                             }
                         }
-                        tmem_st16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float term = w == 0.f ? 0.f : __fmul_rn(w, v[k]);
+                            acc[k] = sp > 0 ? __fadd_rn(acc[k], term) : term;
+                        }
+                        tmem_st16(acc_cols + (uint32_t)c * 16u, acc);
                     }
-                    first = false;
-                    __syncwarp();   // the next round's loads reuse this warp's region
+                    __syncwarp();   // the next split's loads reuse this warp's region
                 }
                 if (ok) {
                     const float inv = 1.0f / L;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         float o[16];
-                        tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
+                        tmem_ld16(acc_cols + (uint32_t)c * 16u, o);
                         if (row_valid) {
                             uint4 v0, v1;
                             v0.x = pack_bf16(o[0] * inv, o[1] * inv);
