@@ -7,17 +7,15 @@
 // Repair for Evolving Contexts", Sec. 13.2, Eq. 22, and Eqs. 23-24 for the
 // per-query-tile K/V tile counts that bound the loop.)
 //
-// One CTA per (query tile, K/V head, K/V chunk), two CTAs per SM (97 KB of
-// shared memory and 256 tensor-memory columns each), so one CTA's set-up,
-// merge and tail overlap the other's main loop and two softmax warps share
-// each scheduler.  The 128 MMA rows are the tile's positions times the G
-// query heads of that K/V head (row = p*G + i), so all of them read the same
-// K/V tiles and one causal limit g_p serves a whole group.  Per 64-key tile:
+// One CTA per (query tile, K/V head, K/V chunk).  The 128 MMA rows are the
+// tile's positions times the G query heads of that K/V head (row = p*G + i),
+// so all of them read the same K/V tiles and one causal limit g_p serves a
+// whole group.  Per 128-key tile:
 //   warp 0      TMA: K and V tiles (two 64-column boxes each, 128-B swizzle)
-//               into 2-stage rings, K one tile ahead of V; keys >= n_tokens
+//               into 3-stage rings, K one tile ahead of V; keys >= n_tokens
 //               arrive as zeros;
-//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers,
-//               up to two tiles ahead of the PV product;
+//   warp 1      tcgen05.mma: S = Q K^T into one of three TMEM score buffers,
+//               up to three tiles ahead of the PV product;
 //   warp 6      tcgen05.mma: O += P V into the TMEM output accumulator (V
 //               read MN-major straight from its cache layout);
 //   warps 2-5   one thread per row: scores from TMEM, scale + bias + causal
@@ -47,29 +45,23 @@ namespace kvr {
 namespace {
 
 constexpr int kThreads = 224;
-constexpr int kKeys = 64;                       // keys per K/V tile
-constexpr uint32_t kQHalf = 16384;              // Q: 128 rows x 128 B per 64-dim half
-constexpr uint32_t kQTile = 2 * kQHalf;
-constexpr uint32_t kKVHalf = kKeys * 128;       // K or V: 64 keys x 128 B per 64-dim half
-constexpr uint32_t kKVTile = 2 * kKVHalf;       // 64 x 128 bf16
-constexpr int kStages = 2;                      // K and V ring depth; K runs one tile ahead of V
+constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
+constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
+constexpr int kStages = 3;                      // K and V ring depth; K runs one tile ahead of V
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kQTile;
-constexpr uint32_t kOffV = kOffK + kStages * kKVTile;
-constexpr uint32_t kOffBar = kOffV + kStages * kKVTile;
+constexpr uint32_t kOffK = kTile;
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 // split merge: each softmax warp loads the other splits' rows of its 32 rows
 // as 128-byte-swizzled 32 x 32-float boxes into its share of the (then idle)
-// K and V rings, kMergeRound partials at a time
-constexpr uint32_t kMergeWarpBytes = 2 * kStages * kKVTile / 4;   // 16 KB per softmax warp
-constexpr int kMergeRound = (int)(kMergeWarpBytes / 16384u);      // one partial quarter of 16 KB
-static_assert(kMergeRound >= 1, "the merge needs room for one partial quarter per warp");
-constexpr int kSBufs = 2;                       // score buffers: the QK product runs up to two tiles ahead
-// TMEM columns: S[b] at 64 b (P, bf16 pairs, over its first 32 once the
-// scores are read), O 128-255
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCols = kKeys;
-constexpr uint32_t kTmemO = kSBufs * kSCols;
+// K and V rings, kMergeRound splits per load round
+constexpr uint32_t kMergeWarpBytes = 2 * kStages * kTile / 4;     // 48 KB per softmax warp
+constexpr int kMergeRound = (int)(kMergeWarpBytes / 16384u);      // 3 partial quarters of 16 KB
+constexpr int kSBufs = 3;                       // score buffers: the QK product runs two tiles ahead
+// TMEM columns: S[b] at 128 b (P, bf16 pairs, over its first 64 once the
+// scores are read), O 384-511
+constexpr uint32_t kTmemO = 384;
 constexpr float kRescale = 8.0f;                // log2 of the largest P before O is rescaled
 
 // max of three (one instruction on sm_100 and later)
@@ -105,7 +97,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // kBiased: the alpha/beta logit bias is on (the mask words are read); the
 // unbiased instance carries none of that code.
 template <bool kBiased>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP, AttnLaunch a) {
     extern __shared__ uint8_t smem_raw[];
@@ -160,7 +152,7 @@ __global__ void __maxnreg__(144)
         if (n_live > 1) prefetch_tmap(&tmP);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
 
@@ -173,9 +165,9 @@ __global__ void __maxnreg__(144)
     if (row_valid) g = a.U[row0 + p];
     // K/V producer, steps t = 0 .. n_total: K_t and V_{t-1} on one barrier,
     // so K stays one tile ahead of V.  The ring slots are freed by the
-    // signals the products already send: K_t replaces K_{t-2}, read by the
-    // QK product of tile t - 2 (s_full); V_{t-1} replaces V_{t-3}, read by the
-    // PV product of tile t - 3 (o_done).  The Q tile (two boxes of 64 dims x
+    // signals the products already send: K_t replaces K_{t-3}, read by the
+    // QK product of tile t - 3 (s_full); V_{t-1} replaces V_{t-4}, read by the
+    // PV product of tile t - 4 (o_done).  The Q tile (two boxes of 64 dims x
     // G heads x P positions, landing as rows p * G + i) and the first two
     // steps go out before the block-wide barrier, under the tensor-memory
     // allocation.
@@ -183,28 +175,26 @@ __global__ void __maxnreg__(144)
     auto produce = [&](int t) -> bool {
         const int st = t % kStages;
         if (t >= kStages) {
-            // The slot's barrier finished its previous phase (step t - 2), and
+            // The slot's barrier finished its previous phase (step t - 3), and
             // every thread that polls that phase has seen it: the QK issuer
-            // (its product S_{t-2} is done, which also frees K_{t-2}'s slot)
-            // and the PV issuer (its product of tile t - 3 is done, which
-            // frees V_{t-3}'s slot).  Only then is the barrier re-armed.
+            // (its product S_{t-3} is done, which also frees K_{t-3}'s slot)
+            // and the PV issuer (its product of tile t - 4 is done, which
+            // frees V_{t-4}'s slot).  Only then is the barrier re-armed.
             if (!mbar_wait(&kv_full[st], (uint32_t)((t - kStages) / kStages) & 1u) ||
-                !mbar_wait(&s_full[(t - kStages) % kSBufs], (uint32_t)((t - kStages) / kSBufs) & 1u))
+                !mbar_wait(&s_full[(t - 3) % kSBufs], (uint32_t)((t - 3) / kSBufs) & 1u))
                 return false;
-            if (t >= kStages + 1 &&
-                !mbar_wait(&o_done[(t - 1 - kStages) & 3], (uint32_t)((t - 1 - kStages) >> 2) & 1u))
-                return false;
+            if (t >= 4 && !mbar_wait(&o_done[(t - 4) & 3], (uint32_t)((t - 4) >> 2) & 1u)) return false;
         }
-        mbar_arrive_expect_tx(&kv_full[st], (t < n_total ? kKVTile : 0u) + (t >= 1 ? kKVTile : 0u));
+        mbar_arrive_expect_tx(&kv_full[st], (t < n_total ? kTile : 0u) + (t >= 1 ? kTile : 0u));
         if (t < n_total) {
-            uint8_t* kd = smem + kOffK + st * kKVTile;
-            tma_load_3d(kd, &tmK, &kv_full[st], 0, (jb + t) * kKeys, head_index);
-            tma_load_3d(kd + kKVHalf, &tmK, &kv_full[st], 64, (jb + t) * kKeys, head_index);
+            uint8_t* kd = smem + kOffK + st * kTile;
+            tma_load_3d(kd, &tmK, &kv_full[st], 0, (jb + t) * 128, head_index);
+            tma_load_3d(kd + kHalf, &tmK, &kv_full[st], 64, (jb + t) * 128, head_index);
         }
         if (t >= 1) {
-            uint8_t* vd = smem + kOffV + ((t - 1) % kStages) * kKVTile;
-            tma_load_3d(vd, &tmV, &kv_full[st], 0, (jb + t - 1) * kKeys, head_index);
-            tma_load_3d(vd + kKVHalf, &tmV, &kv_full[st], 64, (jb + t - 1) * kKeys, head_index);
+            uint8_t* vd = smem + kOffV + ((t - 1) % kStages) * kTile;
+            tma_load_3d(vd, &tmV, &kv_full[st], 0, (jb + t - 1) * 128, head_index);
+            tma_load_3d(vd + kHalf, &tmV, &kv_full[st], 64, (jb + t - 1) * 128, head_index);
         }
         ++issued;
         return true;
@@ -214,7 +204,7 @@ __global__ void __maxnreg__(144)
         // P * G <= 128 rows of 128 bytes in each half (126 when G = 6)
         mbar_arrive_expect_tx(q_full, 2u * 128u * (uint32_t)(P * G));
         tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, h * G, row0);
-        tma_load_3d(smem + kOffQ + kQHalf, &tmQ, q_full, 64, h * G, row0);
+        tma_load_3d(smem + kOffQ + kHalf, &tmQ, q_full, 64, h * G, row0);
         for (; t_prod < 2 && t_prod <= n_total && ok; ++t_prod) ok = produce(t_prod);
     }
     tc_fence_before();
@@ -239,16 +229,16 @@ __global__ void __maxnreg__(144)
         // Two threads feed the tensor pipe: warp 1 the score products S_j =
         // Q K_j^T, warp 6 the output products O += P_j V_j.  An issuing thread
         // stalls while the pipe's short queue is full, so while one waits on a
-        // barrier the other keeps the pipe busy.  The scores run up to two
-        // tiles ahead: S_j goes into buffer j % 2 once the PV product of tile
-        // j - 2 has read the P stored over that buffer's scores.  Each thread
+        // barrier the other keeps the pipe busy.  The scores run up to three
+        // tiles ahead: S_j goes into buffer j % 3 once the PV product of tile
+        // j - 3 has read the P stored over that buffer's scores.  Each thread
         // commits its own products.
         if (lane == 0) {
             auto step_landed = [&](int t) {
                 return mbar_wait(&kv_full[t % kStages], (uint32_t)(t / kStages) & 1u);
             };
             if (warp == 1) {
-                const uint32_t idesc_s = idesc_bf16(128, kKeys, 0, 0);
+                const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
                 if (n_total > 0) ok = mbar_wait(q_full, 0);
                 for (int j = 0; ok && j < n_total; ++j) {
                     if (!step_landed(j) ||   // K_j
@@ -257,13 +247,12 @@ __global__ void __maxnreg__(144)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + (uint32_t)(j % kStages) * kKVTile;
-                    const uint32_t d = tmem + (uint32_t)(j % kSBufs) * kSCols;
+                    const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + (uint32_t)(j % kStages) * kTile;
+                    const uint32_t d = tmem + (uint32_t)(j % kSBufs) * 128u;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {   // K = 16 dims per product
-                        const uint32_t qo = (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u;
-                        const uint32_t ko = (uint32_t)(kk >> 2) * kKVHalf + (uint32_t)(kk & 3) * 32u;
-                        mma_bf16(d, sdesc_sw128(qa + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024), idesc_s, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+                        mma_bf16(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
                     }
                     mma_commit(&s_full[j % kSBufs]);
                 }
@@ -276,12 +265,12 @@ __global__ void __maxnreg__(144)
                     }
                     tc_fence_after();
                     // O += P V_j: P over the scores of tile j
-                    const uint32_t pt = tmem + (uint32_t)(j % kSBufs) * kSCols;
-                    const uint32_t va = sbase + kOffV + (uint32_t)(j % kStages) * kKVTile;
+                    const uint32_t pt = tmem + (uint32_t)(j % kSBufs) * 128u;
+                    const uint32_t va = sbase + kOffV + (uint32_t)(j % kStages) * kTile;
 #pragma unroll
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {   // K = 16 keys per product
+                    for (int kk = 0; kk < 8; ++kk) {
                         mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)kk * 8u,
-                                    sdesc_sw128(va + (uint32_t)kk * 2048u, kKVHalf, 1024), idesc_o, (j > 0 || kk > 0));
+                                    sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
                     }
                     mma_commit(&o_done[j & 3]);
                 }
@@ -307,17 +296,16 @@ __global__ void __maxnreg__(144)
         bool s_ready = false;
         // mask words of the tile, loaded one tile ahead so their latency hides
         // behind the previous tile's work
-        constexpr int kWords = kKeys / 32;   // mask words per tile
-        uint32_t lw[kWords] = {}, sw[kWords] = {};
+        uint32_t lw[4] = {0u, 0u, 0u, 0u}, sw[4] = {0u, 0u, 0u, 0u};
         auto load_words = [&](int key0, uint32_t* l, uint32_t* k) {
 #pragma unroll
-            for (int t = 0; t < kWords; ++t) {
+            for (int t = 0; t < 4; ++t) {
                 const int wd = (key0 >> 5) + t;
                 l[t] = wd < a.words ? loc[wd] : 0u;
                 k[t] = wd < a.words ? snk[wd] : 0u;
             }
         };
-        if (biased && n_total > 0) load_words(jb * kKeys, lw, sw);
+        if (biased && n_total > 0) load_words(jb * 128, lw, sw);
         for (int j = 0; j < n_total; ++j) {
             const int sb = j % kSBufs;
             if (__any_sync(0xffffffffu, !s_ready) && !warp_wait(&s_full[sb], (uint32_t)(j / kSBufs) & 1u)) {
@@ -325,17 +313,17 @@ __global__ void __maxnreg__(144)
                 break;
             }
             tc_fence_after();
-            float s[kKeys];
-            tmem_ld32x2(tmem + lane_base + (uint32_t)sb * kSCols, s);
+            float s[128];
+            tmem_ld32x4(tmem + lane_base + (uint32_t)sb * 128u, s);
 
-            const int key0 = (jb + j) * kKeys;
+            const int key0 = (jb + j) * 128;
             const bool masked = jb + j >= n_full;
             if (biased) {
                 // the mask words are the same for every row of the tile, so the
                 // branches are warp-uniform: words with no bit set cost nothing,
                 // all-local words one add per key
 #pragma unroll
-                for (int t = 0; t < kWords; ++t) {
+                for (int t = 0; t < 4; ++t) {
                     if ((lw[t] | sw[t]) == 0u) continue;
                     if (sw[t] == 0u && lw[t] == 0xffffffffu) {
 #pragma unroll
@@ -353,7 +341,7 @@ __global__ void __maxnreg__(144)
             if (masked) {
                 const int lim = g - key0;   // keys k > lim are in the row's future
 #pragma unroll
-                for (int k = 0; k < kKeys; ++k)
+                for (int k = 0; k < 128; ++k)
                     if (k > lim) s[k] = -INFINITY;
             }
             // row max over 8 independent chains of 3-input maxima
@@ -362,11 +350,11 @@ __global__ void __maxnreg__(144)
             for (int i = 0; i < 8; ++i) {
                 mx[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-                for (int t = 1; t < kKeys / 16; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
+                for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
             }
             const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
             s_ready = j + 1 < n_total && mbar_test(&s_full[(j + 1) % kSBufs], (uint32_t)((j + 1) / kSBufs) & 1u);
-            if (biased && j + 1 < n_total) load_words(key0 + kKeys, lw, sw);
+            if (biased && j + 1 < n_total) load_words(key0 + 128, lw, sw);
             // O is rescaled only after the previous PV has finished.  P_j goes
             // over the scores just read; the buffer's earlier P (tile j - 3)
             // was read before S_j's product was issued, so P_j needs no wait.
@@ -398,11 +386,11 @@ __global__ void __maxnreg__(144)
             // P goes to tensor memory as the PV product's A operand: column c of
             // the row holds keys 2c, 2c+1 as packed bf16
             const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
-            const uint32_t ptm = tmem + lane_base + (uint32_t)sb * kSCols;
+            const uint32_t ptm = tmem + lane_base + (uint32_t)sb * 128u;
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -509,7 +497,7 @@ __global__ void __maxnreg__(144)
                 // which CTA came last.  The merged rows build up 16 columns at a
                 // time in the (now idle) score-buffer columns of tensor memory,
                 // beside this CTA's own rows, so few registers are live.
-                float msp[8], lsp[8];   // n_live <= n_split <= 8 is not assumed: read on demand past 8
+                float msp[8], lsp[8];   // the first 8 splits' (max, sum); later ones are read again when used
                 float M = -INFINITY;
                 for (int sp = 0; sp < n_live; ++sp) {
                     float ms = m_run, ls = l_run;
@@ -545,21 +533,31 @@ __global__ void __maxnreg__(144)
                 }
                 tc_fence_after();
                 const uint32_t region = sbase + kOffK + (uint32_t)q4 * kMergeWarpBytes;
-                const uint32_t acc_cols = tmem + lane_base;   // the score buffers' 128 columns
+                const uint32_t acc_cols = tmem + lane_base;   // the first score buffer's 128 columns
                 uint32_t phase = 0;
+                const int n_other = n_live - 1;
                 for (int sp = 0; sp < n_live && ok; ++sp) {
                     float ms, ls;
                     ml_of(sp, &ms, &ls);
                     const float w = ms == -INFINITY ? 0.f : ex2(ms - M);
                     const bool own = sp == split;
-                    if (!own) {
+                    // the other splits land kMergeRound at a time, in split order
+                    const int k = sp - (sp > split ? 1 : 0);   // rank among the other splits
+                    if (!own && k % kMergeRound == 0) {
+                        __syncwarp();   // the previous round's rows are all read
+                        const int n_in = min(kMergeRound, n_other - k);
                         if (lane == 0) {
-                            const int slot = (sp * a.n_tiles + tile) * a.n_kv_heads + h;
                             fence_proxy_async_global();
-                            mbar_arrive_expect_tx(&merge_full[q4], 16384u);
-                            for (int cb = 0; cb < 4; ++cb)
-                                tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)cb * 4096u,
-                                            &tmP, &merge_full[q4], cb * 32, slot * 128 + 32 * q4);
+                            mbar_arrive_expect_tx(&merge_full[q4], (uint32_t)n_in * 16384u);
+                            for (int i = 0; i < n_in; ++i) {
+                                const int other = k + i;
+                                const int s_id = other + (other >= split ? 1 : 0);
+                                const int slot = (s_id * a.n_tiles + tile) * a.n_kv_heads + h;
+                                for (int cb = 0; cb < 4; ++cb)
+                                    tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)i * 16384u +
+                                                    (uint32_t)cb * 4096u,
+                                                &tmP, &merge_full[q4], cb * 32, slot * 128 + 32 * q4);
+                            }
                         }
                         if (!warp_wait(&merge_full[q4], phase)) {
                             ok = false;
@@ -567,7 +565,7 @@ __global__ void __maxnreg__(144)
                         }
                         phase ^= 1u;
                     }
-                    const uint32_t base = region + (uint32_t)lane * 128u;
+                    const uint32_t base = region + (uint32_t)(own ? 0 : k % kMergeRound) * 16384u + (uint32_t)lane * 128u;
                     for (int c = 0; c < 8; ++c) {   // 16 output columns at a time
                         float acc[16], v[16];
                         if (sp > 0) tmem_ld16(acc_cols + (uint32_t)c * 16u, acc);
@@ -585,13 +583,12 @@ __global__ void __maxnreg__(144)
                             }
                         }
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float term = w == 0.f ? 0.f : __fmul_rn(w, v[k]);
-                            acc[k] = sp > 0 ? __fadd_rn(acc[k], term) : term;
+                        for (int e = 0; e < 16; ++e) {
+                            const float term = w == 0.f ? 0.f : __fmul_rn(w, v[e]);
+                            acc[e] = sp > 0 ? __fadd_rn(acc[e], term) : term;
                         }
                         tmem_st16(acc_cols + (uint32_t)c * 16u, acc);
                     }
-                    __syncwarp();   // the next split's loads reuse this warp's region
                 }
                 if (ok) {
                     const float inv = 1.0f / L;
@@ -628,7 +625,7 @@ __global__ void __maxnreg__(144)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -642,9 +639,6 @@ cudaError_t set_smem_attr() {
     if (!attr) {
         for (auto* f : {attn_tc_kernel<false>, attn_tc_kernel<true>}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-            if (e != cudaSuccess) return e;
-            // two CTAs per SM need the largest shared-memory carve-out
-            e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             if (e != cudaSuccess) return e;
         }
         attr = true;
@@ -668,11 +662,9 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
     CUtensorMap tk, tv;
     const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
     const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
-    if (!make_tmap_3d_bf16(&tk, a.k_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, kKeys, 1,
-                           why))
+    if (!make_tmap_3d_bf16(&tk, a.k_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
         return cudaErrorInvalidValue;
-    if (!make_tmap_3d_bf16(&tv, a.v_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, kKeys, 1,
-                           why))
+    if (!make_tmap_3d_bf16(&tv, a.v_base, 128, (uint64_t)a.n_tokens, heads, row_bytes, head_bytes, 64, 128, 1, why))
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_attr();
     if (e != cudaSuccess) return e;

@@ -21,8 +21,8 @@ enum : int {
 };
 
 constexpr int kNumSMs = 152;          // GB300
-constexpr int kAttnKeysPerTile = 64;  // K/V tile of the tensor-core attention
-constexpr int kAttnCTAsPerSM = 2;     // tensor-core attention CTAs resident per SM
+constexpr int kAttnKeysPerTile = 128; // K/V tile of the tensor-core attention
+constexpr int kAttnCTAsPerSM = 1;     // tensor-core attention CTAs resident per SM
 constexpr int kSimtRowsPerTile = 16;  // query positions per CTA of the SIMT attention
 constexpr int kSimtKeysPerTile = 64;
 
@@ -233,7 +233,7 @@ void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_ti
 void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split);
 // Scratch bytes of the split partials (0 = unsplit); never above
 // kAttnMaxSplitCTAs CTAs' worth.
-constexpr int kAttnMaxSplitCTAs = 8 * kNumSMs;
+constexpr int kAttnMaxSplitCTAs = 4 * kNumSMs;
 size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_heads);
 
 // ---------------------------------------------------------------- dependent launch

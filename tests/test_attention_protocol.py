@@ -16,7 +16,8 @@ completing in issue order per issuing thread:
              writes P_j over S_j; at the end waits for the last PV.
 
 KS (ring stages) and SB (score buffers) are the kernel's kStages and kSBufs:
-2 and 2 (64-key tiles, two CTAs per SM); the deeper 3 and 3 is checked too.
+3 and 3; the shallower 2 and 2 (a 64-key, two-CTAs-per-SM form, measured
+slower) is checked too.
 An mbarrier poll succeeds when the barrier's completed-phase count has the
 other parity than the one asked for, so a waiter that falls two phases
 behind, or polls a phase two ahead, would be fooled: the model asserts that
@@ -35,7 +36,7 @@ class Alias(AssertionError):
     pass
 
 
-def simulate(n, seed, wait_s_on_last_step=True, KS=2, SB=2):
+def simulate(n, seed, wait_s_on_last_step=True, KS=3, SB=3):
     """KS: K and V ring stages; SB: score buffers (the kernel's kStages and
     kSBufs)."""
     R = random.Random(seed)
@@ -141,8 +142,8 @@ def simulate(n, seed, wait_s_on_last_step=True, KS=2, SB=2):
 @pytest.mark.parametrize("n", list(range(0, 12)))
 @pytest.mark.parametrize("KS,SB", [(2, 2), (3, 3)])
 def test_protocol_has_no_alias_deadlock_or_overwrite(n, KS, SB):
-    """(2, 2) is the kernel's depth (64-key tiles, two CTAs per SM); (3, 3) the
-    deeper form the same protocol also supports."""
+    """(3, 3) is the kernel's depth; (2, 2) the shallower form the same
+    protocol also supports."""
     for seed in range(400):
         simulate(n, seed, KS=KS, SB=SB)
 
