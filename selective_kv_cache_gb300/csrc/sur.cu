@@ -16,11 +16,14 @@
 //                       unit that does not fit, and compaction of the selected
 //                       tokens into ascending global positions
 // The scoring contraction is fp32 as the pages state.  For bf16 embeddings it
-// runs on the tensor cores (sur_qsplit_kernel, sur_gather_kernel, the tcgen05
-// projection kernel, sur_finish_kernel): the normalised query splits exactly
-// into three bf16 terms and bf16 products are exact in fp32, so the dot
-// products are fp32 up to summation order.  fp32 embeddings take the FFMA
-// kernel.  Everything after it is a few passes over S floats.
+// runs on the tensor cores (sur_prep_kernel: the query split and the suffix
+// rows' gather in one launch; the tcgen05 projection kernel;
+// sur_finish_kernel): the normalised query splits exactly into three bf16
+// terms and bf16 products are exact in fp32, so the dot products are fp32 up
+// to summation order.  fp32 embeddings take the FFMA kernel.  Everything after
+// it is a few passes over S floats.  Kernels after the projection go out as
+// dependent launches: each starts while its predecessor drains and waits for
+// it before reading what it wrote.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -211,11 +214,9 @@ __global__ void __launch_bounds__(256) sur_score_kernel(const T* __restrict__ E,
 
 // one CTA per query token: q = E[q_j] / ||E[q_j]|| in fp32, written as the rows
 // j (hi), Q + j (mid), 2Q + j (lo) of qp
-__global__ void __launch_bounds__(256) sur_qsplit_kernel(const __nv_bfloat16* __restrict__ E, int vocab, int d,
-                                                         const int32_t* __restrict__ qids, int Q,
-                                                         __nv_bfloat16* __restrict__ qp, int32_t* err) {
+__device__ void sur_qsplit(int j, const __nv_bfloat16* __restrict__ E, int vocab, int d,
+                           const int32_t* __restrict__ qids, int Q, __nv_bfloat16* __restrict__ qp, int32_t* err) {
     __shared__ float red[256];
-    const int j = blockIdx.x;
     const int id = qids[j];
     const bool ok = id >= 0 && id < vocab;
     if (!ok && threadIdx.x == 0) atomicOr(err, DEV_ERR_INDEX);
@@ -247,11 +248,10 @@ __global__ void __launch_bounds__(256) sur_qsplit_kernel(const __nv_bfloat16* __
 
 // one warp per suffix token: its embedding row into eg (16-byte copies) and
 // its fp32 norm; rows S..S_pad-1 are zero
-__global__ void __launch_bounds__(256) sur_gather_kernel(const __nv_bfloat16* __restrict__ E, int vocab, int d,
-                                                         const int32_t* __restrict__ sids, int S, int S_pad,
-                                                         __nv_bfloat16* __restrict__ eg, float* __restrict__ enorm,
-                                                         int32_t* err) {
-    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+__device__ void sur_gather(int i, const __nv_bfloat16* __restrict__ E, int vocab, int d,
+                           const int32_t* __restrict__ sids, int S, int S_pad, __nv_bfloat16* __restrict__ eg,
+                           float* __restrict__ enorm, int32_t* err) {
+    const int lane = threadIdx.x & 31;
     if (i >= S_pad) return;
     uint4* dst = reinterpret_cast<uint4*>(eg + (size_t)i * d);
     const int nv = d / 8;
@@ -279,19 +279,38 @@ __global__ void __launch_bounds__(256) sur_gather_kernel(const __nv_bfloat16* __
     if (lane == 0 && i < S) enorm[i] = sqrtf(ss);
 }
 
-// scores from the GEMM partials: 32 suffix tokens per CTA, 8 threads per token
-// split the queries; consecutive threads take consecutive tokens (coalesced)
-__global__ void __launch_bounds__(256) sur_finish_kernel(const float* __restrict__ part, int splits, int S, int S_pad,
-                                                         int Q, const float* __restrict__ enorm,
-                                                         const int32_t* __restrict__ sids,
-                                                         const int32_t* __restrict__ qids, float* __restrict__ scores) {
-    __shared__ float red[8][32];
+// the query split (CTAs 0 .. Q-1, one per query token) and the suffix rows'
+// gather (the other CTAs, one warp per suffix token) in one launch
+__global__ void __launch_bounds__(256) sur_prep_kernel(const __nv_bfloat16* __restrict__ E, int vocab, int d,
+                                                       const int32_t* __restrict__ qids, int Q,
+                                                       __nv_bfloat16* __restrict__ qp,
+                                                       const int32_t* __restrict__ sids, int S, int S_pad,
+                                                       __nv_bfloat16* __restrict__ eg, float* __restrict__ enorm,
+                                                       int32_t* err) {
+    if ((int)blockIdx.x < Q) {
+        sur_qsplit(blockIdx.x, E, vocab, d, qids, Q, qp, err);
+    } else {
+        const int i = (int)(blockIdx.x - Q) * 8 + (threadIdx.x >> 5);
+        sur_gather(i, E, vocab, d, sids, S, S_pad, eg, enorm, err);
+    }
+}
+
+// scores from the GEMM partials: 32 suffix tokens per CTA, 32 threads per
+// token splitting the queries; consecutive threads take consecutive tokens
+// (coalesced), and every load of a thread is independent of the others
+__global__ void __launch_bounds__(1024) sur_finish_kernel(const float* __restrict__ part, int splits, int S, int S_pad,
+                                                          int Q, const float* __restrict__ enorm,
+                                                          const int32_t* __restrict__ sids,
+                                                          const int32_t* __restrict__ qids, float* __restrict__ scores) {
+    __shared__ float red[32][33];
+    pdl_trigger();
+    pdl_wait();
     const int fl = threadIdx.x & 31, jg = threadIdx.x >> 5;
     const int f = blockIdx.x * 32 + fl;
     const size_t split_stride = (size_t)3 * Q * S_pad;
     float best = -INFINITY;
     if (f < S) {
-        for (int j = jg; j < Q; j += 8) {
+        for (int j = jg; j < Q; j += 32) {
             float dot = 0.f;
             for (int s = 0; s < splits; ++s) {
                 const float* p = part + s * split_stride + f;
@@ -303,8 +322,8 @@ __global__ void __launch_bounds__(256) sur_finish_kernel(const float* __restrict
     red[jg][fl] = best;
     __syncthreads();
     if (jg == 0 && f < S) {
-#pragma unroll
-        for (int g = 1; g < 8; ++g) best = fmaxf(best, red[g][fl]);
+#pragma unroll 8
+        for (int g = 1; g < 32; ++g) best = fmaxf(best, red[g][fl]);
         const int id = sids[f];
         bool in_q = false;
         for (int j = 0; j < Q && !in_q; ++j) in_q = qids[j] == id;
@@ -317,6 +336,8 @@ __global__ void __launch_bounds__(256) sur_finish_kernel(const float* __restrict
 // mean of the four largest scores of each unit (all of them below four)
 __global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int n_units,
                                 float* __restrict__ unit_score, int32_t* err) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= n_units) return;
     const int b = bounds[warp], e = bounds[warp + 1];
@@ -362,6 +383,8 @@ __global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t*
 // rank of unit u: units with a higher score, or the same score and an earlier start
 __global__ void sur_rank_kernel(const float* __restrict__ unit_score, int n_units, int32_t* __restrict__ order) {
     __shared__ float sc[1024];
+    pdl_trigger();
+    pdl_wait();
     const int u = blockIdx.x * blockDim.x + threadIdx.x;
     const float mine = u < n_units ? unit_score[u] : 0.f;
     int rank = 0;
@@ -413,6 +436,8 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
                                                                   double* __restrict__ cum,
                                                                   int32_t* __restrict__ positions) {
     __shared__ int s_partial, s_w;
+    pdl_trigger();
+    pdl_wait();
     const int W = (S + 31) / 32;
     for (int w = threadIdx.x; w < W; w += blockDim.x) sel[w] = 0u;
     if (threadIdx.x == 0) {
@@ -547,6 +572,7 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
             redi[wid] = best_a;
         }
         __syncthreads();
+        __shared__ int s_ba;
         if (threadIdx.x == 0) {
             double bb = red[0];
             int ba = redi[0];
@@ -555,7 +581,14 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
                     bb = red[k];
                     ba = redi[k];
                 }
-            for (int i = b + ba; i < b + ba + w; ++i) sel[i >> 5] |= 1u << (i & 31);
+            s_ba = ba;
+        }
+        __syncthreads();
+        // the window's bits, set in parallel (the whole units' bits are in other words
+        // or other bits of these words, so the ORs commute)
+        for (int t = threadIdx.x; t < w; t += blockDim.x) {
+            const int i = b + s_ba + t;
+            atomicOr(&sel[i >> 5], 1u << (i & 31));
         }
     }
     __syncthreads();
@@ -629,6 +662,12 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, bool tc, SurWs* L, uint8_
 
 using namespace kvr;
 
+#define KVR_CHECK_LAUNCH_SUR(expr)                              \
+    do {                                                        \
+        cudaError_t e_ = (expr);                                \
+        if (e_ != cudaSuccess) return cuda_fail(e_, "sur launch"); \
+    } while (0)
+
 extern "C" {
 
 size_t kvr_sur_workspace_bytes(int32_t S, int32_t Q, int32_t d, int32_t n_units) {
@@ -672,18 +711,23 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
     float* scores = scores_out ? scores_out : L.scores;
     cudaError_t e = cudaMemsetAsync(L.err, 0, 16, s);
     if (e != cudaSuccess) return cuda_fail(e, "sur");
+    pdl_begin_call();   // the first kernel keeps plain stream order
     if (tc) {
-        pdl_begin_call();   // the projection kernel must not overlap the gather that feeds it
         const int S_pad = (S + 127) / 128 * 128;
-        sur_qsplit_kernel<<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, Q, L.qp, L.err);
-        sur_gather_kernel<<<(unsigned)(((size_t)S_pad * 32 + 255) / 256), 256, 0, s>>>(
-            (const __nv_bfloat16*)embed, vocab, d, suffix_ids, S, S_pad, L.eg, L.enorm, L.err);
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_prep_kernel, dim3((unsigned)(Q + (S_pad + 7) / 8)), dim3(256), 0, s,
+                                           (const __nv_bfloat16*)embed, vocab, d, query_ids, Q, L.qp, suffix_ids, S,
+                                           S_pad, L.eg, L.enorm, L.err));
+        // the projection fetches its first operand tiles before it waits for
+        // the previous kernel, and those tiles are the rows just gathered: it
+        // keeps plain stream order
+        pdl_begin_call();
         const GemmPlan gp = plan_gemm(KVR_BF16, S_pad, d, 3 * Q);
         std::string why;
         e = launch_gemm(KVR_BF16, gp, L.eg, L.qp, L.part, L.err, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("sur scoring " + why).c_str());
-        sur_finish_kernel<<<(S + 31) / 32, 256, 0, s>>>(L.part, gp.splits, S, S_pad, Q, L.enorm, suffix_ids,
-                                                        query_ids, scores);
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_finish_kernel, dim3((unsigned)((S + 31) / 32)), dim3(1024), 0, s,
+                                           (const float*)L.part, gp.splits, S, S_pad, Q, (const float*)L.enorm,
+                                           suffix_ids, query_ids, scores));
     } else if (dtype == KVR_BF16) {
         sur_qnorm_kernel<__nv_bfloat16><<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, L.qn,
                                                           L.err);
@@ -694,11 +738,16 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
         sur_score_kernel<float><<<(S + kTokTile - 1) / kTokTile, 256, 0, s>>>(
             (const float*)embed, vocab, d, suffix_ids, S, query_ids, Q, L.qn, scores, L.err);
     }
-    sur_unit_kernel<<<(n_units * 32 + 255) / 256, 256, 0, s>>>(scores, unit_bounds, n_units, L.unit_score, L.err);
-    sur_rank_kernel<<<(n_units + 1023) / 1024, 1024, 0, s>>>(L.unit_score, n_units, L.order);
+    // the FFMA scoring kernels above are plain launches, so the unit kernel's
+    // dependent launch waits for them like any other predecessor
+    KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_unit_kernel, dim3((unsigned)((n_units * 32 + 255) / 256)), dim3(256), 0,
+                                       s, (const float*)scores, unit_bounds, n_units, L.unit_score, L.err));
+    KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_rank_kernel, dim3((unsigned)((n_units + 1023) / 1024)), dim3(1024), 0, s,
+                                       (const float*)L.unit_score, n_units, L.order));
     if (B > 0)
-        sur_admit_kernel<<<1, kAdmitThreads, 0, s>>>(scores, unit_bounds, n_units, L.order, S, B, suffix_start,
-                                                     L.sel, L.cum, positions_out);
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_admit_kernel, dim3(1), dim3(kAdmitThreads), 0, s, (const float*)scores,
+                                           unit_bounds, n_units, (const int32_t*)L.order, S, B, suffix_start, L.sel,
+                                           L.cum, positions_out));
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sur launch");
     return KVR_OK;
