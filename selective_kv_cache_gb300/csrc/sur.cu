@@ -334,17 +334,14 @@ __global__ void __launch_bounds__(1024) sur_finish_kernel(const float* __restric
 }
 
 // mean of the four largest scores of each unit (all of them below four)
-__global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int n_units,
-                                float* __restrict__ unit_score, int32_t* err) {
-    pdl_trigger();
-    pdl_wait();
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= n_units) return;
-    const int b = bounds[warp], e = bounds[warp + 1];
+// one warp: the unit score of unit u (returned in every lane)
+__device__ float unit_score_warp(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int u,
+                                 int32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const int b = bounds[u], e = bounds[u + 1];
     if (b >= e) {
         if (lane == 0) atomicOr(err, DEV_ERR_INDEX);
-        if (lane == 0) unit_score[warp] = -INFINITY;
-        return;
+        return -INFINITY;
     }
     // each lane keeps its own top four, then four rounds of warp max take the unit's
     float t[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -377,7 +374,17 @@ __global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t*
         sum += m;
         if (lane == who) ++head;
     }
-    if (lane == 0) unit_score[warp] = sum / (float)n;
+    return sum / (float)n;
+}
+
+__global__ void sur_unit_kernel(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int n_units,
+                                float* __restrict__ unit_score, int32_t* err) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= n_units) return;
+    const float v = unit_score_warp(scores, bounds, warp, err);
+    if (lane == 0) unit_score[warp] = v;
 }
 
 // rank of unit u: units with a higher score, or the same score and an earlier start
@@ -429,16 +436,55 @@ __device__ int block_scan_incl(int v, int* total) {
     return r;
 }
 
+// The selection mask and the envelope's prefix sums live in shared memory when
+// they fit (kAdmitSelWords words, kAdmitCumLen doubles), else in the
+// workspace; generic pointers keep one code path.  Every phase is then one
+// block-wide step, with global round trips only for the unit order, the unit
+// bounds and the partial unit's scores.
+constexpr int kAdmitSelWords = 8192;
+constexpr int kAdmitCumLen = 4096;
+constexpr size_t kAdmitSmem = kAdmitSelWords * sizeof(uint32_t) + kAdmitCumLen * sizeof(double);
+// fused: n_units <= kAdmitThreads, so this block also computes the unit
+// scores (one warp per unit) and their order (one thread per unit) itself,
+// in shared memory, instead of reading `order` from the two kernels before it
 __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* __restrict__ scores,
                                                                   const int32_t* __restrict__ bounds, int n_units,
-                                                                  const int32_t* __restrict__ order, int S, int B,
-                                                                  int suffix_start, uint32_t* __restrict__ sel,
-                                                                  double* __restrict__ cum,
-                                                                  int32_t* __restrict__ positions) {
+                                                                  const int32_t* __restrict__ order_in, int S, int B,
+                                                                  int suffix_start, uint32_t* __restrict__ sel_ws,
+                                                                  double* __restrict__ cum_ws,
+                                                                  int32_t* __restrict__ positions, int fused,
+                                                                  int32_t* err) {
+    extern __shared__ __align__(16) uint8_t admit_smem[];
     __shared__ int s_partial, s_w;
+    __shared__ float s_us[kAdmitThreads];
+    __shared__ int s_order[kAdmitThreads];
     pdl_trigger();
     pdl_wait();
+    const int32_t* order = order_in;
+    if (fused) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int u = warp; u < n_units; u += kAdmitThreads / 32) {
+            const float v = unit_score_warp(scores, bounds, u, err);
+            if (lane == 0) s_us[u] = v;
+        }
+        __syncthreads();
+        // rank of unit u: units with a higher score, or the same score and an earlier start
+        const int u = threadIdx.x;
+        if (u < n_units) {
+            const float mine = s_us[u];
+            int rank = 0;
+            for (int k = 0; k < n_units; ++k) {
+                const float x = s_us[k];
+                rank += (x > mine || (x == mine && k < u)) ? 1 : 0;
+            }
+            s_order[rank] = u;
+        }
+        __syncthreads();
+        order = s_order;
+    }
     const int W = (S + 31) / 32;
+    uint32_t* sel = W <= kAdmitSelWords ? reinterpret_cast<uint32_t*>(admit_smem) : sel_ws;
+    double* cum_smem = reinterpret_cast<double*>(admit_smem + kAdmitSelWords * sizeof(uint32_t));
     for (int w = threadIdx.x; w < W; w += blockDim.x) sel[w] = 0u;
     if (threadIdx.x == 0) {
         s_partial = -1;
@@ -482,6 +528,7 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
         __shared__ double red[32];
         __shared__ int redi[32];
         const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w, len = e - b;
+        double* cum = len <= kAdmitCumLen ? cum_smem : cum_ws;
         const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
         // r_max of the unit
         double rm = -INFINITY;
@@ -738,16 +785,28 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
         sur_score_kernel<float><<<(S + kTokTile - 1) / kTokTile, 256, 0, s>>>(
             (const float*)embed, vocab, d, suffix_ids, S, query_ids, Q, L.qn, scores, L.err);
     }
-    // the FFMA scoring kernels above are plain launches, so the unit kernel's
-    // dependent launch waits for them like any other predecessor
-    KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_unit_kernel, dim3((unsigned)((n_units * 32 + 255) / 256)), dim3(256), 0,
-                                       s, (const float*)scores, unit_bounds, n_units, L.unit_score, L.err));
-    KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_rank_kernel, dim3((unsigned)((n_units + 1023) / 1024)), dim3(1024), 0, s,
-                                       (const float*)L.unit_score, n_units, L.order));
-    if (B > 0)
-        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_admit_kernel, dim3(1), dim3(kAdmitThreads), 0, s, (const float*)scores,
-                                           unit_bounds, n_units, (const int32_t*)L.order, S, B, suffix_start, L.sel,
-                                           L.cum, positions_out));
+    // the FFMA scoring kernels above are plain launches, so the next kernel's
+    // dependent launch waits for them like any other predecessor.  Up to
+    // kAdmitThreads units, the admission kernel scores and orders the units
+    // itself.
+    const bool fused = n_units <= kAdmitThreads;
+    if (!fused) {
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_unit_kernel, dim3((unsigned)((n_units * 32 + 255) / 256)), dim3(256),
+                                           0, s, (const float*)scores, unit_bounds, n_units, L.unit_score, L.err));
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_rank_kernel, dim3((unsigned)((n_units + 1023) / 1024)), dim3(1024), 0,
+                                           s, (const float*)L.unit_score, n_units, L.order));
+    }
+    if (B > 0 || fused) {   // fused, it also checks the units, whatever the budget
+        static bool admit_attr = false;
+        if (!admit_attr) {
+            KVR_CHECK_LAUNCH_SUR(
+                cudaFuncSetAttribute(sur_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAdmitSmem));
+            admit_attr = true;
+        }
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_admit_kernel, dim3(1), dim3(kAdmitThreads), kAdmitSmem, s,
+                                           (const float*)scores, unit_bounds, n_units, (const int32_t*)L.order, S, B,
+                                           suffix_start, L.sel, L.cum, positions_out, fused ? 1 : 0, L.err));
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sur launch");
     return KVR_OK;
