@@ -443,12 +443,14 @@ __device__ int block_scan_incl(int v, int* total) {
 // bounds and the partial unit's scores.
 constexpr int kAdmitSelWords = 8192;
 constexpr int kAdmitCumLen = 4096;
-constexpr size_t kAdmitSmem = kAdmitSelWords * sizeof(uint32_t) + kAdmitCumLen * sizeof(double);
+constexpr int kAdmitScores = 16384;   // token scores staged in shared memory (one coalesced pass)
+constexpr size_t kAdmitSmem = kAdmitSelWords * sizeof(uint32_t) + kAdmitCumLen * sizeof(double) +
+                              kAdmitScores * sizeof(float) + (kAdmitThreads + 1) * sizeof(int32_t);
 // fused: n_units <= kAdmitThreads, so this block also computes the unit
 // scores (one warp per unit) and their order (one thread per unit) itself,
 // in shared memory, instead of reading `order` from the two kernels before it
-__global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* __restrict__ scores,
-                                                                  const int32_t* __restrict__ bounds, int n_units,
+__global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* __restrict__ scores_g,
+                                                                  const int32_t* __restrict__ bounds_g, int n_units,
                                                                   const int32_t* __restrict__ order_in, int S, int B,
                                                                   int suffix_start, uint32_t* __restrict__ sel_ws,
                                                                   double* __restrict__ cum_ws,
@@ -460,6 +462,18 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
     __shared__ int s_order[kAdmitThreads];
     pdl_trigger();
     pdl_wait();
+    // the token scores and the unit bounds, staged in one coalesced pass when they fit
+    float* sc_smem = reinterpret_cast<float*>(admit_smem + kAdmitSelWords * sizeof(uint32_t) +
+                                              kAdmitCumLen * sizeof(double));
+    int32_t* bd_smem = reinterpret_cast<int32_t*>(sc_smem + kAdmitScores);
+    const bool sc_fit = S <= kAdmitScores, bd_fit = n_units + 1 <= kAdmitThreads + 1;
+    if (sc_fit)
+        for (int i = threadIdx.x; i < S; i += blockDim.x) sc_smem[i] = scores_g[i];
+    if (bd_fit)
+        for (int i = threadIdx.x; i <= n_units; i += blockDim.x) bd_smem[i] = bounds_g[i];
+    __syncthreads();
+    const float* scores = sc_fit ? sc_smem : scores_g;
+    const int32_t* bounds = bd_fit ? bd_smem : bounds_g;
     const int32_t* order = order_in;
     if (fused) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -530,71 +544,39 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
         const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w, len = e - b;
         double* cum = len <= kAdmitCumLen ? cum_smem : cum_ws;
         const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-        // r_max of the unit
-        double rm = -INFINITY;
-        for (int t = threadIdx.x; t < len; t += blockDim.x) rm = fmax(rm, (double)scores[b + t]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) rm = fmax(rm, __shfl_xor_sync(0xffffffffu, rm, o));
-        if (lane == 0) red[wid] = rm;
-        __syncthreads();
+        // One warp walks the unit in chunks of 32 (a unit is a few dozen to a
+        // few hundred tokens): r_max, then the prefix max of rho_s + s/16 and
+        // the prefix sum of u, with carries between chunks.  The other warps
+        // would only add double-precision scans over empty lanes.
         if (wid == 0) {
-            double v = lane < nw ? red[lane] : -INFINITY;
+            double rmax = -INFINITY;
+            for (int t = lane; t < len; t += 32) rmax = fmax(rmax, (double)scores[b + t]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[0] = v;
-        }
-        __syncthreads();
-        const double rmax = red[0];
-        __syncthreads();
-        // prefix max of rho_s + s/16 and prefix sum of u, chunk by chunk
-        double pm_carry = -INFINITY, cs_carry = 0.0;
-        for (int base = 0; base < len; base += blockDim.x) {
-            const int t = base + threadIdx.x;
-            double a = t < len ? ((double)scores[b + t] - rmax) + (double)t / 16.0 : -INFINITY;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, a, o);
-                if (lane >= o) a = fmax(a, y);
-            }
-            if (lane == 31) red[wid] = a;
-            __syncthreads();
-            if (wid == 0) {
-                double v = lane < nw ? red[lane] : -INFINITY;
+            for (int o = 16; o > 0; o >>= 1) rmax = fmax(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+            double pm_carry = -INFINITY, cs_carry = 0.0;
+            for (int base = 0; base < len; base += 32) {
+                const int t = base + lane;
+                const double ts = (double)t * 0.0625;   // t / 16, exactly
+                double pm = t < len ? ((double)scores[b + t] - rmax) + ts : -INFINITY;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v = fmax(v, y);
+                    const double y = __shfl_up_sync(0xffffffffu, pm, o);
+                    if (lane >= o) pm = fmax(pm, y);
                 }
-                red[lane] = v;
-            }
-            __syncthreads();
-            const double pm = fmax(pm_carry, fmax(a, wid > 0 ? red[wid - 1] : -INFINITY));
-            const double chunk_max = red[nw - 1];
-            __syncthreads();
-            double u = t < len ? exp(pm - (double)t / 16.0) : 0.0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, u, o);
-                if (lane >= o) u += y;
-            }
-            if (lane == 31) red[wid] = u;
-            __syncthreads();
-            if (wid == 0) {
-                double v = lane < nw ? red[lane] : 0.0;
+                pm = fmax(pm_carry, pm);
+                pm_carry = __shfl_sync(0xffffffffu, pm, 31);
+                double c = t < len ? exp(pm - ts) : 0.0;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += y;
+                    const double y = __shfl_up_sync(0xffffffffu, c, o);
+                    if (lane >= o) c += y;
                 }
-                red[lane] = v;
+                c += cs_carry;
+                if (t < len) cum[t] = c;
+                cs_carry = __shfl_sync(0xffffffffu, c, 31);
             }
-            __syncthreads();
-            const double c = cs_carry + u + (wid > 0 ? red[wid - 1] : 0.0);
-            if (t < len) cum[t] = c;
-            cs_carry += red[nw - 1];
-            pm_carry = fmax(pm_carry, chunk_max);
-            __syncthreads();
         }
+        __syncthreads();
         // best window start
         double best = -INFINITY;
         int best_a = 0;
