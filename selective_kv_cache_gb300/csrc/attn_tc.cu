@@ -55,7 +55,7 @@ constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 // split merge: each softmax warp loads the other splits' rows of its 32 rows
 // as 128-byte-swizzled 32 x 32-float boxes into its share of the (then idle)
-// K and V rings, kMergeRound splits per load round
+// K and V rings, kMergeRound splits per load round and column pass
 constexpr uint32_t kMergeWarpBytes = 2 * kStages * kTile / 4;     // 48 KB per softmax warp
 constexpr int kMergeRound = (int)(kMergeWarpBytes / 16384u);      // 3 partial quarters of 16 KB
 constexpr int kSBufs = 3;                       // score buffers: the QK product runs two tiles ahead
@@ -535,26 +535,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t region = sbase + kOffK + (uint32_t)q4 * kMergeWarpBytes;
                 const uint32_t acc_cols = tmem + lane_base;   // the first score buffer's 128 columns
                 uint32_t phase = 0;
-                const int n_other = n_live - 1;
-                for (int sp = 0; sp < n_live && ok; ++sp) {
-                    float ms, ls;
-                    ml_of(sp, &ms, &ls);
-                    const float w = ms == -INFINITY ? 0.f : ex2(ms - M);
-                    const bool own = sp == split;
-                    // the other splits land kMergeRound at a time, in split order
-                    const int k = sp - (sp > split ? 1 : 0);   // rank among the other splits
-                    if (!own && k % kMergeRound == 0) {
-                        __syncwarp();   // the previous round's rows are all read
-                        const int n_in = min(kMergeRound, n_other - k);
+                // rounds: runs of consecutive splits holding up to kMergeRound
+                // others (and this CTA's own split where it falls in order);
+                // one load round trip and one pass over the columns per round
+                int sp0 = 0;
+                bool first = true;
+                while (sp0 < n_live && ok) {
+                    int ids[kMergeRound + 1], slots[kMergeRound + 1];
+                    int n_ids = 0, n_oth = 0, e = sp0;
+                    while (e < n_live && n_ids < kMergeRound + 1 && (e == split || n_oth < kMergeRound)) {
+                        ids[n_ids] = e;
+                        slots[n_ids] = e == split ? -1 : n_oth++;
+                        ++n_ids;
+                        ++e;
+                    }
+                    if (n_oth > 0) {
                         if (lane == 0) {
                             fence_proxy_async_global();
-                            mbar_arrive_expect_tx(&merge_full[q4], (uint32_t)n_in * 16384u);
-                            for (int i = 0; i < n_in; ++i) {
-                                const int other = k + i;
-                                const int s_id = other + (other >= split ? 1 : 0);
-                                const int slot = (s_id * a.n_tiles + tile) * a.n_kv_heads + h;
+                            mbar_arrive_expect_tx(&merge_full[q4], (uint32_t)n_oth * 16384u);
+                            for (int i = 0; i < n_ids; ++i) {
+                                if (slots[i] < 0) continue;
+                                const int slot = (ids[i] * a.n_tiles + tile) * a.n_kv_heads + h;
                                 for (int cb = 0; cb < 4; ++cb)
-                                    tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)i * 16384u +
+                                    tma_load_2d(smem + kOffK + (uint32_t)q4 * kMergeWarpBytes + (uint32_t)slots[i] * 16384u +
                                                     (uint32_t)cb * 4096u,
                                                 &tmP, &merge_full[q4], cb * 32, slot * 128 + 32 * q4);
                             }
@@ -565,30 +568,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         phase ^= 1u;
                     }
-                    const uint32_t base = region + (uint32_t)(own ? 0 : k % kMergeRound) * 16384u + (uint32_t)lane * 128u;
-                    for (int c = 0; c < 8; ++c) {   // 16 output columns at a time
-                        float acc[16], v[16];
-                        if (sp > 0) tmem_ld16(acc_cols + (uint32_t)c * 16u, acc);
-                        if (own) {
-                            tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, v);
-                        } else {
+                    float wv[kMergeRound + 1];
 #pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const int q16 = 4 * c + t;   // 16-byte chunk of the row
-                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                             : "=f"(v[4 * t]), "=f"(v[4 * t + 1]), "=f"(v[4 * t + 2]),
-                                               "=f"(v[4 * t + 3])
-                                             : "r"(base + (uint32_t)(q16 >> 3) * 4096u +
-                                                   ((uint32_t)((q16 & 7) ^ (lane & 7)) << 4)));
-                            }
+                    for (int i = 0; i < kMergeRound + 1; ++i) {
+                        wv[i] = 0.f;
+                        if (i < n_ids) {
+                            float ms, ls;
+                            ml_of(ids[i], &ms, &ls);
+                            wv[i] = ms == -INFINITY ? 0.f : ex2(ms - M);
                         }
+                    }
+                    for (int c = 0; c < 8; ++c) {   // 16 output columns at a time
+                        float acc[16];
+                        if (!first) tmem_ld16(acc_cols + (uint32_t)c * 16u, acc);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float term = w == 0.f ? 0.f : __fmul_rn(w, v[e]);
-                            acc[e] = sp > 0 ? __fadd_rn(acc[e], term) : term;
+                        for (int i = 0; i < kMergeRound + 1; ++i) {
+                            if (i >= n_ids) break;
+                            float v[16];
+                            if (slots[i] < 0) {
+                                tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, v);
+                            } else {
+                                const uint32_t base = region + (uint32_t)slots[i] * 16384u + (uint32_t)lane * 128u;
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    const int q16 = 4 * c + t;   // 16-byte chunk of the row
+                                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                                 : "=f"(v[4 * t]), "=f"(v[4 * t + 1]), "=f"(v[4 * t + 2]),
+                                                   "=f"(v[4 * t + 3])
+                                                 : "r"(base + (uint32_t)(q16 >> 3) * 4096u +
+                                                       ((uint32_t)((q16 & 7) ^ (lane & 7)) << 4)));
+                                }
+                            }
+                            const bool init = first && i == 0;   // split 0 starts the sum
+#pragma unroll
+                            for (int x = 0; x < 16; ++x) {
+                                const float term = wv[i] == 0.f ? 0.f : __fmul_rn(wv[i], v[x]);
+                                acc[x] = init ? term : __fadd_rn(acc[x], term);
+                            }
                         }
                         tmem_st16(acc_cols + (uint32_t)c * 16u, acc);
                     }
+                    first = false;
+                    sp0 = e;
+                    __syncwarp();   // the next round's loads reuse this warp's region
                 }
                 if (ok) {
                     const float inv = 1.0f / L;
