@@ -23,9 +23,11 @@ size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_hea
 // fastest, then the query tiles from the last, whose ranges are the longest,
 // then the split), each of the kAttnCTAsPerSM slots of an SM taking the next
 // CTA when its last one ends; a CTA costs ~6 tile-times of set-up plus one per
-// K/V tile of its chunk (an empty chunk almost nothing), one more when it
-// stores its split rows, and the first chunk's CTA stands for the one that
-// merges: ~1.5 tile-times per round of three other splits it loads and adds.
+// K/V tile of its chunk (an empty chunk almost nothing), three more when its
+// query tile is split (its rows' store, the ticket, the wait), and the first
+// chunk's CTA stands for the one that merges: ~1.7 tile-times per other
+// split.  (Fitted to kvr_attend over chunk sizes at the Llama-3-8B, seam and
+// matched-work shapes on GB300; a 128-key tile-time is ~0.7 us.)
 // tile_kv[t] = K/V tiles of query tile t.
 void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
     *chunk = 1 << 30;
@@ -43,9 +45,9 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
                     const int v = tile_kv[t];
                     const int n = std::max(0, std::min(C, v - z * C));
                     const int live = (v + C - 1) / C;
-                    const double merge = (z == 0 && live > 1) ? 1.5 * ((live - 1 + 2) / 3) : 0.0;
+                    const double merge = (z == 0 && live > 1) ? 1.7 * (live - 1) : 0.0;
                     std::pop_heap(sm_free.begin(), sm_free.end(), later);
-                    sm_free.back() += n > 0 ? n + 6.0 + (live > 1 ? 1.0 : 0.0) + merge : 0.3;
+                    sm_free.back() += n > 0 ? n + 6.0 + (live > 1 ? 3.0 : 0.0) + merge : 0.3;
                     std::push_heap(sm_free.begin(), sm_free.end(), later);
                 }
         return *std::max_element(sm_free.begin(), sm_free.end());
