@@ -104,6 +104,7 @@ void set_attention_scratch(AttnLaunch* a, float* region, size_t bytes, const kvr
     a->sync = c->d_attn_sync;
     a->chunk = c->sel.attn_chunk;
     a->n_split = c->sel.attn_split;
+    a->merge = c->sel.attn_merge;
     if (need == 0 || !region || bytes < need) {
         a->n_split = 1;
         return;
@@ -334,6 +335,7 @@ kvr_status run_layer(kvr_cache* c, int layer, const kvr_layer_weights* w, void* 
         a.beta = c->beta;
         a.err = c->d_err;
         set_attention_scratch(&a, part, L.part_size, c);
+        p.launches = attention_launches(dt, a);
         cudaError_t e = launch_attention(dt, a, s, &why);
         if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     }
@@ -612,7 +614,7 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
     sel.n_rows = rows;
     sel.n_intervals = ivs;
     sel.n_tiles = tiles;
-    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split);
+    attention_chunking(c->m.dtype, tile_kv, c->m.n_kv_heads, &sel.attn_chunk, &sel.attn_split, &sel.attn_merge);
 
     // the staging buffer may still feed the previous upload
     cudaError_t e = cudaEventSynchronize(c->stage_ev);
@@ -1184,6 +1186,7 @@ kvr_status kvr_attend(kvr_cache* c, int32_t layer, const void* q, void* out, voi
                           ws_bytes, c);
     std::string why;
     Prof p(c, KVR_K_ATTN, s);
+    p.launches = attention_launches(c->m.dtype, a);
     cudaError_t e = launch_attention(c->m.dtype, a, s, &why);
     if (e != cudaSuccess) return cuda_fail(e, ("attention " + why).c_str());
     return KVR_OK;

@@ -2,6 +2,8 @@
 // its query-tile geometry (the plan is built over these tiles): the
 // tensor-core kernel for bf16 models, the CUDA-core kernel for fp32 models.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <functional>
 
 #include "kvr_internal.h"
@@ -18,26 +20,40 @@ size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_hea
     return dtype == KVR_BF16 ? attn_tc_scratch_bytes(n_split, n_tiles, n_kv_heads) : 0;
 }
 
-// Pick the chunk size C that minimises the modelled time.  The model plays
-// out the hardware's dispatch: CTAs go to the SMs in launch order (K/V head
-// fastest, then the query tiles from the last, whose ranges are the longest,
-// then the split), each of the kAttnCTAsPerSM slots of an SM taking the next
-// CTA when its last one ends; a CTA costs ~6 tile-times of set-up plus one per
-// K/V tile of its chunk (an empty chunk almost nothing), three more when its
-// query tile is split (its rows' store, the ticket, the wait), and the first
-// chunk's CTA stands for the one that merges: ~1.7 tile-times per other
-// split.  (Fitted to kvr_attend over chunk sizes at the Llama-3-8B, seam and
-// matched-work shapes on GB300; a 128-key tile-time is ~0.7 us.)
+// Pick the chunk size C and the merge that minimise the modelled time.  The
+// model plays out the hardware's dispatch: CTAs go to the SMs in launch order
+// (K/V head fastest, then the query tiles from the last, whose ranges are the
+// longest, then the split), each of the kAttnCTAsPerSM slots of an SM taking
+// the next CTA when its last one ends; a CTA costs ~6 tile-times of set-up
+// plus one per K/V tile of its chunk (an empty chunk almost nothing), and a
+// CTA of a split query tile one more for storing its rows.
+//   merge by the last CTA: such a CTA costs two more (the ticket, the wait),
+//     and the first chunk's CTA stands for the one that merges: ~2.5
+//     tile-times per other split;
+//   merge kernel: the kernel that follows adds ~4 tile-times plus 0.5 per
+//     split to the makespan.
+// (Fitted to kvr_attend over every chunk size and both merges at the
+// Llama-3-8B, seam and matched-work shapes on GB300, for the least loss
+// against the fastest measured choice; a 128-key tile-time is ~0.7 us.)  Two
+// environment variables narrow the choice, for tests and tuning:
+// KVR_ATTN_MERGE=cta|kernel allows one merge only (at the same chunk both
+// give the same output bits); KVR_ATTN_CHUNK=C fixes the chunk at C K/V tiles
+// when the split that makes stays within kAttnMaxSplitCTAs CTAs.
 // tile_kv[t] = K/V tiles of query tile t.
-void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split) {
+void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split,
+                        int* merge) {
     *chunk = 1 << 30;
     *n_split = 1;
+    *merge = kAttnMergeLastCTA;
     if (dtype != KVR_BF16 || tile_kv.empty()) return;
+    const char* env = std::getenv("KVR_ATTN_MERGE");
+    const bool allow_cta = !(env && std::strcmp(env, "kernel") == 0);
+    const bool allow_kernel = !(env && std::strcmp(env, "cta") == 0);
     int max_kv = 1;
     for (int v : tile_kv) max_kv = std::max(max_kv, v);
     std::vector<double> sm_free;
     std::greater<double> later;
-    auto makespan = [&](int C, int splits) {
+    auto makespan = [&](int C, int splits, int how) {
         sm_free.assign(kNumSMs * kAttnCTAsPerSM, 0.0);
         for (int z = 0; z < splits; ++z)
             for (int t = (int)tile_kv.size() - 1; t >= 0; --t)
@@ -45,22 +61,37 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
                     const int v = tile_kv[t];
                     const int n = std::max(0, std::min(C, v - z * C));
                     const int live = (v + C - 1) / C;
-                    const double merge = (z == 0 && live > 1) ? 1.7 * (live - 1) : 0.0;
+                    double cost = n > 0 ? n + 6.0 : 0.3;
+                    if (n > 0 && live > 1) cost += 1.0;
+                    if (n > 0 && live > 1 && how == kAttnMergeLastCTA) cost += 2.0 + (z == 0 ? 2.5 * (live - 1) : 0.0);
                     std::pop_heap(sm_free.begin(), sm_free.end(), later);
-                    sm_free.back() += n > 0 ? n + 6.0 + (live > 1 ? 3.0 : 0.0) + merge : 0.3;
+                    sm_free.back() += cost;
                     std::push_heap(sm_free.begin(), sm_free.end(), later);
                 }
-        return *std::max_element(sm_free.begin(), sm_free.end());
+        const double t = *std::max_element(sm_free.begin(), sm_free.end());
+        return how == kAttnMergeKernel && splits > 1 ? t + 4.0 + 0.5 * splits : t;
     };
+    const char* env_c = std::getenv("KVR_ATTN_CHUNK");
+    const int fixed = env_c ? std::atoi(env_c) : 0;
+    auto fits = [&](int C) {
+        const long long splits = (max_kv + C - 1) / C;
+        return splits == 1 || splits * (long long)tile_kv.size() * n_kv_heads <= kAttnMaxSplitCTAs;
+    };
+    const bool pinned = fixed >= 1 && fits(fixed);
     double best = 1e30;
-    for (int C = max_kv; C >= 2; --C) {
+    for (int C = pinned ? std::min(fixed, max_kv) : max_kv; C >= (pinned ? std::min(fixed, max_kv) : 2); --C) {
         const int splits = (max_kv + C - 1) / C;
-        if (splits > 1 && (long long)splits * (long long)tile_kv.size() * n_kv_heads > kAttnMaxSplitCTAs) break;
-        const double t = makespan(C, splits);
-        if (t < best * 0.98) {
-            best = t;
-            *chunk = C;
-            *n_split = splits;
+        if (!fits(C)) break;
+        for (int how : {kAttnMergeLastCTA, kAttnMergeKernel}) {
+            if ((how == kAttnMergeLastCTA && !allow_cta) || (how == kAttnMergeKernel && !allow_kernel)) continue;
+            if (splits == 1 && how == kAttnMergeKernel && allow_cta) continue;   // nothing to merge
+            const double t = makespan(C, splits, how);
+            if (t < best * 0.98) {
+                best = t;
+                *chunk = C;
+                *n_split = splits;
+                *merge = how;
+            }
         }
     }
     if (*n_split == 1) *chunk = 1 << 30;
@@ -74,6 +105,11 @@ void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_ti
         *rows_per_tile = attn_simt_rows_per_tile(n_q_heads, n_kv_heads);
         *keys_per_tile = kSimtKeysPerTile;
     }
+}
+
+int attention_launches(int dtype, const AttnLaunch& a) {
+    const bool merged = dtype == KVR_BF16 && a.n_tiles > 0 && a.part_o && a.n_split > 1 && a.merge == kAttnMergeKernel;
+    return merged ? 2 : 1;
 }
 
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why) {

@@ -24,12 +24,17 @@
 //               2^8, so P stays <= 256), P as bf16 pairs over the tile's
 //               scores in TMEM, the A operand of the PV product.
 // A query tile's K/V range may be split into chunks of C tiles over several
-// CTAs.  At the end of its chunk each of them takes a ticket; all but the
-// last store their unnormalised O rows and (running max, sum) in fp32 to the
-// workspace and count themselves done; the last one waits for that count
-// (its peers are past their main loops, so the wait ends), loads their rows
-// by TMA, merges them with its own and writes the bf16 output: no second
-// kernel, and the last CTA never stores its own partial.
+// CTAs, whose unnormalised O rows and (running max, sum) are merged in one of
+// two ways, chosen per selection:
+//   by the last CTA: at the end of its chunk each CTA takes a ticket; all but
+//     the last store their rows in fp32 to the workspace and count themselves
+//     done; the last one waits for that count (its peers are past their main
+//     loops, so the wait ends), loads their rows by TMA, merges them with its
+//     own and writes the bf16 output;
+//   by a merge kernel: every CTA stores its rows and ends; a second launch,
+//     one warp per row, merges them.
+// Both sum in split order with the same roundings: the output bits do not
+// depend on the merge or on which CTA came last.
 // Tiles below the plan's n_full are wholly visible to every row and skip the
 // causal test.  Every wait is bounded; on a timeout the CTA records the error,
 // drains its copies and MMAs, frees TMEM and returns.
@@ -44,7 +49,7 @@
 namespace kvr {
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;                   // 11 warps
 constexpr uint32_t kHalf = 16384;               // 128 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;           // 128 x 128 bf16
 constexpr int kStages = 3;                      // K and V ring depth; K runs one tile ahead of V
@@ -52,7 +57,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kOffLsum = kOffBar + 256;      // [128] the second softmax half's row sums
+constexpr uint32_t kSmemBytes = kOffLsum + 512 + 1024;
 // split merge: each softmax warp loads the other splits' rows of its 32 rows
 // as 128-byte-swizzled 32 x 32-float boxes into its share of the (then idle)
 // K and V rings, kMergeRound splits per load round and column pass
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&kv_full[i], 1);
         for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 4);
+        for (int i = 0; i < 4; ++i) mbar_init(&p_full[i], 8);   // both softmax halves of every quarter
         for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
         mbar_init(mma_done, 2);
         mbar_init(q_full, 1);
@@ -157,10 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     pdl_wait();   // Q rows and the cache rows written by the previous kernel
-    // rows of this thread (softmax warps): m = 32 * (warp % 4) + lane
+    // rows of this thread (softmax warps 2-5 and 7-10): m = 32 * (warp % 4) +
+    // lane; warps 2-5 take keys 0-63 of each tile, warps 7-10 keys 64-127
     const int m = 32 * (warp & 3) + lane;
     const int p = m / G, gi = m % G;
-    const bool row_valid = warp >= 2 && warp < 6 && m < P * G && p < nrows;
+    const int half = warp >= 7 ? 1 : 0;
+    const bool row_valid = warp >= 2 && warp != 6 && m < P * G && p < nrows;
     int g = umin;
     if (row_valid) g = a.U[row0 + p];
     // K/V producer, steps t = 0 .. n_total: K_t and V_{t-1} on one barrier,
@@ -264,12 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    // O += P V_j: P over the scores of tile j
+                    // O += P V_j: P over the scores of tile j, keys 0-63 in
+                    // columns 0-31 of the buffer, keys 64-127 in columns 64-95
                     const uint32_t pt = tmem + (uint32_t)(j % kSBufs) * 128u;
                     const uint32_t va = sbase + kOffV + (uint32_t)(j % kStages) * kTile;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)kk * 8u,
+                        mma_bf16_ta(tmem + kTmemO, pt + (uint32_t)(kk & 3) * 8u + (uint32_t)(kk >> 2) * 64u,
                                     sdesc_sw128(va + (uint32_t)kk * 2048u, kHalf, 1024), idesc_o, (j > 0 || kk > 0));
                     }
                     mma_commit(&o_done[j & 3]);
@@ -306,34 +315,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         if (biased && n_total > 0) load_words(jb * 128, lw, sw);
+        // The quarter's two halves meet at their pair barrier once per tile
+        // (twice when their maxima are swapped) and once after the loop.  A
+        // half that gives up on a wait still passes the barriers of the tiles
+        // left, asking for no swap, so its partner never blocks there.
+        const uint32_t pair_bar = 2u + (uint32_t)(warp & 3);
+        auto drain = [&](int from) {
+            for (int r = from; r < n_total; ++r)
+                if (named_bar_red_or(pair_bar, 64, false)) named_bar_sync(pair_bar, 64);
+        };
         for (int j = 0; j < n_total; ++j) {
             const int sb = j % kSBufs;
             if (__any_sync(0xffffffffu, !s_ready) && !warp_wait(&s_full[sb], (uint32_t)(j / kSBufs) & 1u)) {
                 ok = false;
+                drain(j);
                 break;
             }
             tc_fence_after();
-            float s[128];
-            tmem_ld32x4(tmem + lane_base + (uint32_t)sb * 128u, s);
+            // this half's 64 keys (columns own .. own + 63 of the buffer)
+            const uint32_t own = tmem + lane_base + (uint32_t)sb * 128u + 64u * (uint32_t)half;
+            float s[64];
+            tmem_ld32x2(own, s);
 
-            const int key0 = (jb + j) * 128;
+            const int tile_key0 = (jb + j) * 128, key0 = tile_key0 + 64 * half;
             const bool masked = jb + j >= n_full;
             if (biased) {
                 // the mask words are the same for every row of the tile, so the
                 // branches are warp-uniform: words with no bit set cost nothing,
                 // all-local words one add per key
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    if ((lw[t] | sw[t]) == 0u) continue;
-                    if (sw[t] == 0u && lw[t] == 0xffffffffu) {
+                for (int t = 0; t < 2; ++t) {
+                    const uint32_t lt = half ? lw[2 + t] : lw[t];
+                    const uint32_t st = half ? sw[2 + t] : sw[t];
+                    if ((lt | st) == 0u) continue;
+                    if (st == 0u && lt == 0xffffffffu) {
 #pragma unroll
                         for (int k = 0; k < 32; ++k) s[32 * t + k] += ar;
                         continue;
                     }
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        float b = ((lw[t] >> k) & 1u) ? ar : 0.f;
-                        b += ((sw[t] >> k) & 1u) ? br : 0.f;
+                        float b = ((lt >> k) & 1u) ? ar : 0.f;
+                        b += ((st >> k) & 1u) ? br : 0.f;
                         s[32 * t + k] += b;
                     }
                 }
@@ -341,20 +364,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (masked) {
                 const int lim = g - key0;   // keys k > lim are in the row's future
 #pragma unroll
-                for (int k = 0; k < 128; ++k)
+                for (int k = 0; k < 64; ++k)
                     if (k > lim) s[k] = -INFINITY;
             }
-            // row max over 8 independent chains of 3-input maxima
+            // the half's max over 8 independent chains of 3-input maxima
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 mx[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-                for (int t = 1; t < 8; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
+                for (int t = 1; t < 4; ++t) mx[i] = max3f(mx[i], s[i + 16 * t], s[i + 16 * t + 8]);
             }
-            const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+            const float mh = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            // The running max is raised only when a tile's max passes it by
+            // more than kRescale, so the halves need each other's maxima only
+            // when one of them sees that for some row: the pair barrier ORs
+            // the halves' findings.  Then they swap their maxima through the
+            // last column of their own score halves (read already, and not
+            // part of P), ordered by a second pass of the barrier, and both
+            // hold the same row max.
+            float mt = m_run;
+            if (named_bar_red_or(pair_bar, 64, mh * sl2 > m_run + kRescale)) {
+                tmem_st1(own + 63u, __float_as_uint(mh));
+                tc_fence_before();
+                named_bar_sync(pair_bar, 64);
+                tc_fence_after();
+                const float mo =
+                    __uint_as_float(tmem_ld1(tmem + lane_base + (uint32_t)sb * 128u + 64u * (uint32_t)(1 - half) + 63u));
+                mt = fmaxf(mh, mo) * sl2;
+            }
             s_ready = j + 1 < n_total && mbar_test(&s_full[(j + 1) % kSBufs], (uint32_t)((j + 1) / kSBufs) & 1u);
-            if (biased && j + 1 < n_total) load_words(key0 + 128, lw, sw);
+            if (biased && j + 1 < n_total) load_words(tile_key0 + 128, lw, sw);
             // O is rescaled only after the previous PV has finished.  P_j goes
             // over the scores just read; the buffer's earlier P (tile j - 3)
             // was read before S_j's product was issued, so P_j needs no wait.
@@ -363,19 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rescale) {
                 if (!warp_wait(&o_done[(j - 1) & 3], (uint32_t)((j - 1) >> 2) & 1u)) {
                     ok = false;
+                    drain(j + 1);
                     break;
                 }
                 tc_fence_after();
             }
-            if (rescale) {
+            if (rescale) {   // each half rescales its 64 of O's columns
                 const float f = raise ? ex2(m_run - mt) : 1.f;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     float o[16];
-                    tmem_ld16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
+                    const uint32_t col = kTmemO + 64u * (uint32_t)half + (uint32_t)c * 16u;
+                    tmem_ld16(tmem + lane_base + col, o);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) o[t] *= f;
-                    tmem_st16(tmem + lane_base + kTmemO + (uint32_t)c * 16u, o);
+                    tmem_st16(tmem + lane_base + col, o);
                 }
                 if (raise) l_run *= f;
             }
@@ -383,14 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // p = 2^(x - m): one packed FMA per two keys, then ex2; l sums the
             // fp32 probabilities (the PV product sees them rounded to bf16: a
             // relative difference of at most 2^-9 per term, unbiased)
-            // P goes to tensor memory as the PV product's A operand: column c of
-            // the row holds keys 2c, 2c+1 as packed bf16
+            // P goes to tensor memory as the PV product's A operand over this
+            // half's own scores: column own + c holds its keys 2c, 2c+1 as
+            // packed bf16
             const float2 sc = make_float2(sl2, sl2), nm = make_float2(-m_run, -m_run);
-            const uint32_t ptm = tmem + lane_base + (uint32_t)sb * 128u;
+            const uint32_t ptm = own;
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -410,9 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[j & 3]);
         }
-        if (ok && !warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u)) ok = false;
+        // the second half hands its row sums to the first, which finishes the
+        // rows (l = first half's sum + second half's)
+        float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+        if (half) lsum[m] = l_run;
+        named_bar_sync(pair_bar, 64);
+        if (!half) l_run += lsum[m];
+        if (!half && ok && !warp_wait(&o_done[(n_total - 1) & 3], (uint32_t)((n_total - 1) >> 2) & 1u)) ok = false;
         __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(row0 + p) * a.n_q_heads + h * G + gi) * 128;
-        if (n_live == 1) {
+        if (half) {
+            // done: O and the merge are the first half's
+        } else if (n_live == 1) {
             if (ok) {
                 tc_fence_after();
                 const float inv = 1.0f / l_run;
@@ -441,9 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int* count = a.sync + pair;                                   // tickets taken
             int* done = a.sync + (size_t)a.n_tiles * a.n_kv_heads + pair;  // partials stored
             const int q4 = warp & 3;
-            if (warp == 2 && lane == 0) *ticket = atomicAdd(count, 1);
-            named_bar_sync(1, 128);
-            const bool last = *ticket == n_live - 1;   // CTA-uniform
+            const bool merge_here = a.merge == kAttnMergeLastCTA;   // launch-uniform
+            if (merge_here) {
+                if (warp == 2 && lane == 0) *ticket = atomicAdd(count, 1);
+                named_bar_sync(1, 128);
+            }
+            const bool last = merge_here && *ticket == n_live - 1;   // CTA-uniform
             if (!last) {
                 // unnormalised fp32 rows plus (running max in base 2, sum): the
                 // warp's 32 rows leave as four TMA stores of 32 x 32 floats
@@ -473,14 +527,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cb = 0; cb < 4; ++cb)
                         tma_store_2d(&tmP, stg + cb * 4096, cb * 32, (int)(slot * 128) + 32 * q4);
                     bulk_commit();
-                    bulk_wait_all();            // the rows are in global memory
-                    fence_proxy_async_global();
-                    __threadfence();
+                    if (merge_here) {
+                        bulk_wait_all();            // the rows are in global memory
+                        fence_proxy_async_global();
+                        __threadfence();
+                    } else {
+                        bulk_wait_read_all();       // the staging may be released; the rows land before the grid ends
+                    }
                 }
-                named_bar_sync(1, 128);
-                if (warp == 2 && lane == 0) {   // after every warp's stores and fences: a release
-                    __threadfence();
-                    atomicAdd(done, 1);
+                if (merge_here) {
+                    named_bar_sync(1, 128);
+                    if (warp == 2 && lane == 0) {   // after every warp's stores and fences: a release
+                        __threadfence();
+                        atomicAdd(done, 1);
+                    }
                 }
             } else {
                 // every peer took its ticket after its main loop, so each is
@@ -651,6 +711,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// The merge kernel: one warp per MMA row of a split (query tile, K/V head),
+// four output columns per lane.  It does the last CTA's arithmetic in the
+// same order (M the largest split max, L and the rows summed in split order
+// with products and sums rounded separately, splits with no visible key of
+// the row left out), so either merge writes the same bits.  Lane k holds
+// split k's (max, sum); the rows of the first eight splits are loaded with
+// them, so up to eight splits cost one load round trip.
+__global__ void __launch_bounds__(256) attn_merge_kernel(AttnLaunch a) {
+    pdl_wait();   // every split's rows are stored
+    pdl_trigger();
+    const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp_id >= (long long)a.n_tiles * a.n_kv_heads * 128) return;
+    const int m = (int)(warp_id & 127);
+    const int h = (int)((warp_id >> 7) % a.n_kv_heads);
+    const int tile = (int)((warp_id >> 7) / a.n_kv_heads);
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int p = m / G, gi = m % G;
+    const int* plan = a.plan + 8 * tile;
+    const int n_live = min(a.n_split, (plan[5] + a.chunk - 1) / a.chunk);
+    if (n_live <= 1 || m >= (128 / G) * G || p >= plan[1]) return;   // written by the attention, or no row
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+    const float4* rows = reinterpret_cast<const float4*>(a.part_o);
+    auto row_of = [&](int sp) { return (((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h) * 128 + m; };
+    constexpr int kGroup = 8;
+    float4 v[kGroup];
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k)
+        v[k] = k < n_live ? rows[row_of(k) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float2 mine = lane < n_live ? ml[row_of(lane)] : make_float2(-INFINITY, 0.f);
+    float M = mine.x;
+    for (int s0 = 32; s0 < n_live; s0 += 32)
+        if (s0 + lane < n_live) M = fmaxf(M, ml[row_of(s0 + lane)].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // weight and sum term of split s0 + lane, L summed in split order
+    float L = 0.f, w_mine = 0.f;
+    for (int s0 = 0; s0 < n_live; s0 += 32) {
+        const float2 x = s0 == 0 ? mine : (s0 + lane < n_live ? ml[row_of(s0 + lane)] : make_float2(-INFINITY, 0.f));
+        const float w = x.x == -INFINITY ? 0.f : ex2(x.x - M);
+        const float term = x.x == -INFINITY ? 0.f : __fmul_rn(w, x.y);
+        if (s0 == 0) w_mine = w;
+        const int n = min(32, n_live - s0);
+        for (int k = 0; k < n; ++k) {
+            const float tk = __shfl_sync(0xffffffffu, term, k);
+            const float mk = __shfl_sync(0xffffffffu, x.x, k);
+            if (mk != -INFINITY) L = __fadd_rn(L, tk);
+        }
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n_live; s0 += kGroup) {
+        if (s0 > 0) {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k)
+                if (s0 + k < n_live) v[k] = rows[row_of(s0 + k) * 32 + lane];
+        }
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            const int sp = s0 + k;
+            if (sp >= n_live) break;
+            float w;
+            if (sp < 32) {
+                w = __shfl_sync(0xffffffffu, w_mine, sp);
+            } else {
+                const float ms = ml[row_of(sp)].x;
+                w = ms == -INFINITY ? 0.f : ex2(ms - M);
+            }
+            const float4 t = w == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : make_float4(__fmul_rn(w, v[k].x), __fmul_rn(w, v[k].y),
+                                                    __fmul_rn(w, v[k].z), __fmul_rn(w, v[k].w));
+            if (sp == 0) {
+                acc = t;   // split 0 starts the sum
+            } else {
+                acc.x = __fadd_rn(acc.x, t.x);
+                acc.y = __fadd_rn(acc.y, t.y);
+                acc.z = __fadd_rn(acc.z, t.z);
+                acc.w = __fadd_rn(acc.w, t.w);
+            }
+        }
+    }
+    const float inv = 1.0f / L;
+    __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan[0] + p) * a.n_q_heads + h * G + gi) * 128;
+    uint2 o;
+    o.x = pack_bf16(acc.x * inv, acc.y * inv);
+    o.y = pack_bf16(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(out)[lane] = o;
+}
+
 }  // namespace
 
 int attn_tc_rows_per_tile(int n_q_heads, int n_kv_heads) { return 128 / (n_q_heads / n_kv_heads); }
@@ -680,7 +828,8 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         if (why) *why = "tensor-core attention needs head_dim 128";
         return cudaErrorInvalidValue;
     }
-    const int n_split = (a.part_o && a.sync && a.n_split > 1) ? a.n_split : 1;
+    const int n_split =
+        (a.part_o && (a.sync || a.merge == kAttnMergeKernel) && a.n_split > 1) ? a.n_split : 1;
     CUtensorMap tk, tv;
     const uint64_t heads = (uint64_t)a.batch * a.n_layers * a.n_kv_heads;
     const uint64_t row_bytes = 128 * 2, head_bytes = (uint64_t)a.capacity * row_bytes;
@@ -710,6 +859,10 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         KVR_LAUNCH(attn_tc_kernel<true>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
     else
         KVR_LAUNCH(attn_tc_kernel<false>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
+    if (n_split > 1 && b.merge == kAttnMergeKernel) {
+        const long long threads = (long long)a.n_tiles * a.n_kv_heads * 128 * 32;
+        KVR_LAUNCH(attn_merge_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, b);
+    }
     return cudaSuccess;
 }
 

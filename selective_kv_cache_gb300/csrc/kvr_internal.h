@@ -23,6 +23,10 @@ enum : int {
 constexpr int kNumSMs = 152;          // GB300
 constexpr int kAttnKeysPerTile = 128; // K/V tile of the tensor-core attention
 constexpr int kAttnCTAsPerSM = 1;     // tensor-core attention CTAs resident per SM
+// Merge of a split query tile's partials: by the last of its CTAs inside the
+// attention launch, or by a second kernel over all split tiles.
+constexpr int kAttnMergeLastCTA = 0;
+constexpr int kAttnMergeKernel = 1;
 constexpr int kSimtRowsPerTile = 16;  // query positions per CTA of the SIMT attention
 constexpr int kSimtKeysPerTile = 64;
 
@@ -30,6 +34,7 @@ struct Selection {
     int32_t n_rows = 0, n_intervals = 0, n_tiles = 0;
     int32_t rows_per_tile = 0, keys_per_tile = 0;
     int32_t attn_chunk = 1 << 30, attn_split = 1;   // K/V split of the attention
+    int32_t attn_merge = kAttnMergeLastCTA;         // who merges the split partials
     std::vector<int32_t> counts, row_off, iv_count, iv_off, tile_count, tile_off;
     bool valid = false;
 };
@@ -224,13 +229,18 @@ struct AttnLaunch {
     int* sync;                 // [2][tiles][H_kv] merge counters, zero between launches
     int chunk;                 // K/V tiles per CTA when split
     int n_split;               // CTAs per (query tile, K/V head); 1 = unsplit
+    int merge;                 // kAttnMergeLastCTA or kAttnMergeKernel
 };
 cudaError_t launch_attention(int dtype, const AttnLaunch& a, cudaStream_t s, std::string* why);
+// Kernels launch_attention issues for a (2 when a merge kernel follows).
+int attention_launches(int dtype, const AttnLaunch& a);
 // Query tile geometry of the attention kernel for a model.
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile);
 // Split of each query tile's K/V range over CTAs, from the per-tile K/V tile
-// counts of a selection: chunk tiles per CTA, n_split CTAs per (tile, head).
-void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split);
+// counts of a selection: chunk tiles per CTA, n_split CTAs per (tile, head),
+// and which merge (kAttnMerge*) combines the splits.
+void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split,
+                        int* merge);
 // Scratch bytes of the split partials (0 = unsplit); never above
 // kAttnMaxSplitCTAs CTAs' worth.
 constexpr int kAttnMaxSplitCTAs = 4 * kNumSMs;

@@ -115,6 +115,20 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also ORs a predicate over its `count` threads: every
+// participant gets the same result.
+__device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 // Wait until *p >= target (acquire at GPU scope); false after the budget.
 __device__ __forceinline__ bool spin_ge_acquire(const int* p, int target, long long budget = kWaitLimitCycles) {
     auto ld = [&]() {
@@ -329,6 +343,25 @@ __device__ __forceinline__ void tmem_ld32x4(uint32_t taddr, float* v) {
                  "+r"(r[109]), "+r"(r[110]), "+r"(r[111]), "+r"(r[112]), "+r"(r[113]), "+r"(r[114]), "+r"(r[115]),
                  "+r"(r[116]), "+r"(r[117]), "+r"(r[118]), "+r"(r[119]), "+r"(r[120]), "+r"(r[121]), "+r"(r[122]),
                  "+r"(r[123]), "+r"(r[124]), "+r"(r[125]), "+r"(r[126]), "+r"(r[127])::"memory");
+}
+
+// One column of this thread's lane: store (waited) and load (waited).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "r"(v)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(v)
+        : "r"(taddr)
+        : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {

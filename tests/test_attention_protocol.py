@@ -11,9 +11,16 @@ completing in issue order per issuing thread:
              t - 1 - KS;
   QK issuer  S_j = Q K_j^T into score buffer j % SB once step j has landed
              and (j >= SB) the PV product of tile j - SB is done;
-  PV issuer  O += P_j V_j once P_j (p_full[j & 3]) and step j + 1 are there;
-  softmax    waits for S_j, sometimes for the previous PV (an O rescale),
-             writes P_j over S_j; at the end waits for the last PV.
+  PV issuer  O += P_j V_j once P_j (p_full[j & 3], one arrival from each
+             softmax half) and step j + 1 are there;
+  softmax    two halves (keys 0-63 and 64-127 of each tile): each waits for
+             S_j, reads its own half of the scores and meets the other half
+             at their pair barrier; when a row's running max is raised they
+             swap half-maxima (each writes its own last score column, they
+             meet again, each reads the other's); sometimes (an O rescale)
+             they wait for the previous PV; each writes its P over its own
+             scores and arrives; at the end the halves meet once more and the
+             first waits for the last PV.
 
 KS (ring stages) and SB (score buffers) are the kernel's kStages and kSBufs:
 3 and 3; the shallower 2 and 2 (a 64-key, two-CTAs-per-SM form, measured
@@ -23,7 +30,8 @@ other parity than the one asked for, so a waiter that falls two phases
 behind, or polls a phase two ahead, would be fooled: the model asserts that
 never happens, that no barrier is re-armed with a phase still open, and that
 no shared-memory slot or tensor-memory buffer is overwritten while a product
-or the softmax still reads it.  The variant without the producer's wait for
+or the softmax still reads it (a half's exchange column included), and that
+the pair barrier never leaves one half waiting for good.  The variant without the producer's wait for
 S_{t-KS} on the last (K-less) step is shown to alias (at KS = 3), which is
 why that wait is unconditional in the kernel.
 """
@@ -41,7 +49,9 @@ def simulate(n, seed, wait_s_on_last_step=True, KS=3, SB=3):
     kSBufs)."""
     R = random.Random(seed)
     done = {}                    # barrier -> completed phases
-    fin = {"QK": set(), "PV": set(), "P": set(), "land": set()}
+    fin = {"QK": set(), "PV": set(), "P": set(), "land": set(), "X": set()}
+    arrivals = {}                # tile -> softmax halves that stored their P
+    pair = {}                    # pair barrier round -> halves arrived
     tma, qk_q, pv_q = [], [], []
 
     def count(b):
@@ -82,6 +92,8 @@ def simulate(n, seed, wait_s_on_last_step=True, KS=3, SB=3):
                 while not poll(("o", (j - SB) & 3), (j - SB) >> 2):
                     yield
                 assert j - SB in fin["PV"] and j - SB in fin["P"], "score buffer reused too early"
+                if swaps[j - SB]:
+                    assert (j - SB, 0) in fin["X"] and (j - SB, 1) in fin["X"], "exchange column overwritten unread"
             qk_q.append(j)
             yield
 
@@ -95,23 +107,39 @@ def simulate(n, seed, wait_s_on_last_step=True, KS=3, SB=3):
             pv_q.append(j)
             yield
 
-    def softmax():
+    def meet(r):
+        pair[r] = pair.get(r, 0) + 1
+        while pair[r] < 2:
+            yield
+
+    swaps = [j == 0 or R.random() < 0.3 for j in range(n)]          # the same decisions in both halves
+    rescales = [j > 0 and swaps[j] and R.random() < 0.7 for j in range(n)]
+
+    def softmax(half):
         for j in range(n):
             while not poll(("s", j % SB), j // SB):
                 yield
             assert j in fin["QK"]
-            if j > 0 and R.random() < 0.3:   # an O rescale waits for the previous PV
+            yield from meet(("any", j))       # does some row raise its max?
+            if swaps[j]:
+                yield from meet(("swap", j))  # half-maxima written, then read
+                fin["X"].add((j, half))
+                yield
+            if rescales[j]:                   # an O rescale waits for the previous PV
                 while not poll(("o", (j - 1) & 3), (j - 1) >> 2):
                     yield
             assert j < SB or j - SB in fin["PV"], "P written over a P still being read"
-            fin["P"].add(j)
-            done[("p", j & 3)] = count(("p", j & 3)) + 1
+            arrivals[j] = arrivals.get(j, 0) + 1
+            if arrivals[j] == 2:
+                fin["P"].add(j)
+                done[("p", j & 3)] = count(("p", j & 3)) + 1
             yield
-        if n:
+        yield from meet(("sums", n))          # the second half's row sums
+        if n and half == 0:
             while not poll(("o", (n - 1) & 3), (n - 1) >> 2):
                 yield
 
-    roles = [producer(), qk_issuer(), pv_issuer(), softmax()]
+    roles = [producer(), qk_issuer(), pv_issuer(), softmax(0), softmax(1)]
     live = [True] * len(roles)
     for _ in range(200000):
         if not (any(live) or tma or qk_q or pv_q):
