@@ -33,6 +33,11 @@
  *   - KVR_PDL=0 in the environment (read once per process) turns off
  *     programmatic dependent launch between the kernels of a call; it
  *     changes how work is launched, never what it computes.
+ *   - KVR_ATTN_MERGE=cta|kernel and KVR_ATTN_CHUNK=C in the environment
+ *     (read by every kvr_select) narrow the attention's split choice, for
+ *     tests and tuning: the merge of split K/V ranges by the last CTA of each
+ *     query tile or by a merge kernel, and the K/V tiles per CTA.  At the same
+ *     chunk both merges give the same output bits.
  *   - KVR_FAULT in the environment (read at the start of every call) makes
  *     one host-side step fail, for tests of the error paths; no GPU fault is
  *     made.  "alloc" or "alloc:N": the device allocations of
