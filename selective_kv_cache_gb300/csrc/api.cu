@@ -446,6 +446,7 @@ bool alloc_fault() {
     if (t_fault.rfind("alloc:", 0) == 0) return t_alloc_count == std::atoi(t_fault.c_str() + 6);
     return false;
 }
+void pdl_disarm() { t_pdl_armed = false; }
 bool pdl_take() {
     const bool r = t_pdl_armed && pdl_enabled();
     t_pdl_armed = true;
@@ -693,6 +694,10 @@ kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* coun
                                            s),
                              "row gather");
     }
+    // the kernels that read this selection (plan, rows, masks) start after
+    // it is complete: the next launch waits for the whole stream, so no
+    // kernel ever reads the plan in its pre-wait part while it is written
+    pdl_disarm();
     sel.valid = true;
     c->sel = sel;
     if (n_rows_out) *n_rows_out = rows;

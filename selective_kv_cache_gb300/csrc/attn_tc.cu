@@ -162,15 +162,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
 
-    pdl_wait();   // Q rows and the cache rows written by the previous kernel
     // rows of this thread (softmax warps 2-5 and 7-10): m = 32 * (warp % 4) +
     // lane; warps 2-5 take keys 0-63 of each tile, warps 7-10 keys 64-127
     const int m = 32 * (warp & 3) + lane;
     const int p = m / G, gi = m % G;
     const int half = warp >= 7 ? 1 : 0;
     const bool row_valid = warp >= 2 && warp != 6 && m < P * G && p < nrows;
-    int g = umin;
-    if (row_valid) g = a.U[row0 + p];
     // K/V producer, steps t = 0 .. n_total: K_t and V_{t-1} on one barrier,
     // so K stays one tile ahead of V.  The ring slots are freed by the
     // signals the products already send: K_t replaces K_{t-3}, read by the
@@ -208,6 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     int t_prod = 0;
+    pdl_wait();   // Q rows and the cache rows written by the previous kernel
+    int g = umin;
+    if (row_valid) g = a.U[row0 + p];
     if (warp == 0 && lane == 0) {
         // P * G <= 128 rows of 128 bytes in each half (126 when G = 6)
         mbar_arrive_expect_tx(q_full, 2u * 128u * (uint32_t)(P * G));

@@ -265,6 +265,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // same call (false for a call's first launch; set by pdl_begin_call()).
 void pdl_begin_call();
 bool pdl_take();   // returns the current permission and grants it to later launches
+void pdl_disarm(); // the next launch waits for all earlier work of the stream
 
 // Host-side fault injection (KVR_FAULT, read by pdl_begin_call at the start
 // of every call): whether the named step fails in this call.  "alloc" counts
