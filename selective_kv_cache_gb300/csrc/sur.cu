@@ -26,6 +26,7 @@
 // it before reading what it wrote.
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <cmath>
 
 #include "kvr_internal.h"
@@ -334,7 +335,11 @@ __global__ void __launch_bounds__(1024) sur_finish_kernel(const float* __restric
 }
 
 // mean of the four largest scores of each unit (all of them below four)
-// one warp: the unit score of unit u (returned in every lane)
+// one warp: the unit score of unit u (returned in every lane).  Each lane
+// keeps the four largest of its strided share in descending order; five
+// butterfly steps merge the lanes' lists (the larger half of a bitonic
+// sequence, then two compare-exchange stages), so every lane ends with the
+// unit's four largest, summed largest first.
 __device__ float unit_score_warp(const float* __restrict__ scores, const int32_t* __restrict__ bounds, int u,
                                  int32_t* err) {
     const int lane = threadIdx.x & 31;
@@ -343,7 +348,6 @@ __device__ float unit_score_warp(const float* __restrict__ scores, const int32_t
         if (lane == 0) atomicOr(err, DEV_ERR_INDEX);
         return -INFINITY;
     }
-    // each lane keeps its own top four, then four rounds of warp max take the unit's
     float t[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     for (int i = b + lane; i < e; i += 32) {
         float v = scores[i];
@@ -356,24 +360,26 @@ __device__ float unit_score_warp(const float* __restrict__ scores, const int32_t
             }
         }
     }
-    float sum = 0.f;
-    const int n = min(4, e - b);
-    int head = 0;
-    for (int k = 0; k < n; ++k) {
-        float m = head < 4 ? t[head] : -INFINITY;
-        int who = lane;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
-            if (m2 > m || (m2 == m && w2 < who)) {
-                m = m2;
-                who = w2;
-            }
-        }
-        sum += m;
-        if (lane == who) ++head;
+    for (int o = 1; o < 32; o <<= 1) {
+        float p[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[k] = __shfl_xor_sync(0xffffffffu, t[k], o);
+        // t descending, p descending: max(t_k, p_{3-k}) holds the four largest
+        // of both as a bitonic sequence; sort it descending
+        float c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = fmaxf(t[k], p[3 - k]);
+        float x0 = fmaxf(c[0], c[2]), x2 = fminf(c[0], c[2]);
+        float x1 = fmaxf(c[1], c[3]), x3 = fminf(c[1], c[3]);
+        t[0] = fmaxf(x0, x1);
+        t[1] = fminf(x0, x1);
+        t[2] = fmaxf(x2, x3);
+        t[3] = fminf(x2, x3);
     }
+    const int n = min(4, e - b);
+    float sum = t[0];
+    for (int k = 1; k < n; ++k) sum += t[k];
     return sum / (float)n;
 }
 
@@ -539,78 +545,118 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
     // window [a, a + w) sums to C[a + w - 1] - C[a - 1].  The largest sum wins,
     // the earliest start on ties.
     if (s_partial >= 0) {
-        __shared__ double red[32];
-        __shared__ int redi[32];
         const int b = bounds[s_partial], e = bounds[s_partial + 1], w = s_w, len = e - b;
         double* cum = len <= kAdmitCumLen ? cum_smem : cum_ws;
-        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-        // One warp walks the unit in chunks of 32 (a unit is a few dozen to a
-        // few hundred tokens): r_max, then the prefix max of rho_s + s/16 and
-        // the prefix sum of u, with carries between chunks.  The other warps
-        // would only add double-precision scans over empty lanes.
-        if (wid == 0) {
-            double rmax = -INFINITY;
-            for (int t = lane; t < len; t += 32) rmax = fmax(rmax, (double)scores[b + t]);
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        // The double-precision pipe of this part is narrow, so the work is
+        // spread over the warps, in chunks of 32 tokens: r_max (a block max);
+        // each chunk's prefix max of rho_s + s/16; the chunks' carries (a
+        // prefix max over the chunk maxima, on one warp); u_t =
+        // exp(pm_t - t/16) per token; each chunk's prefix sum of u; the sums'
+        // carries, added chunk after chunk by one thread, so every C_t is
+        // (chunk prefix) + (sum of the earlier chunks' totals, first to last)
+        // and does not depend on how the chunks were spread.
+        const int nch = (len + 31) / 32, nw = blockDim.x >> 5;
+        __shared__ float s_cred[32];
+        __shared__ double s_carry[kAdmitCumLen / 32 + 1];
+        double* chunk = len <= kAdmitCumLen ? s_carry : cum_ws + len;   // per-chunk values
+        // r_max on the float pipe: a max of floats is exact, so widening it
+        // afterwards gives the same double as a max of widened scores.  Only
+        // warps with tokens in hand run double-precision work below.
+        float rm = -INFINITY;
+        for (int t = threadIdx.x; t < len; t += blockDim.x) rm = fmaxf(rm, scores[b + t]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) rmax = fmax(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
-            double pm_carry = -INFINITY, cs_carry = 0.0;
-            for (int base = 0; base < len; base += 32) {
-                const int t = base + lane;
-                const double ts = (double)t * 0.0625;   // t / 16, exactly
-                double pm = t < len ? ((double)scores[b + t] - rmax) + ts : -INFINITY;
+        for (int o = 16; o > 0; o >>= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
+        if (lane == 0) s_cred[wid] = rm;
+        __syncthreads();
+        float rmf = s_cred[0];
+        for (int k = 1; k < nw; ++k) rmf = fmaxf(rmf, s_cred[k]);
+        const double rmax = (double)rmf;
+        for (int c = wid; c < nch; c += nw) {   // chunk prefix max of rho_s + s/16
+            const int t = 32 * c + lane;
+            double pm = t < len ? ((double)scores[b + t] - rmax) + (double)t * 0.0625 : -INFINITY;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, pm, o);
+                if (lane >= o) pm = fmax(pm, y);
+            }
+            if (t < len) cum[t] = pm;
+            if (lane == 31) chunk[c] = pm;
+        }
+        __syncthreads();
+        if (wid == 0) {   // exclusive prefix max of the chunk maxima (max is exact in any order)
+            double carry = -INFINITY;
+            for (int c0 = 0; c0 < nch; c0 += 32) {
+                const int c = c0 + lane;
+                double v = c < nch ? chunk[c] : -INFINITY;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xffffffffu, pm, o);
-                    if (lane >= o) pm = fmax(pm, y);
+                    const double y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v = fmax(v, y);
                 }
-                pm = fmax(pm_carry, pm);
-                pm_carry = __shfl_sync(0xffffffffu, pm, 31);
-                double c = t < len ? exp(pm - ts) : 0.0;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double y = __shfl_up_sync(0xffffffffu, c, o);
-                    if (lane >= o) c += y;
-                }
-                c += cs_carry;
-                if (t < len) cum[t] = c;
-                cs_carry = __shfl_sync(0xffffffffu, c, 31);
+                const double prev = __shfl_up_sync(0xffffffffu, v, 1);
+                const double excl = lane == 0 ? carry : fmax(carry, prev);
+                carry = fmax(carry, __shfl_sync(0xffffffffu, v, 31));
+                __syncwarp();
+                if (c < nch) chunk[c] = excl;
             }
         }
         __syncthreads();
-        // best window start
-        double best = -INFINITY;
-        int best_a = 0;
-        for (int a0 = threadIdx.x; a0 + w <= len; a0 += blockDim.x) {
-            const double sum = cum[a0 + w - 1] - (a0 > 0 ? cum[a0 - 1] : 0.0);
-            if (sum > best) {   // a0 ascends per thread: the first maximiser stays
-                best = sum;
-                best_a = a0;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oa = __shfl_xor_sync(0xffffffffu, best_a, o);
-            if (ob > best || (ob == best && oa < best_a)) {
-                best = ob;
-                best_a = oa;
-            }
-        }
-        if (lane == 0) {
-            red[wid] = best;
-            redi[wid] = best_a;
+        for (int t = threadIdx.x; t < len; t += blockDim.x) {   // u_t = exp(max_{s<=t}(rho_s + s/16) - t/16)
+            const double pm = fmax(chunk[t >> 5], cum[t]);
+            cum[t] = exp(pm - (double)t * 0.0625);
         }
         __syncthreads();
+        for (int c = wid; c < nch; c += nw) {   // chunk prefix sums of u
+            const int t = 32 * c + lane;
+            double v = t < len ? cum[t] : 0.0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (t < len) cum[t] = v;
+            if (lane == 31) chunk[c] = v;   // the chunk's total
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {   // carries: the earlier chunks' totals, added first to last
+            double carry = 0.0;
+            for (int c = 0; c < nch; ++c) {
+                const double total = chunk[c];
+                chunk[c] = carry;
+                carry = total + carry;
+            }
+        }
+        __syncthreads();
+        for (int t = threadIdx.x; t < len; t += blockDim.x) cum[t] = cum[t] + chunk[t >> 5];
+        __syncthreads();
+        // best window start, on one warp: each window sum is mapped to a
+        // 64-bit key that orders as the double does (sign-magnitude to
+        // two's-complement order), so the comparisons stay on the integer
+        // pipe; the earliest start wins a tie
         __shared__ int s_ba;
-        if (threadIdx.x == 0) {
-            double bb = red[0];
-            int ba = redi[0];
-            for (int k = 1; k < nw; ++k)
-                if (red[k] > bb || (red[k] == bb && redi[k] < ba)) {
-                    bb = red[k];
-                    ba = redi[k];
+        if (wid == 0) {
+            unsigned long long best = 0ull;
+            int best_a = INT_MAX;
+            for (int a0 = lane; a0 + w <= len; a0 += 32) {
+                const double sum = cum[a0 + w - 1] - (a0 > 0 ? cum[a0 - 1] : 0.0);
+                const unsigned long long bits = (unsigned long long)__double_as_longlong(sum);
+                const unsigned long long key = (bits >> 63) ? ~bits : (bits | 0x8000000000000000ull);
+                if (best_a == INT_MAX || key > best) {   // a0 ascends per lane: the first maximiser stays
+                    best = key;
+                    best_a = a0;
                 }
-            s_ba = ba;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oa = __shfl_xor_sync(0xffffffffu, best_a, o);
+                if (ob > best || (ob == best && oa < best_a)) {
+                    best = ob;
+                    best_a = oa;
+                }
+            }
+            if (lane == 0) s_ba = best_a;
         }
         __syncthreads();
         // the window's bits, set in parallel (the whole units' bits are in other words
@@ -656,8 +702,8 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, bool tc, SurWs* L, uint8_
     off += al((size_t)n_units * sizeof(int32_t));
     const size_t o_sel = off;
     off += al((size_t)((S + 31) / 32) * sizeof(uint32_t));
-    const size_t o_cum = off;
-    off += al((size_t)S * sizeof(double));
+    const size_t o_cum = off;   // the envelope's prefix sums, then one value per 32-token chunk
+    off += al((size_t)(S + (S + 31) / 32 + 1) * sizeof(double));
     size_t o_eg = 0, o_qp = 0, o_en = 0, o_part = 0;
     if (tc) {
         const int S_pad = (S + 127) / 128 * 128;
