@@ -458,73 +458,96 @@ kvr_status cuda_fail(cudaError_t e, const char* what) {
     return KVR_ECUDA;
 }
 
-bool make_tmap_2d_bf16(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
-                       uint32_t box_inner, uint32_t box_rows, std::string* why) {
+namespace {
+// Encoded tensor maps, cached per thread: an encoding is a pure function of
+// its arguments, and a call re-encodes the same few maps for every launch.
+struct TmapKey {
+    int dtype, rank, l2;
+    const void* base;
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+};
+struct TmapSlot {
+    bool used;
+    TmapKey key;
+    CUtensorMap map;
+};
+constexpr int kTmapSlots = 256;
+thread_local TmapSlot t_tmaps[kTmapSlots];
+
+bool encode_cached(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                   const uint64_t* strides, const uint32_t* box, CUtensorMapL2promotion l2, const char* what,
+                   std::string* why) {
+    TmapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.dtype = (int)dtype;
+    k.rank = rank;
+    k.l2 = (int)l2;
+    k.base = base;
+    for (int i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    uint64_t h = 1469598103934665603ull;   // FNV-1a over the key's bytes
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(&k);
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+    TmapSlot& slot = t_tmaps[h % kTmapSlots];
+    if (slot.used && std::memcmp(&slot.key, &k, sizeof(k)) == 0) {
+        *out = slot.map;
+        return true;
+    }
     if (!get_encode(why)) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint64_t d[4], st[3];
+    cuuint32_t bx[4], es[4] = {1, 1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = g_encode(out, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled failed with " + std::to_string((int)r);
+        if (why) *why = std::string("cuTensorMapEncodeTiled") + what + " failed with " + std::to_string((int)r);
         return false;
     }
+    slot.used = true;
+    slot.key = k;
+    slot.map = *out;
     return true;
+}
+}  // namespace
+
+bool make_tmap_2d_bf16(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows, std::string* why) {
+    const uint64_t dims[2] = {inner, rows}, strides[1] = {row_stride_bytes};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_cached(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "", why);
 }
 
 bool make_tmap_3d_bf16(CUtensorMap* out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                        std::string* why) {
-    if (!get_encode(why)) return false;
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    cuuint32_t box[3] = {b0, b1, b2};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled failed with " + std::to_string((int)r);
-        return false;
-    }
-    return true;
+    const uint64_t dims[3] = {d0, d1, d2}, strides[2] = {stride1_bytes, stride2_bytes};
+    const uint32_t box[3] = {b0, b1, b2};
+    return encode_cached(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "", why);
 }
 
 bool make_tmap_4d_bf16(CUtensorMap* out, const void* base, const uint64_t dims_in[4], const uint64_t strides_bytes[3],
                        const uint32_t box_in[4], std::string* why) {
-    if (!get_encode(why)) return false;
-    cuuint64_t dims[4] = {dims_in[0], dims_in[1], dims_in[2], dims_in[3]};
-    cuuint64_t strides[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
-    cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled (4-d) failed with " + std::to_string((int)r);
-        return false;
-    }
-    return true;
+    return encode_cached(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims_in, strides_bytes, box_in,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, " (4-d)", why);
 }
 
 bool make_tmap_2d_f32_sw128(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
                             std::string* why) {
-    if (!get_encode(why)) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 4};
-    cuuint32_t box[2] = {32, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled (fp32 rows) failed with " + std::to_string((int)r);
-        return false;
-    }
-    return true;
+    const uint64_t dims[2] = {inner, rows}, strides[1] = {inner * 4};
+    const uint32_t box[2] = {32, box_rows};
+    return encode_cached(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, " (fp32 rows)", why);
 }
 
 kvr_status do_select(kvr_cache* c, const int32_t* positions, const int32_t* counts, int32_t budget_percent,

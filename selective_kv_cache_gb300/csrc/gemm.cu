@@ -42,6 +42,7 @@ struct GemmDev {
     // act[r][f] = silu(g) * u in bf16
     int swiglu_F;
     __nv_bfloat16* act;
+    int prefill;   // 1: the weights are written by no kernel of the call (their first tiles load before the wait)
 };
 
 // one lane polls, the whole warp follows with the result
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // of the first ring stages go out before the wait for the previous
             // kernel, whose outputs (the activation rows) are read after it.
             int pre = 0;
-            for (int item = blockIdx.x; item < g.items && pre < stages; item += gridDim.x) {
+            for (int item = blockIdx.x; g.prefill && item < g.items && pre < stages; item += gridDim.x) {
                 int m_t, n_t, split, kb0, kb1;
                 item_coords(g, item, m_t, n_t, split, kb0, kb1);
                 for (int kb = kb0; kb < kb1 && pre < stages; ++kb, ++pre) {
@@ -415,7 +416,7 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
 size_t gemm_partial_bytes(const GemmPlan& p) { return (size_t)p.splits * p.R * p.n_out * sizeof(float); }
 
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
-                        cudaStream_t s, std::string* why, void* act) {
+                        cudaStream_t s, std::string* why, void* act, bool w_written_before) {
     if (p.R <= 0) return cudaSuccess;
     if (dtype == KVR_F32) {
         dim3 grid(p.m_tiles, p.n_tiles, p.splits);
@@ -451,6 +452,7 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     g.atoms = p.atoms;
     g.swiglu_F = p.swiglu_F;
     g.act = (__nv_bfloat16*)act;
+    g.prefill = w_written_before ? 0 : 1;
     if (p.swiglu_F && (p.splits != 1 || !act || p.swiglu_F % 64 || p.n_out != 2 * p.swiglu_F)) {
         if (why) *why = "fused SwiGLU needs one K split and an output buffer";
         return cudaErrorInvalidValue;

@@ -176,8 +176,10 @@ struct GemmPlan {
 };
 GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
 size_t gemm_partial_bytes(const GemmPlan& p);
+// w_written_before: an earlier kernel of the call writes w, so its tiles are
+// loaded only after the wait for the previous kernel.
 cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void* x, float* part, int32_t* err,
-                        cudaStream_t s, std::string* why, void* act = nullptr);
+                        cudaStream_t s, std::string* why, void* act = nullptr, bool w_written_before = false);
 
 // Epilogues (sum split partials in split order, then the fused op).
 struct QkvEpi {

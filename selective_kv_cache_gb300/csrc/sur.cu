@@ -51,9 +51,9 @@ struct SurWs {
     uint32_t* sel;       // [ceil(S/32)]
     double* cum;         // [S] prefix sums of the envelope of the partial unit
     // bf16 embeddings: the scoring contraction on the tensor cores
-    __nv_bfloat16* eg;   // [S_pad][d] gathered suffix embedding rows (zero rows past S)
     __nv_bfloat16* qp;   // [3Q][d] normalised query rows as hi, mid and lo bf16 terms
-    float* enorm;        // [S] ||E[s_i]||
+    __nv_bfloat16* eg;   // [S_pad][d] gathered suffix embedding rows (zero rows past S)
+    float* enorm;        // [S] ||E[s_i]||, or -1 for a token that occurs in the query
     float* part;         // GEMM partials [splits][3Q][S_pad]
 };
 
@@ -248,10 +248,11 @@ __device__ void sur_qsplit(int j, const __nv_bfloat16* __restrict__ E, int vocab
 }
 
 // one warp per suffix token: its embedding row into eg (16-byte copies) and
-// its fp32 norm; rows S..S_pad-1 are zero
+// its fp32 norm, or -1 when the token occurs in the query; rows S..S_pad-1
+// are zero
 __device__ void sur_gather(int i, const __nv_bfloat16* __restrict__ E, int vocab, int d,
-                           const int32_t* __restrict__ sids, int S, int S_pad, __nv_bfloat16* __restrict__ eg,
-                           float* __restrict__ enorm, int32_t* err) {
+                           const int32_t* __restrict__ sids, int S, int S_pad, const int32_t* __restrict__ qids,
+                           int Q, __nv_bfloat16* __restrict__ eg, float* __restrict__ enorm, int32_t* err) {
     const int lane = threadIdx.x & 31;
     if (i >= S_pad) return;
     uint4* dst = reinterpret_cast<uint4*>(eg + (size_t)i * d);
@@ -277,7 +278,11 @@ __device__ void sur_gather(int i, const __nv_bfloat16* __restrict__ E, int vocab
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0 && i < S) enorm[i] = sqrtf(ss);
+    if (i >= S) return;
+    bool in_q = false;
+    for (int j = lane; j < Q; j += 32) in_q |= qids[j] == sids[i];
+    in_q = __any_sync(0xffffffffu, in_q);
+    if (lane == 0) enorm[i] = in_q ? -1.0f : sqrtf(ss);
 }
 
 // the query split (CTAs 0 .. Q-1, one per query token) and the suffix rows'
@@ -288,49 +293,58 @@ __global__ void __launch_bounds__(256) sur_prep_kernel(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ sids, int S, int S_pad,
                                                        __nv_bfloat16* __restrict__ eg, float* __restrict__ enorm,
                                                        int32_t* err) {
+    pdl_trigger();   // the projection after it reads nothing before its wait
     if ((int)blockIdx.x < Q) {
         sur_qsplit(blockIdx.x, E, vocab, d, qids, Q, qp, err);
     } else {
         const int i = (int)(blockIdx.x - Q) * 8 + (threadIdx.x >> 5);
-        sur_gather(i, E, vocab, d, sids, S, S_pad, eg, enorm, err);
+        sur_gather(i, E, vocab, d, sids, S, S_pad, qids, Q, eg, enorm, err);
     }
 }
 
-// scores from the GEMM partials: 32 suffix tokens per CTA, 32 threads per
-// token splitting the queries; consecutive threads take consecutive tokens
-// (coalesced), and every load of a thread is independent of the others
+// scores from the GEMM partials: 128 suffix tokens per CTA; lane l of warp w
+// takes tokens 4l..4l+3 (16-byte loads along the token axis) for the queries
+// j = w, w + 32, ...; the warps' maxima meet in shared memory.  Per query the
+// dot product sums (hi + mid) + lo per split, splits in order.
 __global__ void __launch_bounds__(1024) sur_finish_kernel(const float* __restrict__ part, int splits, int S, int S_pad,
                                                           int Q, const float* __restrict__ enorm,
-                                                          const int32_t* __restrict__ sids,
-                                                          const int32_t* __restrict__ qids, float* __restrict__ scores) {
-    __shared__ float red[32][33];
+                                                          float* __restrict__ scores) {
+    __shared__ float4 red[32][33];
     pdl_trigger();
     pdl_wait();
-    const int fl = threadIdx.x & 31, jg = threadIdx.x >> 5;
-    const int f = blockIdx.x * 32 + fl;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int f0 = blockIdx.x * 128 + 4 * lane;
     const size_t split_stride = (size_t)3 * Q * S_pad;
-    float best = -INFINITY;
-    if (f < S) {
-        for (int j = jg; j < Q; j += 32) {
-            float dot = 0.f;
-            for (int s = 0; s < splits; ++s) {
-                const float* p = part + s * split_stride + f;
-                dot += (p[(size_t)j * S_pad] + p[(size_t)(Q + j) * S_pad]) + p[(size_t)(2 * Q + j) * S_pad];
-            }
-            best = fmaxf(best, dot);
+    float4 best = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int j = w; j < Q; j += 32) {
+        float4 dot = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < splits; ++sp) {
+            const float* p = part + sp * split_stride + f0;
+            const float4 h = *reinterpret_cast<const float4*>(p + (size_t)j * S_pad);
+            const float4 m = *reinterpret_cast<const float4*>(p + (size_t)(Q + j) * S_pad);
+            const float4 l = *reinterpret_cast<const float4*>(p + (size_t)(2 * Q + j) * S_pad);
+            dot.x += (h.x + m.x) + l.x;
+            dot.y += (h.y + m.y) + l.y;
+            dot.z += (h.z + m.z) + l.z;
+            dot.w += (h.w + m.w) + l.w;
         }
+        best.x = fmaxf(best.x, dot.x);
+        best.y = fmaxf(best.y, dot.y);
+        best.z = fmaxf(best.z, dot.z);
+        best.w = fmaxf(best.w, dot.w);
     }
-    red[jg][fl] = best;
+    red[w][lane] = best;
     __syncthreads();
-    if (jg == 0 && f < S) {
+    if (threadIdx.x < 128) {
+        const int t = threadIdx.x, f = blockIdx.x * 128 + t;
+        float bv = -INFINITY;
 #pragma unroll 8
-        for (int g = 1; g < 32; ++g) best = fmaxf(best, red[g][fl]);
-        const int id = sids[f];
-        bool in_q = false;
-        for (int j = 0; j < Q && !in_q; ++j) in_q = qids[j] == id;
-        const float nr = enorm[f];
-        // a token of the query meets its own embedding: cosine exactly 1
-        scores[f] = in_q ? 1.25f : (nr > 0.f ? best / nr : 0.f);
+        for (int g = 0; g < 32; ++g) bv = fmaxf(bv, reinterpret_cast<const float*>(&red[g][t >> 2])[t & 3]);
+        if (f < S) {
+            const float nr = enorm[f];
+            // a token of the query meets its own embedding: cosine exactly 1
+            scores[f] = nr < 0.f ? 1.25f : (nr > 0.f ? bv / nr : 0.f);
+        }
     }
 }
 
@@ -792,17 +806,15 @@ kvr_status kvr_sur_select(const void* embed, int32_t vocab, int32_t d, int32_t d
         KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_prep_kernel, dim3((unsigned)(Q + (S_pad + 7) / 8)), dim3(256), 0, s,
                                            (const __nv_bfloat16*)embed, vocab, d, query_ids, Q, L.qp, suffix_ids, S,
                                            S_pad, L.eg, L.enorm, L.err));
-        // the projection fetches its first operand tiles before it waits for
-        // the previous kernel, and those tiles are the rows just gathered: it
-        // keeps plain stream order
-        pdl_begin_call();
+        // the projection's first operand is the rows just gathered, so it
+        // loads them only after its wait for the prep kernel
         const GemmPlan gp = plan_gemm(KVR_BF16, S_pad, d, 3 * Q);
         std::string why;
-        e = launch_gemm(KVR_BF16, gp, L.eg, L.qp, L.part, L.err, s, &why);
+        e = launch_gemm(KVR_BF16, gp, L.eg, L.qp, L.part, L.err, s, &why, nullptr, true);
         if (e != cudaSuccess) return cuda_fail(e, ("sur scoring " + why).c_str());
-        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_finish_kernel, dim3((unsigned)((S + 31) / 32)), dim3(1024), 0, s,
+        KVR_CHECK_LAUNCH_SUR(launch_kernel(sur_finish_kernel, dim3((unsigned)(S_pad / 128)), dim3(1024), 0, s,
                                            (const float*)L.part, gp.splits, S, S_pad, Q, (const float*)L.enorm,
-                                           suffix_ids, query_ids, scores));
+                                           scores));
     } else if (dtype == KVR_BF16) {
         sur_qnorm_kernel<__nv_bfloat16><<<Q, 256, 0, s>>>((const __nv_bfloat16*)embed, vocab, d, query_ids, L.qn,
                                                           L.err);

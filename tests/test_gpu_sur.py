@@ -124,3 +124,35 @@ def test_sur_validation_and_device_checks():
         kvr.kvr_sur_select(E, sids, q[:1], bounds, 101, 0, ws, pos)
     with pytest.raises(kvr.KvrError):
         kvr.kvr_sur_select(E, sids, q[:1], bounds, 50, 0, ws[:16], pos)
+
+
+def test_sur_tensor_core_path_out_of_range_suffix_ids():
+    """bf16 embeddings (the tensor-core path, whose prep kernel gathers the
+    suffix rows for the scoring projection): suffix ids outside the vocabulary
+    are reported (KVR_EDEVICE) and score as zero rows (cosine 0); every other
+    token's score matches the oracle's."""
+    vocab, d, S, Q = 300, 512, 700, 24
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    E = torch.randn(vocab, d, generator=g, device="cuda").to(torch.bfloat16)
+    rng = np.random.default_rng(12)
+    sids = rng.integers(0, vocab, S).astype(np.int32)
+    qids = wl.make_query_ids(vocab, Q, 13, sids, overlap=3)
+    bad = np.array([5, 131, 600, 699])
+    sids[bad] = [-3, vocab, vocab + 77, -1]
+    bounds = wl.make_unit_bounds(S, 14)
+    ws = torch.empty(kvr.kvr_sur_workspace_bytes(S, Q, d, len(bounds) - 1), dtype=torch.uint8, device="cuda")
+    pos = torch.empty(S, dtype=torch.int32, device="cuda")
+    sc = torch.empty(S, dtype=torch.float32, device="cuda")
+    kvr.kvr_sur_select(E, torch.from_numpy(sids).cuda(), torch.from_numpy(qids).cuda(), torch.from_numpy(bounds).cuda(),
+                       5, 0, ws, pos, sc)
+    with pytest.raises(kvr.KvrError) as e:
+        kvr.kvr_sur_status(ws)
+    assert e.value.status == kvr.KVR_EDEVICE
+    # the oracle on a table with one zero row appended, the bad ids pointing at it
+    Ew = np.concatenate([f64(E), np.zeros((1, d))])
+    s_ref = sids.copy()
+    s_ref[bad] = vocab
+    r_ref = OS.token_scores(Ew, s_ref, qids)
+    assert np.all(r_ref[bad] == 0.0)
+    np.testing.assert_allclose(f64(sc), r_ref, atol=2e-5, rtol=0)
