@@ -98,11 +98,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const Tin* __restrict__ in
 }
 
 // ------------------------------------------------------------------ QKV
-// one thread per (row, head, 8-pair chunk of the first half of head_dim)
+// one thread per (row, head, 8-pair chunk of the first half of head_dim).
+// The row's position and sequence and its rotary factors (a chain of two
+// loads) are written by no kernel of the call (a selection's last launch is
+// followed by one that waits for the whole stream), so they are loaded before
+// the wait for the projection; its partials, the bias and the norm weights
+// after it, all in one round trip.
 template <typename T>
-__global__ void epi_qkv_kernel(QkvEpi a) {
+__global__ void __launch_bounds__(256) epi_qkv_kernel(QkvEpi a) {
     pdl_trigger();
-    pdl_wait();
     const int dh = a.head_dim, half = dh / 2, chunks = half / 8;
     const int heads = a.n_q_heads + 2 * a.n_kv_heads;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -114,6 +118,21 @@ __global__ void epi_qkv_kernel(QkvEpi a) {
     const int n_qkv = heads * dh;
     const size_t split_stride = (size_t)a.R * n_qkv;
     const int f1 = hh * dh + c * 8, f2 = f1 + half;
+    const bool is_v = hh >= a.n_q_heads + a.n_kv_heads;
+    const int u = a.U[r];
+    const int seq = a.row_seq[r];
+    const bool u_ok = u >= 0 && u < a.capacity;
+    float2 cs[8];
+    if (!is_v && u_ok) {
+        const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)u * half + c * 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 e = rp[j];
+            cs[2 * j] = make_float2(e.x, e.y);
+            cs[2 * j + 1] = make_float2(e.z, e.w);
+        }
+    }
+    pdl_wait();
     float x1[8], x2[8];
     sum_parts8(a.part, split_stride, a.splits, (size_t)r * n_qkv + f1, x1);
     sum_parts8(a.part, split_stride, a.splits, (size_t)r * n_qkv + f2, x2);
@@ -144,15 +163,11 @@ __global__ void epi_qkv_kernel(QkvEpi a) {
             x2[j] = x2[j] * inv * w2[j];
         }
     }
-    const int u = a.U[r];
-    const int seq = a.row_seq[r];
-    if (u < 0 || u >= a.capacity) {
+    if (!u_ok) {
         atomicOr(a.err, DEV_ERR_INDEX);
         return;
     }
-    const bool is_v = hh >= a.n_q_heads + a.n_kv_heads;
     if (!is_v) {
-        const float2* cs = a.rope + (size_t)u * half + c * 8;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float2 e = cs[j];
