@@ -384,12 +384,16 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
     p.m_tiles = n_out / 128;
     p.n_tiles = std::max(1, (R + 255) / 256);
     p.BN = std::max(16, round_up((R + p.n_tiles - 1) / p.n_tiles, 16));
-    // K depth per pipeline stage: up to 4 swizzle atoms (256 elements, 512 B
-    // of each weight row), so each TMA round reads longer runs of every row
-    p.atoms = (K % (2 * kBK) == 0) ? 2 : 1;
-    const int KB = K / (kBK * p.atoms);
+    // K depth per pipeline stage: two swizzle atoms (128 elements, 256 B of
+    // each weight row), so each TMA round reads longer runs of every row, as
+    // long as the ring keeps at least three stages; wide row tiles (BN above
+    // ~160) take one atom per stage and a deeper ring instead (at BN = 224,
+    // five stages of 44 KB instead of two of 88 KB)
     const int tileB = p.BN * 128;
-    p.stages = std::min(8, (kSmemBudget - 1024 - 1024) / (p.atoms * (kTileABytes + tileB)));
+    const int ring = kSmemBudget - 1024 - 1024;
+    p.atoms = (K % (2 * kBK) == 0 && ring / (2 * (kTileABytes + tileB)) >= 3) ? 2 : 1;
+    const int KB = K / (kBK * p.atoms);
+    p.stages = std::min(8, ring / (p.atoms * (kTileABytes + tileB)));
     p.swiglu_F = 0;
     // K splits from a cost model fitted to measurements on GB300: one item
     // streams its (128 + BN) x (K / S) operand tiles at ~100 GB/s per SM, the
