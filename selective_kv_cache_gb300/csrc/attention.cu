@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <functional>
+#include <string>
 
 #include "kvr_internal.h"
 
@@ -39,9 +40,54 @@ size_t attention_scratch_bytes(int dtype, int n_split, int n_tiles, int n_kv_hea
 // KVR_ATTN_MERGE=cta|kernel allows one merge only (at the same chunk both
 // give the same output bits); KVR_ATTN_CHUNK=C fixes the chunk at C K/V tiles
 // when the split that makes stays within kAttnMaxSplitCTAs CTAs.
-// tile_kv[t] = K/V tiles of query tile t.
+// tile_kv[t] = K/V tiles of query tile t.  A candidate's dispatch is played
+// out only when a lower bound of its makespan leaves it a chance, and the
+// last few choices are kept per thread.
+namespace {
+// The last few choices, per thread: a selection with the same query-tile
+// geometry (and the same overrides) gets the same answer without the search.
+struct ChunkMemo {
+    int dtype = -1, heads = 0;
+    std::string env_merge, env_chunk;
+    std::vector<int> tile_kv;
+    int chunk = 0, n_split = 0, merge = 0;
+};
+constexpr int kChunkMemo = 8;
+thread_local ChunkMemo t_chunk_memo[kChunkMemo];
+thread_local int t_chunk_next = 0;
+void attention_chunking_search(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split,
+                               int* merge);
+}  // namespace
+
 void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split,
                         int* merge) {
+    const char* em = std::getenv("KVR_ATTN_MERGE");
+    const char* ec = std::getenv("KVR_ATTN_CHUNK");
+    const std::string env_merge = em ? em : "", env_chunk = ec ? ec : "";
+    for (const ChunkMemo& e : t_chunk_memo)
+        if (e.dtype == dtype && e.heads == n_kv_heads && e.env_merge == env_merge && e.env_chunk == env_chunk &&
+            e.tile_kv == tile_kv) {
+            *chunk = e.chunk;
+            *n_split = e.n_split;
+            *merge = e.merge;
+            return;
+        }
+    attention_chunking_search(dtype, tile_kv, n_kv_heads, chunk, n_split, merge);
+    ChunkMemo& e = t_chunk_memo[t_chunk_next];
+    t_chunk_next = (t_chunk_next + 1) % kChunkMemo;
+    e.dtype = dtype;
+    e.heads = n_kv_heads;
+    e.env_merge = env_merge;
+    e.env_chunk = env_chunk;
+    e.tile_kv = tile_kv;
+    e.chunk = *chunk;
+    e.n_split = *n_split;
+    e.merge = *merge;
+}
+
+namespace {
+void attention_chunking_search(int dtype, const std::vector<int>& tile_kv, int n_kv_heads, int* chunk, int* n_split,
+                               int* merge) {
     *chunk = 1 << 30;
     *n_split = 1;
     *merge = kAttnMergeLastCTA;
@@ -53,23 +99,39 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
     for (int v : tile_kv) max_kv = std::max(max_kv, v);
     std::vector<double> sm_free;
     std::greater<double> later;
+    auto cta_cost = [&](int C, int z, int v, int how) {
+        const int n = std::max(0, std::min(C, v - z * C));
+        const int live = (v + C - 1) / C;
+        double cost = n > 0 ? n + 6.0 : 0.3;
+        if (n > 0 && live > 1) cost += 1.0;
+        if (n > 0 && live > 1 && how == kAttnMergeLastCTA) cost += 2.0 + (z == 0 ? 2.5 * (live - 1) : 0.0);
+        return cost;
+    };
+    auto merge_cost = [&](int splits, int how) { return how == kAttnMergeKernel && splits > 1 ? 4.0 + 0.5 * splits : 0.0; };
+    // a lower bound of the makespan: no SM finishes before its longest CTA,
+    // nor before an even share of all the work
+    auto lower_bound = [&](int C, int splits, int how) {
+        double longest = 0.0, total = 0.0;
+        for (int z = 0; z < splits; ++z)
+            for (int v : tile_kv) {
+                const double c = cta_cost(C, z, v, how);
+                longest = std::max(longest, c);
+                total += c * n_kv_heads;
+            }
+        return std::max(longest, total / (kNumSMs * kAttnCTAsPerSM)) + merge_cost(splits, how);
+    };
     auto makespan = [&](int C, int splits, int how) {
         sm_free.assign(kNumSMs * kAttnCTAsPerSM, 0.0);
         for (int z = 0; z < splits; ++z)
-            for (int t = (int)tile_kv.size() - 1; t >= 0; --t)
+            for (int t = (int)tile_kv.size() - 1; t >= 0; --t) {
+                const double cost = cta_cost(C, z, tile_kv[t], how);
                 for (int y = 0; y < n_kv_heads; ++y) {
-                    const int v = tile_kv[t];
-                    const int n = std::max(0, std::min(C, v - z * C));
-                    const int live = (v + C - 1) / C;
-                    double cost = n > 0 ? n + 6.0 : 0.3;
-                    if (n > 0 && live > 1) cost += 1.0;
-                    if (n > 0 && live > 1 && how == kAttnMergeLastCTA) cost += 2.0 + (z == 0 ? 2.5 * (live - 1) : 0.0);
                     std::pop_heap(sm_free.begin(), sm_free.end(), later);
                     sm_free.back() += cost;
                     std::push_heap(sm_free.begin(), sm_free.end(), later);
                 }
-        const double t = *std::max_element(sm_free.begin(), sm_free.end());
-        return how == kAttnMergeKernel && splits > 1 ? t + 4.0 + 0.5 * splits : t;
+            }
+        return *std::max_element(sm_free.begin(), sm_free.end()) + merge_cost(splits, how);
     };
     const char* env_c = std::getenv("KVR_ATTN_CHUNK");
     const int fixed = env_c ? std::atoi(env_c) : 0;
@@ -85,6 +147,10 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
         for (int how : {kAttnMergeLastCTA, kAttnMergeKernel}) {
             if ((how == kAttnMergeLastCTA && !allow_cta) || (how == kAttnMergeKernel && !allow_kernel)) continue;
             if (splits == 1 && how == kAttnMergeKernel && allow_cta) continue;   // nothing to merge
+            // a candidate wins only below 0.98 of the best so far: play out its
+            // dispatch only when its lower bound leaves it a chance (the choice
+            // is the same as with every candidate played out)
+            if (lower_bound(C, splits, how) >= best * 0.98) continue;
             const double t = makespan(C, splits, how);
             if (t < best * 0.98) {
                 best = t;
@@ -96,6 +162,7 @@ void attention_chunking(int dtype, const std::vector<int>& tile_kv, int n_kv_hea
     }
     if (*n_split == 1) *chunk = 1 << 30;
 }
+}  // namespace
 
 void attention_tiling(int dtype, int n_q_heads, int n_kv_heads, int* rows_per_tile, int* keys_per_tile) {
     if (dtype == KVR_BF16) {
