@@ -190,21 +190,6 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(QkvEpi a) {
 
 // ------------------------------------------------------------------ O, gate/up, down
 template <typename T>
-__global__ void epi_residual_kernel(const float* __restrict__ part, int splits, int R, int d, const T* __restrict__ x,
-                                    float* __restrict__ h) {
-    pdl_trigger();
-    pdl_wait();
-    const long long i8 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (i8 >= (long long)R * d) return;
-    float v[8], xv[8];
-    sum_parts8(part, (size_t)R * d, splits, (size_t)i8, v);
-    load8<T>(x + i8, xv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] += xv[j];
-    store8<float>(h + i8, v);
-}
-
-template <typename T>
 __global__ void epi_swiglu_kernel(const float* __restrict__ part, int splits, int R, int F, T* __restrict__ act) {
     pdl_trigger();
     pdl_wait();
@@ -364,18 +349,6 @@ cudaError_t launch_epi_qkv(int dtype, const QkvEpi& a, cudaStream_t s) {
         KVR_LAUNCH(epi_qkv_kernel<__nv_bfloat16>, dim3(blocks_for(total, 256)), dim3(256), 0, s, a);
     else
         KVR_LAUNCH(epi_qkv_kernel<float>, dim3(blocks_for(total, 256)), dim3(256), 0, s, a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_epi_residual_f32(int dtype, const float* part, int splits, int R, int d, const void* x,
-                                    float* h_out, cudaStream_t s) {
-    const long long n = (long long)R * d / 8;
-    if (n <= 0) return cudaSuccess;
-    if (dtype == KVR_BF16)
-        KVR_LAUNCH(epi_residual_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d,
-                                                                              (const __nv_bfloat16*)x, h_out);
-    else
-        KVR_LAUNCH(epi_residual_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, d, (const float*)x, h_out);
     return cudaGetLastError();
 }
 

@@ -199,8 +199,6 @@ struct QkvEpi {
     int32_t* err;
 };
 cudaError_t launch_epi_qkv(int dtype, const QkvEpi& a, cudaStream_t s);
-cudaError_t launch_epi_residual_f32(int dtype, const float* part, int splits, int R, int d, const void* x,
-                                    float* h_out, cudaStream_t s);
 cudaError_t launch_epi_swiglu(int dtype, const float* part, int splits, int R, int F, void* act_out,
                               cudaStream_t s);
 cudaError_t launch_epi_down(int dtype, const float* part, int splits, int R, int d, const float* h, void* x_out,
