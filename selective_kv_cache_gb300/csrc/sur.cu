@@ -681,21 +681,26 @@ __global__ void __launch_bounds__(kAdmitThreads) sur_admit_kernel(const float* _
         }
     }
     __syncthreads();
-    // compaction: ascending positions from the bit mask
+    // compaction: ascending positions from the bit mask.  The words' prefix
+    // counts first (in the envelope's space, free by now), then one bit per
+    // thread: a set bit's rank is its word's prefix plus the set bits below it
+    int* wpre = W <= 2 * kAdmitCumLen ? reinterpret_cast<int*>(cum_smem) : reinterpret_cast<int*>(cum_ws);
     int pcarry = 0;
     for (int base = 0; base < W; base += blockDim.x) {
         const int w = base + threadIdx.x;
-        uint32_t word = w < W ? sel[w] : 0u;
+        const uint32_t word = w < W ? sel[w] : 0u;
         int total;
         const int incl = block_scan_incl(__popc(word), &total);
-        int k = pcarry + incl - __popc(word);
-        while (word) {
-            const int bit = __ffs(word) - 1;
-            if (k < B) positions[k] = suffix_start + w * 32 + bit;
-            ++k;
-            word &= word - 1u;
-        }
+        if (w < W) wpre[w] = pcarry + incl - __popc(word);
         pcarry += total;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < W * 32; i += blockDim.x) {
+        const uint32_t word = sel[i >> 5];
+        if ((word >> (i & 31)) & 1u) {
+            const int k = wpre[i >> 5] + __popc(word & ((1u << (i & 31)) - 1u));
+            if (k < B) positions[k] = suffix_start + i;
+        }
     }
 }
 
@@ -716,7 +721,7 @@ size_t sur_ws_layout(int S, int Q, int d, int n_units, bool tc, SurWs* L, uint8_
     off += al((size_t)n_units * sizeof(int32_t));
     const size_t o_sel = off;
     off += al((size_t)((S + 31) / 32) * sizeof(uint32_t));
-    const size_t o_cum = off;   // the envelope's prefix sums, then one value per 32-token chunk
+    const size_t o_cum = off;   // the envelope's prefix sums and one value per 32-token chunk; then the mask words' prefix counts
     off += al((size_t)(S + (S + 31) / 32 + 1) * sizeof(double));
     size_t o_eg = 0, o_qp = 0, o_en = 0, o_part = 0;
     if (tc) {
