@@ -74,7 +74,9 @@ Gemms plan_all(const kvr_model_desc& m, int R) {
     const int hqd = m.n_q_heads * m.head_dim;
     g.qkv = plan_gemm(m.dtype, (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, m.d_model, R);
     g.o = plan_gemm(m.dtype, m.d_model, hqd, R);
-    g.gu = plan_gemm(m.dtype, 2 * m.ffn_dim, m.d_model, R);
+    // unpaired: the fused SwiGLU takes whole K ranges, and paired items of
+    // the gate/up shape would leave the last round half empty
+    g.gu = plan_gemm(m.dtype, 2 * m.ffn_dim, m.d_model, R, false);
     // one K split: the gate/up projection writes silu(g) * u directly (no partials)
     if (m.dtype == KVR_BF16 && g.gu.splits == 1 && m.ffn_dim % 64 == 0) g.gu.swiglu_F = m.ffn_dim;
     g.down = plan_gemm(m.dtype, m.d_model, m.ffn_dim, R);

@@ -11,7 +11,10 @@
 // TMEM accumulator; four epilogue warps read TMEM (warp w reads lanes
 // 32*(w%4)..+31) and store fp32 partials.  Split-K spreads the few feature
 // tiles of a projection over all 152 SMs; the epilogue kernels reduce the
-// splits in a fixed order.
+// splits in a fixed order.  A little above 256 rows, one CTA can take both
+// row tiles of a feature tile (two products of N = BN per K step, side by
+// side in TMEM): each weight tile then crosses from L2 to one SM instead of
+// two, and a stage carries ~24 % fewer bytes per product.
 //
 // fp32 path: plain SIMT FFMA tiles (fp32 storage needs fp32 products).
 #include <cuda_bf16.h>
@@ -43,6 +46,13 @@ struct GemmDev {
     int swiglu_F;
     __nv_bfloat16* act;
     int prefill;   // 1: the weights are written by no kernel of the call (their first tiles load before the wait)
+    // Accumulator windows in tensor memory: even items use the columns
+    // 0 .. W - 1, odd items acc_base1 .. acc_base1 + W - 1 (W = NSUB * BN).
+    // When the two do not fit side by side (ovl = 1) they share the columns
+    // [acc_base1, W): the epilogue reads those first and releases them on
+    // ovl_free, so the next item's products start while it reads the rest.
+    uint32_t acc_base1;
+    int ovl;
 };
 
 // one lane polls, the whole warp follows with the result
@@ -51,8 +61,9 @@ __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity) {
 }
 
 
-// work item -> (feature tile, row tile, K range); row tiles of one feature tile
-// are consecutive items, so CTAs that run at the same time share weight tiles in L2
+// work item -> (feature tile, row group of NSUB row tiles, K range); row groups
+// of one feature tile are consecutive items, so CTAs that run at the same time
+// share weight tiles in L2
 __device__ __forceinline__ void item_coords(const GemmDev& g, int item, int& m_t, int& n_t, int& split, int& kb0,
                                             int& kb1) {
     n_t = item % g.n_tiles;
@@ -68,20 +79,26 @@ __device__ __forceinline__ void item_coords(const GemmDev& g, int item, int& m_t
 // ring runs across item boundaries, and the TMEM accumulator is double
 // buffered, so the epilogue of one item overlaps the main loop of the next.
 //
-// ATOMS (swizzle atoms per ring stage) is a compile-time constant so that the
-// MMA issue block is straight-line code: one elected lane issues the stage's
-// 4 * ATOMS instructions back to back from precomputed descriptors.  A single
-// thread's issue loop bounds narrow (N < 256) tiles, and runtime-shaped loops
-// around tcgen05.mma cost several times the issue time of the instructions.
-template <int ATOMS>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// ATOMS (swizzle atoms per ring stage) and NSUB (row tiles per item) are
+// compile-time constants so that the MMA issue block is straight-line code:
+// one elected lane issues the stage's 4 * ATOMS * NSUB instructions back to
+// back from precomputed descriptors.  A single thread's issue loop bounds
+// narrow (N < 256) tiles, and runtime-shaped loops around tcgen05.mma cost
+// several times the issue time of the instructions.
+//
+// At most 72 registers a thread: 448 x 72 leaves 33,280 of the SM's 65,536
+// registers, enough for one CTA of the row epilogues (512 threads x 64) to
+// start beside this CTA under dependent launch.
+template <int ATOMS, int NSUB>
+__global__ void __maxnreg__(72)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmDev g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int atoms = ATOMS;
     const int BN = g.BN, stages = g.stages;
-    const int tileB = BN * 128;                    // one atom of B
-    const int stA = atoms * kTileABytes, stB = atoms * tileB;
+    const int tileB = BN * 128;                    // one atom of one row tile of B
+    // a stage: ATOMS atoms of A, then for each atom the NSUB row tiles' atoms of B
+    const int stA = atoms * kTileABytes, stB = atoms * NSUB * tileB;
     uint8_t* sA = smem;
     uint8_t* sB = smem + (size_t)stages * stA;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)stages * stB);
@@ -89,9 +106,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* acc_full = empty + stages;   // [2]
     uint64_t* acc_empty = acc_full + 2;    // [2]
     uint64_t* mma_done = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* ovl_free = mma_done + 1;     // the shared columns of the last item's window are read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ovl_free + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t acc_stride = (uint32_t)g.tmem_cols / 2u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -103,6 +120,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_empty[b], kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(ovl_free, kEpiWarps);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -165,7 +183,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         load_a(s, kb, m_t);
                     }
                     for (int a = 0; a < atoms; ++a)
-                        tma_load_2d(sB + (size_t)s * stB + a * tileB, &tmB, &full[s], (kb * atoms + a) * kBK, n_t * BN);
+                        for (int j = 0; j < NSUB; ++j)
+                            tma_load_2d(sB + (size_t)s * stB + (a * NSUB + j) * tileB, &tmB, &full[s],
+                                        (kb * atoms + a) * kBK, (n_t * NSUB + j) * BN);
                 }
             }
             if (!ok) {  // let every copy still in flight land before the CTA exits
@@ -182,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t descA = sdesc_sw128(smem_u32(sA), 16, 1024);
         const uint64_t descB = sdesc_sw128(smem_u32(sB), 16, 1024);
         constexpr uint32_t atA16 = kTileABytes >> 4, stA16 = atoms * atA16;   // descriptor units (16 B)
-        const uint32_t atB16 = (uint32_t)tileB >> 4, stB16 = atoms * atB16;
+        const uint32_t atB16 = (uint32_t)tileB >> 4, stB16 = atoms * NSUB * atB16;
         const bool leader = elect_one();    // the same lane issues every MMA and commit
         int s = 0, local = 0;
         uint32_t phase = 0;
@@ -194,8 +214,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ok = false;
                 break;
             }
+            // overlapping windows: the previous item's shared columns are read
+            if (g.ovl && local > 0 && !warp_wait_all(ovl_free, (uint32_t)(local - 1) & 1u)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)ab * acc_stride;
+            const uint32_t d = tmem + (ab ? g.acc_base1 : 0u);
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!warp_wait_all(&full[s], phase)) {
                     ok = false;
@@ -210,8 +235,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int a = 0; a < atoms; ++a)
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
-                            mma_bf16(d, da + (uint64_t)(a * atA16 + 2 * kk), db + (uint64_t)(a * atB16 + 2 * kk),
-                                     idesc, (a > 0 || kk > 0) ? 1u : first);
+#pragma unroll
+                            for (int j = 0; j < NSUB; ++j)
+                                mma_bf16(d + (uint32_t)(j * BN), da + (uint64_t)(a * atA16 + 2 * kk),
+                                         db + (uint64_t)((a * NSUB + j) * atB16 + 2 * kk), idesc,
+                                         (a > 0 || kk > 0) ? 1u : first);
                     mma_commit(&empty[s]);
                 }
                 __syncwarp();
@@ -229,10 +257,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         warp_wait_all(mma_done, 0);
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;
-        // the warps of a lane quarter split its 16-column chunks between them
-        const int n_chunks = BN / 16, part = (warp - 2) >> 2, per = (n_chunks + kEpiPer - 1) / kEpiPer;
-        const int c_lo = 16 * min(n_chunks, part * per), c_hi = 16 * min(n_chunks, (part + 1) * per);
+        const int q = warp & 3, part = (warp - 2) >> 2;
+        const int W = NSUB * BN;   // accumulator columns (tokens) of an item
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int local = 0;
         for (int item = blockIdx.x; item < g.items; item += gridDim.x, ++local) {
@@ -248,55 +274,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int tok0 = n_t * BN;
-            const uint32_t src = tmem + lane_base + (uint32_t)ab * acc_stride;
-            if (!g.swiglu_F) {
-                // TMEM -> fp32 partials part[split][token][feature].  Lane l holds
-                // feature 4a + b (a = l / 4, b = l % 4) for 16 tokens; a 4 x 4
-                // transpose within each quad of lanes (two xor-shuffle stages)
-                // leaves lane l with features 4a..4a+3 of token 4i + b, stored
-                // as one 16-byte vector per 4 tokens.
-                const int b = lane & 3;
-                float* out = g.part + (size_t)split * g.R * g.n_out + m_t * 128 + q * 32 + (lane & ~3);
-                for (int c = c_lo; c < c_hi; c += 16) {
-                    float v[16];
-                    tmem_ld16(src + (uint32_t)c, v);
+            const int tok0 = n_t * W;
+            const uint32_t src = tmem + lane_base + (ab ? g.acc_base1 : 0u);
+            // the warps of a lane quarter split the 16-column chunks of [lo, hi) between them
+            auto drain = [&](int lo, int hi) {
+                const int n_chunks = (hi - lo) / 16, per = (n_chunks + kEpiPer - 1) / kEpiPer;
+                const int c_lo = lo + 16 * min(n_chunks, part * per), c_hi = lo + 16 * min(n_chunks, (part + 1) * per);
+                if (!g.swiglu_F) {
+                    // TMEM -> fp32 partials part[split][token][feature].  Lane l holds
+                    // feature 4a + b (a = l / 4, b = l % 4) for 16 tokens; a 4 x 4
+                    // transpose within each quad of lanes (two xor-shuffle stages)
+                    // leaves lane l with features 4a..4a+3 of token 4i + b, stored
+                    // as one 16-byte vector per 4 tokens.
+                    const int b = lane & 3;
+                    float* out = g.part + (size_t)split * g.R * g.n_out + m_t * 128 + q * 32 + (lane & ~3);
+                    for (int c = c_lo; c < c_hi; c += 16) {
+                        float v[16];
+                        tmem_ld16(src + (uint32_t)c, v);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float x0 = v[4 * i], x1 = v[4 * i + 1], x2 = v[4 * i + 2], x3 = v[4 * i + 3];
-                        float a0 = (b & 2) ? x0 : x2, a1 = (b & 2) ? x1 : x3;
-                        a0 = __shfl_xor_sync(0xffffffffu, a0, 2);
-                        a1 = __shfl_xor_sync(0xffffffffu, a1, 2);
-                        if (b & 2) { x0 = a0; x1 = a1; } else { x2 = a0; x3 = a1; }
-                        float c0 = (b & 1) ? x0 : x1, c1 = (b & 1) ? x2 : x3;
-                        c0 = __shfl_xor_sync(0xffffffffu, c0, 1);
-                        c1 = __shfl_xor_sync(0xffffffffu, c1, 1);
-                        if (b & 1) { x0 = c0; x2 = c1; } else { x1 = c0; x3 = c1; }
-                        const int tok = tok0 + c + 4 * i + b;
-                        if (tok < g.R) *reinterpret_cast<float4*>(out + (size_t)tok * g.n_out) = make_float4(x0, x1, x2, x3);
+                        for (int i = 0; i < 4; ++i) {
+                            float x0 = v[4 * i], x1 = v[4 * i + 1], x2 = v[4 * i + 2], x3 = v[4 * i + 3];
+                            float a0 = (b & 2) ? x0 : x2, a1 = (b & 2) ? x1 : x3;
+                            a0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+                            a1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+                            if (b & 2) { x0 = a0; x1 = a1; } else { x2 = a0; x3 = a1; }
+                            float c0 = (b & 1) ? x0 : x1, c1 = (b & 1) ? x2 : x3;
+                            c0 = __shfl_xor_sync(0xffffffffu, c0, 1);
+                            c1 = __shfl_xor_sync(0xffffffffu, c1, 1);
+                            if (b & 1) { x0 = c0; x2 = c1; } else { x1 = c0; x3 = c1; }
+                            const int tok = tok0 + c + 4 * i + b;
+                            if (tok < g.R) *reinterpret_cast<float4*>(out + (size_t)tok * g.n_out) = make_float4(x0, x1, x2, x3);
+                        }
+                    }
+                } else {
+                    // this warp's lanes 0-15 hold gate of features f0+16q.., lanes 16-31
+                    // the matching up.  For a column pair (2p, 2p+1) the gate lane takes
+                    // column 2p and the up lane column 2p+1; one exchange across the
+                    // half-warps hands each the other half of its pair.
+                    const bool up_lane = lane >= 16;
+                    const int f = m_t * 64 + q * 16 + (lane & 15);
+                    __nv_bfloat16* act = g.act + f;
+                    for (int c = c_lo; c < c_hi; c += 16) {
+                        float v[16];
+                        tmem_ld16(src + (uint32_t)c, v);
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            const float a = v[2 * p], b = v[2 * p + 1];
+                            const float r = __shfl_xor_sync(0xffffffffu, up_lane ? a : b, 16);
+                            const float gv = up_lane ? r : a, uv = up_lane ? b : r;
+                            const int tok = tok0 + c + 2 * p + (up_lane ? 1 : 0);
+                            const float y = gv / (1.0f + __expf(-gv)) * uv;
+                            if (tok < g.R) act[(size_t)tok * g.swiglu_F] = __float2bfloat16_rn(y);
+                        }
                     }
                 }
+            };
+            if (g.ovl) {   // the columns the next item's window shares first, then release them
+                // shared columns in this window's own numbering
+                const int sh_lo = ab ? 0 : (int)g.acc_base1, sh_hi = ab ? W - (int)g.acc_base1 : W;
+                drain(sh_lo, sh_hi);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ovl_free);
+                drain(0, sh_lo);
+                drain(sh_hi, W);
             } else {
-                // this warp's lanes 0-15 hold gate of features f0+16q.., lanes 16-31
-                // the matching up.  For a column pair (2p, 2p+1) the gate lane takes
-                // column 2p and the up lane column 2p+1; one exchange across the
-                // half-warps hands each the other half of its pair.
-                const bool up_lane = lane >= 16;
-                const int f = m_t * 64 + q * 16 + (lane & 15);
-                __nv_bfloat16* act = g.act + f;
-                for (int c = c_lo; c < c_hi; c += 16) {
-                    float v[16];
-                    tmem_ld16(src + (uint32_t)c, v);
-#pragma unroll
-                    for (int p = 0; p < 8; ++p) {
-                        const float a = v[2 * p], b = v[2 * p + 1];
-                        const float r = __shfl_xor_sync(0xffffffffu, up_lane ? a : b, 16);
-                        const float gv = up_lane ? r : a, uv = up_lane ? b : r;
-                        const int tok = tok0 + c + 2 * p + (up_lane ? 1 : 0);
-                        const float y = gv / (1.0f + __expf(-gv)) * uv;
-                        if (tok < g.R) act[(size_t)tok * g.swiglu_F] = __float2bfloat16_rn(y);
-                    }
-                }
+                drain(0, W);
             }
             tc_fence_before();
             __syncwarp();
@@ -365,11 +408,12 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
+GemmPlan plan_gemm(int dtype, int n_out, int K, int R, bool pair_rows) {
     GemmPlan p{};
     p.n_out = n_out;
     p.K = K;
     p.R = R;
+    p.n_sub = 1;
     if (dtype == KVR_F32) {
         p.m_tiles = (n_out + 63) / 64;
         p.n_tiles = (R + 63) / 64;
@@ -384,36 +428,42 @@ GemmPlan plan_gemm(int dtype, int n_out, int K, int R) {
     p.m_tiles = n_out / 128;
     p.n_tiles = std::max(1, (R + 255) / 256);
     p.BN = std::max(16, round_up((R + p.n_tiles - 1) / p.n_tiles, 16));
-    // K depth per pipeline stage: two swizzle atoms (128 elements, 256 B of
-    // each weight row), so each TMA round reads longer runs of every row, as
-    // long as the ring keeps at least three stages; wide row tiles (BN above
-    // ~160) take one atom per stage and a deeper ring instead (at BN = 224,
-    // five stages of 44 KB instead of two of 88 KB)
-    const int tileB = p.BN * 128;
-    const int ring = kSmemBudget - 1024 - 1024;
-    p.atoms = (K % (2 * kBK) == 0 && ring / (2 * (kTileABytes + tileB)) >= 3) ? 2 : 1;
-    const int KB = K / (kBK * p.atoms);
-    p.stages = std::min(8, ring / (p.atoms * (kTileABytes + tileB)));
     p.swiglu_F = 0;
+    // Row tiles per item: one, or (two row tiles of at most 160 rows) both
+    // row tiles of a feature tile in one CTA.  K depth per pipeline stage: two
+    // swizzle atoms (128 elements, 256 B of each weight row), so each TMA
+    // round reads longer runs of every row, as long as the ring keeps at
+    // least three stages; wide stages take one atom per stage and a deeper
+    // ring instead (at BN = 224, five stages of 44 KB instead of two of 88 KB).
     // K splits from a cost model fitted to measurements on GB300: one item
-    // streams its (128 + BN) x (K / S) operand tiles at ~100 GB/s per SM, the
-    // persistent grid runs ceil(items / 152) rounds, and every split adds an
-    // fp32 partial round trip of R x n_out at ~6 TB/s.
-    const int tiles = p.m_tiles * p.n_tiles;
-    int best = 1;
+    // streams its (128 + NSUB * BN) x (K / S) operand tiles at ~100 GB/s per
+    // SM, the persistent grid runs ceil(items / 152) rounds, and every split
+    // adds an fp32 partial round trip of R x n_out at ~6 TB/s.  A pairing
+    // must win by 3 %.
+    const int ring = kSmemBudget - 1024 - 1024;
     double best_t = 1e30;
-    const int max_split = std::max(1, std::min(KB / 2, 16));
-    for (int s = 1; s <= max_split; ++s) {
-        const long long items = (long long)tiles * s;
-        const long long rounds = (items + kNumSMs - 1) / kNumSMs;
-        const double t = (double)rounds * (128.0 + p.BN) * ((double)K / s) * 2.0 / 100e9 +
-                         2.0 * s * (double)R * n_out * 4.0 / 6e12;
-        if (t < best_t * 0.97) {
-            best_t = t;
-            best = s;
+    for (int ns = 1; ns <= 2; ++ns) {
+        if (ns == 2 && (!pair_rows || p.n_tiles % 2 != 0 || p.BN > 160)) continue;
+        const int stage1 = kTileABytes + ns * p.BN * 128;   // one atom of A and of the item's B
+        const int atoms = (K % (2 * kBK) == 0 && ring / (2 * stage1) >= 3) ? 2 : 1;
+        if (ns == 2 && atoms != 1) continue;
+        const int KB = K / (kBK * atoms);
+        const int tiles = p.m_tiles * (p.n_tiles / ns);
+        const int max_split = std::max(1, std::min(KB / 2, 16));
+        for (int s = 1; s <= max_split; ++s) {
+            const long long items = (long long)tiles * s;
+            const long long rounds = (items + kNumSMs - 1) / kNumSMs;
+            const double t = (double)rounds * (128.0 + ns * p.BN) * ((double)K / s) * 2.0 / 100e9 +
+                             2.0 * s * (double)R * n_out * 4.0 / 6e12;
+            if (t < best_t * 0.97) {
+                best_t = t;
+                p.splits = s;
+                p.n_sub = ns;
+                p.atoms = atoms;
+                p.stages = std::min(8, ring / (atoms * stage1));
+            }
         }
     }
-    p.splits = best;
     return p;
 }
 
@@ -449,10 +499,10 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
     g.R = p.R;
     g.BN = p.BN;
     g.m_tiles = p.m_tiles;
-    g.n_tiles = p.n_tiles;
+    g.n_tiles = p.n_tiles / p.n_sub;   // row groups
     g.splits = p.splits;
     g.stages = p.stages;
-    g.items = p.m_tiles * p.n_tiles * p.splits;
+    g.items = p.m_tiles * g.n_tiles * p.splits;
     g.atoms = p.atoms;
     g.swiglu_F = p.swiglu_F;
     g.act = (__nv_bfloat16*)act;
@@ -461,24 +511,37 @@ cudaError_t launch_gemm(int dtype, const GemmPlan& p, const void* w, const void*
         if (why) *why = "fused SwiGLU needs one K split and an output buffer";
         return cudaErrorInvalidValue;
     }
+    // two accumulator windows of W columns: side by side when they fit in
+    // the allocation, else at both ends of all 512 columns, sharing the
+    // columns [512 - W, W)
+    const int W = p.n_sub * p.BN;
     int cols = 32;
-    while (cols < 2 * p.BN) cols <<= 1;   // two accumulators
+    while (cols < 2 * W && cols < 512) cols <<= 1;
     g.tmem_cols = cols;
+    g.ovl = 2 * W > cols ? 1 : 0;
+    g.acc_base1 = g.ovl ? (uint32_t)(512 - W) : (uint32_t)cols / 2u;
     // alignment slack, pipeline ring, barriers (1 KB)
-    const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.BN * 128) + 1024;
+    const size_t smem = 1024 + (size_t)p.stages * p.atoms * (kTileABytes + p.n_sub * p.BN * 128) + 1024;
+    if (W > 512 || p.n_tiles % p.n_sub != 0 || (p.n_sub == 2 && p.atoms != 1) || p.n_sub > 2 ||
+        smem > (size_t)kSmemBudget) {
+        if (why) *why = "projection plan out of range";
+        return cudaErrorInvalidValue;
+    }
     static bool attr_set = false;
     if (!attr_set) {
-        for (auto* f : {gemm_bf16_tc_kernel<1>, gemm_bf16_tc_kernel<2>}) {
+        for (auto* f : {gemm_bf16_tc_kernel<1, 1>, gemm_bf16_tc_kernel<2, 1>, gemm_bf16_tc_kernel<1, 2>}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
             if (e != cudaSuccess) return e;
         }
         attr_set = true;
     }
     const unsigned grid = (unsigned)std::min(g.items, kNumSMs);
-    if (p.atoms == 2)
-        KVR_LAUNCH(gemm_bf16_tc_kernel<2>, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+    if (p.n_sub == 2)
+        KVR_LAUNCH((gemm_bf16_tc_kernel<1, 2>), dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+    else if (p.atoms == 2)
+        KVR_LAUNCH((gemm_bf16_tc_kernel<2, 1>), dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
     else
-        KVR_LAUNCH(gemm_bf16_tc_kernel<1>, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
+        KVR_LAUNCH((gemm_bf16_tc_kernel<1, 1>), dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, g);
     return cudaSuccess;
 }
 

@@ -172,9 +172,11 @@ cudaError_t launch_rmsnorm(int dtype, const void* in, int in_f32, const void* w,
 struct GemmPlan {
     int n_out, K, R;
     int m_tiles, n_tiles, BN, splits, stages, atoms;
+    int n_sub;      // row tiles of BN rows per work item (1, or 2 when a pair fits one CTA)
     int swiglu_F;   // > 0: gate/up projection with the SwiGLU fused (act output, no partials)
 };
-GemmPlan plan_gemm(int dtype, int n_out, int K, int R);
+// pair_rows: the plan may give one CTA both row tiles of a feature tile
+GemmPlan plan_gemm(int dtype, int n_out, int K, int R, bool pair_rows = true);
 size_t gemm_partial_bytes(const GemmPlan& p);
 // w_written_before: an earlier kernel of the call writes w, so its tiles are
 // loaded only after the wait for the previous kernel.

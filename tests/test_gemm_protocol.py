@@ -17,12 +17,20 @@ completing in issue order:
   epilogue   kEpiWarps warps, each waits acc_full[ab], reads its share and
              arrives on acc_empty[ab] (count kEpiWarps).
 
+With overlapping accumulator windows (two windows of more than half the
+tensor-memory columns, at both ends), every window holds the shared columns:
+the epilogue reads its share of those first and arrives on ovl_free (count
+kEpiWarps), then reads the rest; the MMA role waits, before item i's first
+product, for ovl_free's completion i - 1 as well as for acc_empty[ab].
+
 The first polls of empty and acc_empty ask for the phase before phase 0
 (parity 1 on a fresh barrier), which a fresh barrier reports complete.  The
 model asserts that no poll is fooled by a barrier two phases away, that no
 barrier is re-armed with a phase open, that a ring slot is refilled only
-after its product read it, and that an accumulator is overwritten only after
-every epilogue warp has read it.
+after its product read it, that an accumulator is overwritten only after
+every epilogue warp has read it and, with overlapping windows, that the
+shared columns are overwritten only after every epilogue warp has read the
+previous item's share of them.
 """
 import random
 
@@ -39,7 +47,7 @@ class Hazard(AssertionError):
     pass
 
 
-def simulate(item_kbs, stages, seed, wait_acc_empty=True):
+def simulate(item_kbs, stages, seed, wait_acc_empty=True, ovl=False, wait_ovl=True):
     R = random.Random(seed)
     total = sum(item_kbs)
     pre = min(stages, total)
@@ -48,6 +56,7 @@ def simulate(item_kbs, stages, seed, wait_acc_empty=True):
     fin = {"land": set(), "mma": set(), "drained": set()}
     tma, mma_q = [], []
     acc_reads = {}          # item -> epilogue warps that read it
+    shared_reads = {}       # item -> epilogue warps that read its shared columns
 
     def cnt(b):
         return done.get(b, 0)
@@ -92,8 +101,13 @@ def simulate(item_kbs, stages, seed, wait_acc_empty=True):
             if wait_acc_empty:
                 while not poll(("acc_empty", ab), (item >> 1) - 1):
                     yield
+            if ovl and wait_ovl and item > 0:
+                while not poll(("ovl_free",), item - 1):
+                    yield
             check(item < 2 or acc_reads.get(item - 2, 0) == K_EPI_WARPS,
                   "accumulator overwritten before the epilogue read it")
+            check(not ovl or item < 1 or shared_reads.get(item - 1, 0) == K_EPI_WARPS,
+                  "shared columns overwritten before the epilogue read them")
             for _ in range(kbs):
                 s = it % stages
                 while not poll(("full", s), it // stages):
@@ -111,6 +125,15 @@ def simulate(item_kbs, stages, seed, wait_acc_empty=True):
             while not poll(("acc_full", ab), item >> 1):
                 yield
             check(item in fin["drained"], "accumulator read before its products finished")
+            if ovl:
+                shared_reads[item] = shared_reads.get(item, 0) + 1
+                yield
+                key = ("ovl_free",)
+                arrivals[key] = arrivals.get(key, 0) + 1
+                if arrivals[key] == K_EPI_WARPS:
+                    arrivals[key] = 0
+                    done[key] = cnt(key) + 1
+                yield
             acc_reads[item] = acc_reads.get(item, 0) + 1
             yield
             key = ("acc_empty", ab)
@@ -170,6 +193,24 @@ def test_accumulator_reuse_without_its_wait_is_caught():
     for seed in range(200):
         try:
             simulate([1, 1, 1, 1, 1], 3, seed, wait_acc_empty=False)
+        except (Hazard, Alias):
+            hits += 1
+    assert hits > 0
+
+
+@pytest.mark.parametrize("stages", [3, 4, 8])
+def test_overlapping_windows_have_no_alias_deadlock_or_overwrite(stages):
+    R = random.Random(100 + stages)
+    for seed in range(150):
+        items = [R.randint(1, 6) for _ in range(R.randint(1, 6))]
+        simulate(items, stages, seed, ovl=True)
+
+
+def test_shared_columns_without_their_wait_are_caught():
+    hits = 0
+    for seed in range(200):
+        try:
+            simulate([1, 1, 1, 1, 1], 4, seed, ovl=True, wait_ovl=False)
         except (Hazard, Alias):
             hits += 1
     assert hits > 0
