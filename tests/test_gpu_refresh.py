@@ -241,6 +241,41 @@ def test_llama8b_full_size_against_oracle():
     s.close()
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("n_select", [289, 313])
+def test_llama8b_layer_with_paired_row_tiles(n_select):
+    """One Llama-3-8B-shaped layer (N = 7680) with 289 or 313 selected
+    positions: two row tiles of 160, which the QKV and down projections give
+    to one CTA together (two products of N = 160 per K step, accumulator
+    windows of 320 columns at both ends of tensor memory, sharing 128).  The
+    refreshed rows, the layer's K/V rows and the untouched rows against the
+    oracle, elementwise."""
+    base = wl.WORKLOADS["llama8b"]
+    w = dataclasses.replace(base, model=dataclasses.replace(base.model, n_layers=1), n_select=n_select)
+    s = Setup(w)
+    assert s.n_rows == n_select
+    Ks0, Vs0 = f64(s.K[0]), f64(s.V[0])
+    ids = s.ids.cpu().numpy()
+    U = oracle.sorted_positions(s.positions[0])
+    X_src = np.zeros((w.capacity, w.model.d_model))
+    X_src[U] = f64(s.embed[torch.from_numpy(ids[0][U].astype(np.int64)).cuda()])
+    K_in, V_in = s.K.clone(), s.V.clone()
+    s.select()
+    s.refresh()
+    s.sync()
+    X1, K1, V1, _, _ = oracle.refresh_packed(oracle_spec(w), LazyWeights(s.layers), Ks0, Vs0, s.local_mask[0],
+                                             s.sink_mask[0], U, X_src)
+    assert_close_rows(f64(s.hidden[:len(U)]), X1, TOL["bf16"], "refreshed rows")
+    Ut = torch.from_numpy(U)
+    assert_close(f64(s.K[0, 0][:, Ut]), K1[0][:, U], TOL["bf16"], "K layer 0")
+    assert_close(f64(s.V[0, 0][:, Ut]), V1[0][:, U], TOL["bf16"], "V layer 0")
+    keep = torch.ones(w.capacity, dtype=torch.bool, device=s.K.device)
+    keep[Ut.to(s.K.device)] = False
+    assert torch.equal(s.K[0][:, :, keep], K_in[0][:, :, keep])
+    assert torch.equal(s.V[0][:, :, keep], V_in[0][:, :, keep])
+    s.close()
+
+
 @pytest.mark.parametrize("sink_static", [False, True])
 def test_bf16_seven_query_heads_per_kv_head_block_seams(sink_static):
     """The block-seam geometry at the Qwen2.5-7B head grouping: 7 query heads
