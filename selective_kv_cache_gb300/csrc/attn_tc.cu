@@ -716,26 +716,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // same order (M the largest split max, L and the rows summed in split order
 // with products and sums rounded separately, splits with no visible key of
 // the row left out), so either merge writes the same bits.  Lane k holds
-// split k's (max, sum); the rows of the first eight splits are loaded with
-// them, so up to eight splits cost one load round trip.
-__global__ void __launch_bounds__(256) attn_merge_kernel(AttnLaunch a) {
-    pdl_wait();   // every split's rows are stored
-    pdl_trigger();
-    const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp_id >= (long long)a.n_tiles * a.n_kv_heads * 128) return;
-    const int m = (int)(warp_id & 127);
-    const int h = (int)((warp_id >> 7) % a.n_kv_heads);
-    const int tile = (int)((warp_id >> 7) / a.n_kv_heads);
-    const int G = a.n_q_heads / a.n_kv_heads;
-    const int p = m / G, gi = m % G;
-    const int* plan = a.plan + 8 * tile;
-    const int n_live = min(a.n_split, (plan[5] + a.chunk - 1) / a.chunk);
-    if (n_live <= 1 || m >= (128 / G) * G || p >= plan[1]) return;   // written by the attention, or no row
+// split k's (max, sum); the rows of the first four splits are loaded with
+// them, so up to four splits cost one load round trip.
+// plan0/1/5: the query tile's first row, row count and K/V tile count.
+__device__ __forceinline__ void merge_row(const AttnLaunch& a, int tile, int h, int m, int G, int lane, int plan0,
+                                          int plan1, int plan5) {
+    const int p = m / G, gi = m - p * G;
+    const int n_live = min(a.n_split, (plan5 + a.chunk - 1) / a.chunk);
+    if (n_live <= 1 || m >= (128 / G) * G || p >= plan1) return;   // written by the attention, or no row
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
     const float4* rows = reinterpret_cast<const float4*>(a.part_o);
     auto row_of = [&](int sp) { return (((size_t)sp * a.n_tiles + tile) * a.n_kv_heads + h) * 128 + m; };
-    constexpr int kGroup = 8;
+    constexpr int kGroup = 4;
     float4 v[kGroup];
 #pragma unroll
     for (int k = 0; k < kGroup; ++k)
@@ -792,11 +784,37 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(AttnLaunch a) {
         }
     }
     const float inv = 1.0f / L;
-    __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan[0] + p) * a.n_q_heads + h * G + gi) * 128;
+    __nv_bfloat16* out = (__nv_bfloat16*)a.out + ((size_t)(plan0 + p) * a.n_q_heads + h * G + gi) * 128;
     uint2 o;
     o.x = pack_bf16(acc.x * inv, acc.y * inv);
     o.y = pack_bf16(acc.z * inv, acc.w * inv);
     reinterpret_cast<uint2*>(out)[lane] = o;
+}
+
+// Grid (16, K/V heads, query tiles up to 65,535, walked beyond): block x of a
+// (tile, head) holds its rows 8x..8x+7, one a warp, so no thread divides
+// its index into (tile, head, row).  Four splits per load group keep it at
+// 48 registers, five CTAs an SM (the Llama-shaped selection's 1152 CTAs in
+// 1.5 waves instead of 1.9); the first tile's plan (written by the
+// selection, before any kernel of this call) is read before the wait for
+// the attention.
+__global__ void __launch_bounds__(256, 5) attn_merge_kernel(AttnLaunch a) {
+    const int m = (int)blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+    const int G = a.n_q_heads / a.n_kv_heads;
+    int tile = blockIdx.z;
+    const int* plan = a.plan + 8 * tile;
+    int plan0 = plan[0], plan1 = plan[1], plan5 = plan[5];
+    pdl_wait();   // every split's rows are stored
+    pdl_trigger();
+    while (true) {
+        merge_row(a, tile, (int)blockIdx.y, m, G, (int)(threadIdx.x & 31), plan0, plan1, plan5);
+        tile += gridDim.z;
+        if (tile >= a.n_tiles) break;
+        plan = a.plan + 8 * tile;
+        plan0 = plan[0];
+        plan1 = plan[1];
+        plan5 = plan[5];
+    }
 }
 
 }  // namespace
@@ -859,10 +877,9 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s, std::string
         KVR_LAUNCH(attn_tc_kernel<true>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
     else
         KVR_LAUNCH(attn_tc_kernel<false>, grid, dim3(kThreads), (size_t)kSmemBytes, s, tk, tv, tq, tp, b);
-    if (n_split > 1 && b.merge == kAttnMergeKernel) {
-        const long long threads = (long long)a.n_tiles * a.n_kv_heads * 128 * 32;
-        KVR_LAUNCH(attn_merge_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, b);
-    }
+    if (n_split > 1 && b.merge == kAttnMergeKernel)
+        KVR_LAUNCH(attn_merge_kernel, dim3(16, (unsigned)a.n_kv_heads, (unsigned)std::min(a.n_tiles, 65535)), dim3(256),
+                   0, s, b);
     return cudaSuccess;
 }
 
