@@ -189,13 +189,14 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(QkvEpi a) {
 }
 
 // ------------------------------------------------------------------ O, gate/up, down
+// grid (rows, blocks of 256 8-wide chunks of the row)
 template <typename T>
 __global__ void epi_swiglu_kernel(const float* __restrict__ part, int splits, int R, int F, T* __restrict__ act) {
     pdl_trigger();
     pdl_wait();
-    const long long i8 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (i8 >= (long long)R * F) return;
-    const int r = (int)(i8 / F), f = (int)(i8 % F);
+    const int r = (int)blockIdx.x, f = ((int)blockIdx.y * 256 + (int)threadIdx.x) * 8;
+    if (f >= F) return;
+    const size_t i8 = (size_t)r * F + f;
     const size_t stride = (size_t)R * 2 * F;
     float g[8], u[8];
     sum_parts8(part, stride, splits, (size_t)r * 2 * F + f, g);
@@ -353,13 +354,12 @@ cudaError_t launch_epi_qkv(int dtype, const QkvEpi& a, cudaStream_t s) {
 }
 
 cudaError_t launch_epi_swiglu(int dtype, const float* part, int splits, int R, int F, void* act_out, cudaStream_t s) {
-    const long long n = (long long)R * F / 8;
-    if (n <= 0) return cudaSuccess;
+    if (R <= 0 || F <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)R, blocks_for(F / 8, 256));
     if (dtype == KVR_BF16)
-        KVR_LAUNCH(epi_swiglu_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, F,
-                                                                            (__nv_bfloat16*)act_out);
+        KVR_LAUNCH(epi_swiglu_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, part, splits, R, F, (__nv_bfloat16*)act_out);
     else
-        KVR_LAUNCH(epi_swiglu_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, s, part, splits, R, F, (float*)act_out);
+        KVR_LAUNCH(epi_swiglu_kernel<float>, grid, dim3(256), 0, s, part, splits, R, F, (float*)act_out);
     return cudaGetLastError();
 }
 
