@@ -8,8 +8,8 @@
 // small activation tile is re-read from L2.  Both operands are K-major bf16
 // tiles of 64 elements (128 B) staged by TMA with 128-byte swizzle into a
 // multi-stage shared-memory ring; one thread issues tcgen05.mma into an fp32
-// TMEM accumulator; four epilogue warps read TMEM (warp w reads lanes
-// 32*(w%4)..+31) and store fp32 partials.  Split-K spreads the few feature
+// TMEM accumulator; twelve epilogue warps, three per TMEM lane quarter (warp
+// w reads lanes 32*(w%4)..+31), read it and store fp32 partials.  Split-K spreads the few feature
 // tiles of a projection over all 152 SMs; the epilogue kernels reduce the
 // splits in a fixed order.  A little above 256 rows, one CTA can take both
 // row tiles of a feature tile (two products of N = BN per K step, side by
@@ -46,8 +46,9 @@ struct GemmDev {
     int swiglu_F;
     __nv_bfloat16* act;
     int prefill;   // 1: the weights are written by no kernel of the call (their first tiles load before the wait)
-    // Accumulator windows in tensor memory: even items use the columns
-    // 0 .. W - 1, odd items acc_base1 .. acc_base1 + W - 1 (W = NSUB * BN).
+    // Accumulator windows in tensor memory: a CTA's 1st, 3rd, ... item uses
+    // the columns 0 .. W - 1, its 2nd, 4th, ... acc_base1 .. acc_base1 + W - 1
+    // (W = NSUB * BN).
     // When the two do not fit side by side (ovl = 1) they share the columns
     // [acc_base1, W): the epilogue reads those first and releases them on
     // ovl_free, so the next item's products start while it reads the rest.
