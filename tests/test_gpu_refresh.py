@@ -242,12 +242,14 @@ def test_llama8b_full_size_against_oracle():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("n_select", [289, 313])
+@pytest.mark.parametrize("n_select", [257, 289, 313, 320])
 def test_llama8b_layer_with_paired_row_tiles(n_select):
-    """One Llama-3-8B-shaped layer (N = 7680) with 289 or 313 selected
-    positions: two row tiles of 160, which the QKV and down projections give
-    to one CTA together (two products of N = 160 per K step, accumulator
-    windows of 320 columns at both ends of tensor memory, sharing 128).  The
+    """One Llama-3-8B-shaped layer (N = 7680) whose selection the QKV and
+    down projections split into two row tiles given to one CTA together (two
+    products of N = BN per K step, two accumulator windows at both ends of
+    tensor memory sharing their middle columns): 257 rows (tiles of 144, the
+    second holding one row; windows of 288 sharing 64), 289 and 313 (tiles of
+    160; windows of 320 sharing 128) and 320 (two full tiles of 160).  The
     refreshed rows, the layer's K/V rows and the untouched rows against the
     oracle, elementwise."""
     base = wl.WORKLOADS["llama8b"]
